@@ -1,0 +1,161 @@
+"""Host-side block pool: the control plane that produces block tables and
+slot mappings for the device calls.  It is not on the hot path.
+
+Behaviour follows the pages:
+
+* free blocks sit in a FIFO queue; a request takes blocks from the front and
+  a released block goes to the back ("vLLM PagedAttention: from memory
+  fragmentation to slot mapping" §4 timeline; "vLLM source walkthrough" §1.4);
+* taking blocks is all-or-nothing: when the pool cannot cover the request,
+  ``MemoryError`` is raised and no state changes (same page, §4: a failed
+  grow must leave the free list and the tables untouched);
+* every block carries a reference count; a sequence that shares another's
+  full prefix blocks increments their counts, and a block returns to the free
+  queue only when its count drops to zero ("vLLM source walkthrough" §1.6;
+  first page §5);
+* position p of a sequence lives in slot table[p // B] * B + p % B
+  (first page §3).
+
+Copy-on-write of a shared, partly filled tail block is refused here with
+``SharedTailWrite``: the device copy that would resolve it is a later step.
+"""
+from __future__ import annotations
+
+from collections import deque
+from typing import Hashable, Iterable, Sequence
+
+
+class SharedTailWrite(RuntimeError):
+    """A write would land in a block whose reference count is above one."""
+
+
+class BlockPool:
+    def __init__(self, num_blocks: int, block_size: int,
+                 free_order: Iterable[int] | None = None):
+        if num_blocks <= 0 or block_size <= 0:
+            raise ValueError("num_blocks and block_size must be positive")
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        order = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
+        if sorted(order) != list(range(num_blocks)):
+            raise ValueError("free_order must be a permutation of range(num_blocks)")
+        self.free_queue: deque[int] = deque(order)
+        self.ref_cnt = [0] * self.num_blocks
+        self.tables: dict[Hashable, list[int]] = {}
+        self.lengths: dict[Hashable, int] = {}
+
+    # -- capacity ------------------------------------------------------------
+    def blocks_for(self, num_tokens: int) -> int:
+        return -(-int(num_tokens) // self.block_size)
+
+    @property
+    def num_free(self) -> int:
+        return len(self.free_queue)
+
+    def _take_fresh(self, count: int) -> list[int]:
+        if count < 0:
+            raise ValueError("negative block count")
+        if count > len(self.free_queue):
+            raise MemoryError(f"need {count} blocks, {len(self.free_queue)} free")
+        fresh = [self.free_queue.popleft() for _ in range(count)]
+        for b in fresh:
+            self.ref_cnt[b] = 1
+        return fresh
+
+    # -- sequence lifecycle --------------------------------------------------
+    def add(self, seq: Hashable, num_tokens: int, prefix_of: Hashable | None = None,
+            prefix_tokens: int = 0) -> list[int]:
+        """Register ``seq`` with ``num_tokens`` tokens.  With ``prefix_of``,
+        the first ``prefix_tokens`` (a multiple of B, at most both lengths)
+        reuse that sequence's full blocks instead of fresh ones."""
+        if seq in self.tables:
+            raise KeyError(f"sequence {seq!r} already present")
+        shared: list[int] = []
+        if prefix_of is not None:
+            if prefix_tokens % self.block_size:
+                raise ValueError("a shared prefix must cover whole blocks")
+            if prefix_tokens > min(num_tokens, self.lengths[prefix_of]):
+                raise ValueError("prefix longer than one of the sequences")
+            shared = self.tables[prefix_of][: prefix_tokens // self.block_size]
+        fresh = self._take_fresh(self.blocks_for(num_tokens) - len(shared))
+        for b in shared:
+            self.ref_cnt[b] += 1
+        self.tables[seq] = list(shared) + fresh
+        self.lengths[seq] = int(num_tokens)
+        return self.tables[seq]
+
+    def grow(self, seq: Hashable, new_tokens: int) -> list[int]:
+        """Append ``new_tokens`` positions; returns the blocks taken for them."""
+        old_len = self.lengths[seq]
+        table = self.tables[seq]
+        if new_tokens > 0 and old_len % self.block_size:
+            tail = table[-1]
+            if self.ref_cnt[tail] > 1:
+                raise SharedTailWrite(f"block {tail} is shared (ref_cnt {self.ref_cnt[tail]})")
+        extra = self.blocks_for(old_len + new_tokens) - len(table)
+        fresh = self._take_fresh(max(extra, 0))
+        table.extend(fresh)
+        self.lengths[seq] = old_len + int(new_tokens)
+        return fresh
+
+    def release(self, seq: Hashable) -> list[int]:
+        """Drop ``seq``; blocks whose count reaches zero rejoin the free queue
+        in table order.  Returns those blocks."""
+        table = self.tables.pop(seq)
+        del self.lengths[seq]
+        freed = []
+        for b in table:
+            self.ref_cnt[b] -= 1
+            if self.ref_cnt[b] < 0:
+                raise AssertionError(f"block {b} released more often than acquired")
+            if self.ref_cnt[b] == 0:
+                freed.append(b)
+        self.free_queue.extend(freed)
+        return freed
+
+    # -- addressing ----------------------------------------------------------
+    def slot(self, seq: Hashable, position: int) -> int:
+        if not 0 <= position < self.lengths[seq]:
+            raise IndexError(position)
+        return slot_of(self.tables[seq], self.block_size, position)
+
+    def slots(self, seq: Hashable, start: int, count: int) -> list[int]:
+        return [self.slot(seq, p) for p in range(start, start + count)]
+
+    def table_rows(self, seqs: Sequence[Hashable], width: int | None = None) -> list[list[int]]:
+        """Tables of ``seqs`` padded with -1 to ``width`` entries."""
+        width = max((len(self.tables[s]) for s in seqs), default=0) if width is None else width
+        rows = []
+        for s in seqs:
+            t = self.tables[s]
+            if len(t) > width:
+                raise ValueError(f"table of {s!r} has {len(t)} entries > width {width}")
+            rows.append(t + [-1] * (width - len(t)))
+        return rows
+
+    # -- statistics ----------------------------------------------------------
+    def unique_blocks(self) -> int:
+        return sum(1 for c in self.ref_cnt if c > 0)
+
+    def live_tokens(self) -> int:
+        """Distinct token positions held: a shared prefix block counts once."""
+        seen: dict[int, int] = {}
+        for s, t in self.tables.items():
+            n = self.lengths[s]
+            for lb, b in enumerate(t):
+                filled = min(self.block_size, n - lb * self.block_size)
+                seen[b] = max(seen.get(b, 0), filled)
+        return sum(seen.values())
+
+    def utilization(self) -> float:
+        """live tokens / (allocated blocks * B)  (nxmr.cn article §5.2)."""
+        used = self.unique_blocks()
+        return self.live_tokens() / (used * self.block_size) if used else 1.0
+
+
+def slot_of(table: Sequence[int], block_size: int, position: int) -> int:
+    """slot = table[p // B] * B + p % B for one position of one table."""
+    physical = int(table[position // block_size])
+    if physical < 0:
+        raise IndexError(f"position {position} maps to a padding entry")
+    return physical * block_size + position % block_size
