@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Benchmark: one step = pa_write_kv of the step's new tokens + pa_decode of
+the whole batch (every row of the hot path), on synthetic inputs resident in
+HBM.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mha|gqa|long|cb]
+                    [--impl ours|reference] [--partition P]
+
+Metric: paged-decode KV GB/s = algorithmic bytes of the step / step time;
+also % of the measured HBM peak and decode tokens/s per layer (sequences
+decoded per second).  For N > 1 (torchrun) every rank runs its own replica
+of the batch (the path shards by sequence with no exchange): value is the
+sum over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_109_gb300 import workloads  # noqa: E402
+
+METRIC = "paged decode KV GB/s and % of GB300 HBM peak; decode tokens/s per layer"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_TEXT = {
+    "mha": "MHA decode bf16: 32 seqs, Hq=Hkv=32, D=128, B=16, T~U[128,2048], 8192-block "
+           "shuffled pool; step = write 1 new token per seq + decode",
+    "gqa": "GQA decode bf16: 128 seqs, Hq=32, Hkv=8, D=128, B=16, T~lognormal(median 1024, "
+           "sigma 1) cap 8192, 32 seqs share a 512-token prefix; 65536-block pool; "
+           "step = write 1 new token per seq + decode",
+    "long": "long-context GQA decode bf16: 4 seqs x 131072, Hq=64, Hkv=8, D=128, B=32, "
+            "16384-block pool; step = write 1 new token per seq + split-K decode + merge",
+    "cb": "continuous batching bf16: 256 seqs, Hq=32, Hkv=8, D=128, B=16, T0~U[1,4096]; "
+          "step = write 2304 tokens (1 per seq + 2048-token chunk) + decode all 256; "
+          "10 distinct steps cycled",
+}
+
+
+# ---- byte model ---------------------------------------------------------------
+
+def step_bytes(wl, k: int, split_traffic: bool = True) -> dict:
+    """Algorithmic bytes of step k (see the design notes for the model).
+    With ``split_traffic`` the split-K partial write + read of the library's
+    automatic partition size is included (asks libpa.so for that size)."""
+    st = wl.steps[k]
+    e = wl.elem_bytes
+    row = wl.head_dim * e
+    per_tok = 2 * wl.num_kv_heads * row                 # K + V of one token, one layer
+    lens = st.seq_lens.to(torch.int64)
+    logical_kv = int(lens.sum()) * per_tok
+    # unique: each physical block's valid rows counted once (shared prefix)
+    bs = wl.block_size
+    seen = {}
+    for i, t in enumerate(lens.tolist()):
+        for lb in range(-(-t // bs)):
+            b = int(st.block_tables[i, lb])
+            seen[b] = max(seen.get(b, 0), min(bs, t - lb * bs))
+    unique_kv = sum(seen.values()) * per_tok
+    n, hq = st.q.shape[0], wl.num_q_heads
+    q_out = 2 * n * hq * row
+    tables = sum(-(-t // bs) for t in lens.tolist()) * 4 + n * 4
+    split, ws, part = 0, 0, None
+    if split_traffic:
+        import paged_kv_cache_109_gb300 as pa
+        ws = pa.decode_workspace_bytes(n, hq, int(lens.max()), wl.k_cache, 0)
+        part = pa.decode_partition_tokens(n, hq, int(lens.max()), wl.k_cache)
+        # each split sequence writes and re-reads (D + 2) floats per partition and head
+        for t in lens.tolist():
+            parts = -(-t // part)
+            if parts > 1:
+                split += 2 * parts * hq * (wl.head_dim + 2) * 4
+    n_tok = st.slot_mapping.numel()
+    write = n_tok * (2 * per_tok + 8)                   # read k,v + write cache rows + slot
+    return {"logical_kv": logical_kv, "unique_kv": unique_kv, "decode": unique_kv + q_out +
+            tables + split, "decode_logical": logical_kv + q_out + tables + split,
+            "write": write, "workspace": ws, "partition": part}
+
+
+# ---- clocks --------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max((num(r[3]) or 0) for r in rows)}
+
+
+def measured_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---- CPU oracle (reference arm and cpu_baseline) ----------------------------------
+
+def time_oracle(wl, budget_s: float, max_reps: int = 50) -> dict:
+    """The oracle, as it stands, on the host cores: full steps (write + decode
+    of every (sequence, head)) repeated until ~budget_s seconds."""
+    import oracle
+    threads = oracle.max_threads()
+    kc, vc = wl.k_cache.clone(), wl.v_cache.clone()
+    done_bytes, reps, t0 = 0, 0, time.perf_counter()
+    elapsed = 0.0
+    while reps < max_reps:
+        k = reps % len(wl.steps)
+        st = wl.steps[k]
+        oracle.write_kv(st.k_new, st.v_new, st.slot_mapping, kc, vc)
+        oracle.decode(st.q, kc, vc, st.block_tables, st.seq_lens, wl.scale)
+        b = step_bytes(wl, k, split_traffic=False)
+        done_bytes += b["decode"] + b["write"]
+        reps += 1
+        elapsed = time.perf_counter() - t0
+        if elapsed >= budget_s:
+            break
+    return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds": round(elapsed, 3), "steps": reps,
+            "sample": f"{reps} full step(s) of the {wl.name} workload (write + decode of "
+                      f"all sequences and heads), fp64 C oracle with OpenMP, "
+                      f"{elapsed:.1f} s"}
+
+
+# ---- GPU arm ------------------------------------------------------------------------
+
+def run_ours(args, rank, world, device):
+    import paged_kv_cache_109_gb300 as pa
+    pa.load_library()
+    wl = workloads.make(args.workload)
+    nsteps_wl = len(wl.steps)
+    kc, vc = wl.k_cache.to(device), wl.v_cache.to(device)
+    # device-resident inputs of every distinct step
+    dsteps = []
+    for st in wl.steps:
+        dsteps.append({k: getattr(st, k).to(device) for k in
+                       ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens")})
+    bytes_ = [step_bytes(wl, k) for k in range(nsteps_wl)]
+    maxlens = [int(st.seq_lens.max()) for st in wl.steps]
+    part = args.partition or 0
+    ws_need = max(pa.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, m, kc, part)
+                  for m in maxlens)
+    ws = torch.empty(max(ws_need, 256), dtype=torch.uint8, device=device)
+    outs = [torch.empty_like(d["q"]) for d in dsteps]
+    stream = torch.cuda.current_stream(device)
+
+    def step(k, ev=None):
+        d = dsteps[k]
+        pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
+        if ev is not None:
+            ev[0].record(stream)
+        pa.decode(d["q"], kc, vc, d["block_tables"], d["seq_lens"], maxlens[k], wl.scale,
+                  out=outs[k], workspace=ws, partition_tokens=part)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for w in range(args.warmup):
+        step(w % nsteps_wl)
+    torch.cuda.synchronize(device)
+    if pa.last_device_error() != 0:
+        raise RuntimeError("device error flag raised during warm-up")
+
+    K = args.steps
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index or 0) as clocks:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for it in range(K):
+            step_ev[it][0].record(stream)
+            step(it % nsteps_wl, dec_ev[it])
+            step_ev[it][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+    step_bytes_sum = sum(bytes_[it % nsteps_wl]["decode"] + bytes_[it % nsteps_wl]["write"]
+                         for it in range(K))
+    dec_bytes_sum = sum(bytes_[it % nsteps_wl]["decode"] for it in range(K))
+    seqs = wl.num_seqs * K
+    value = world * step_bytes_sum / (total_ms / 1e3) / 1e9
+    dec_achieved = dec_bytes_sum / (sum(dec_ms) / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    err = pa.last_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error flag {err} raised in the timed region")
+
+    # end to end: host buffers, H2D of the step inputs and D2H of the output
+    e2e = run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_)
+
+    launches_per_step = []
+    for k in range(nsteps_wl):
+        n = 1 if wl.steps[k].slot_mapping.numel() else 0
+        n += 1
+        need = pa.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, maxlens[k], kc, part)
+        n += 1 if need else 0
+        launches_per_step.append(n)
+    launches = sum(launches_per_step[it % nsteps_wl] for it in range(K))
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = time_oracle(wl, args.cpu_seconds)
+    b0 = bytes_[0]
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) K/V/q; tables from a shuffled block pool)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+                   "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "block_size": wl.block_size, "max_seq_len": max(maxlens),
+                   "partition_tokens": b0["partition"],
+                   "l2": f"inputs larger than L2: {b0['unique_kv'] / 2**20:.0f} MiB of K/V "
+                         f"per step vs {L2_BYTES / 2**20:.0f} MiB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "decode_tokens_per_s_per_layer": round(world * seqs / (total_ms / 1e3), 1),
+        "bytes_per_step": {"unique_kv": b0["unique_kv"], "logical_kv": b0["logical_kv"],
+                           "decode": b0["decode"], "write": b0["write"]},
+        "roofline": {"bound": "hbm", "kernel": "pa_decode call (partition kernel + merge)",
+                     "achieved": round(dec_achieved, 2), "peak": peak,
+                     "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
+                     "frac": round(dec_achieved / peak, 4), "traffic": None,
+                     "decode_ms_median": round(statistics.median(dec_ms), 5)},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    return result
+
+
+def run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_):
+    """Same step through the public API from pinned host buffers: H2D of the
+    step's inputs, write + decode, D2H of the output, all timed."""
+    host = []
+    for st in wl.steps:
+        host.append({k: getattr(st, k).pin_memory() for k in
+                     ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens")})
+    dev = [{k: torch.empty_like(v, device=device) for k, v in h.items()} for h in host]
+    outs_h = [torch.empty_like(h["q"]).pin_memory() for h in host]
+    outs_d = [torch.empty_like(d["q"]) for d in dev]
+    n = len(host)
+    K = max(1, min(args.steps, 200))
+
+    def one(k):
+        h, d = host[k], dev[k]
+        for name in h:
+            d[name].copy_(h[name], non_blocking=True)
+        pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
+        pa.decode(d["q"], kc, vc, d["block_tables"], d["seq_lens"], maxlens[k], wl.scale,
+                  out=outs_d[k], workspace=ws, partition_tokens=part)
+        outs_h[k].copy_(outs_d[k], non_blocking=True)
+
+    for w in range(3):
+        one(w % n)
+    torch.cuda.synchronize(device)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for it in range(K):
+        one(it % n)
+    e.record(stream)
+    torch.cuda.synchronize(device)
+    ms = s.elapsed_time(e)
+    total = sum(bytes_[it % n]["decode"] + bytes_[it % n]["write"] for it in range(K))
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = outs_h[0].numel() * outs_h[0].element_size()
+    return {"value": round(total / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "ms_per_step": round(ms / K, 5)}
+
+
+def run_reference(args, rank):
+    """The oracle as the reference arm: bounded full steps on the host cores."""
+    if rank != 0:
+        return None
+    wl = workloads.make(args.workload)
+    steps = max(1, args.steps)
+    cpu = time_oracle(wl, args.cpu_seconds, max_reps=steps)
+    return {"impl": "reference", "metric": METRIC, "value": round(cpu["value"], 4),
+            "unit": "GB/s", "n_gpus": 0, "steps": cpu["steps"], "warmup": 0,
+            "ms_per_step": round(1e3 * cpu["seconds"] / cpu["steps"], 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload],
+                                            "name": args.workload},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(cpu["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="mha")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    res = run_ours(args, rank, world, device)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * pa.h -- C ABI of the paged-attention decode library (libpa.so).
+ *
+ * Two operations, both asynchronous on the caller's CUDA stream and both
+ * reading and writing only caller-owned device memory:
+ *
+ *   pa_write_kv  scatter each new token's K and V rows into its cache slot
+ *                ("vLLM PagedAttention: from memory fragmentation to slot
+ *                mapping", §6: the backend writes new K/V to physical slots
+ *                named by the slot mapping; paper notes' block lifecycle table:
+ *                decode fills the next slot of the last block);
+ *   pa_decode    single-query multi-head / grouped-query attention whose K/V
+ *                history is read through a block table (same page §3-§4:
+ *                logical block floor(t/B), offset t mod B, slot =
+ *                table[logical]*B + offset; "vLLM source walkthrough:
+ *                PagedAttention and Continuous Batching" §1.8: per-block walk,
+ *                V2 partitions merged by a reduce step; "PagedAttention"
+ *                glossary: the result equals attention over contiguous K/V).
+ *
+ * Cache layout (both caches, one layer): [num_blocks][num_kv_heads][block_size]
+ * [head_dim], head_dim contiguous.  One (block, kv head) tile is block_size *
+ * head_dim contiguous elements.  This is the glossary page's teaching layout,
+ * not vLLM's split-x K layout.
+ *
+ * Element types: PA_F32 (IEEE binary32) or PA_BF16 (bfloat16).  q, k, v, out
+ * and both caches share the cache's type; accumulation is fp32.
+ *
+ * Ownership: the caller allocates and frees every buffer (caches, tables,
+ * lengths, q, out, workspace).  The library allocates no device memory and
+ * keeps no per-call state; it caches one TMA descriptor pair per host thread.
+ *
+ * Errors: argument problems found on the host return a status and launch
+ * nothing.  Problems only visible on the device (a needed block-table entry
+ * outside [0, num_blocks), a sequence longer than its table or than
+ * max_seq_len, a slot outside the cache, a pipeline wait that exceeded its
+ * bound) never fault: the kernel skips the offending access, sets a bit in a
+ * device error word and carries on; read it with pa_last_device_error().
+ * No C++ exception crosses this interface.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shapes */
+    PA_ERR_UNSUPPORTED = 2,   /* valid request this build cannot run */
+    PA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    PA_ERR_CUDA = 4           /* a CUDA call or launch failed */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Geometry of one layer's K and V caches (both have this shape). */
+typedef struct {
+    int32_t num_blocks;    /* physical blocks in the pool                */
+    int32_t block_size;    /* B: tokens per block                        */
+    int32_t num_kv_heads;  /* Hkv                                        */
+    int32_t head_dim;      /* D                                          */
+    int32_t dtype;         /* pa_dtype                                   */
+} pa_cache_desc;
+
+/* Device error bits reported by pa_last_device_error(). */
+#define PA_DEVERR_TABLE_ENTRY 1u  /* a needed table entry was outside [0, num_blocks) */
+#define PA_DEVERR_SEQ_LEN     2u  /* seq_lens[i] > max_seq_len or > max_blocks*B     */
+#define PA_DEVERR_SLOT        4u  /* a slot was >= num_blocks * block_size            */
+#define PA_DEVERR_TIMEOUT     8u  /* a pipeline wait gave up after its bound          */
+
+/*
+ * pa_write_kv -- cache write through slot_mapping.
+ *
+ * k, v          device, [num_tokens][num_kv_heads][head_dim], cache dtype.
+ * slot_mapping  device int64 [num_tokens]; token j goes to slot s =
+ *               slot_mapping[j]: block s / B, row s % B, for every kv head.
+ *               s < 0 means "skip this token".  Slots must be distinct within
+ *               one call (two writers of one slot race).
+ * k_cache, v_cache  device caches, written in place.
+ * stream        cudaStream_t (NULL = legacy default stream).
+ * The copy is bit-exact.  num_tokens == 0 is a no-op.  Writing into a block
+ * that several sequences share is the caller's error (copy it first).
+ */
+pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
+                      int32_t num_tokens, void* k_cache, void* v_cache,
+                      const pa_cache_desc* cache, void* stream);
+
+/*
+ * Partition size (tokens, a multiple of block_size) that pa_decode uses when
+ * called with partition_tokens == 0.  Depends only on the arguments and on
+ * the current device's SM count.  Returns <= 0 on invalid arguments.
+ */
+int32_t pa_decode_partition_tokens(int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t max_seq_len, const pa_cache_desc* cache);
+
+/*
+ * Workspace bytes pa_decode needs for these arguments (0 when no sequence can
+ * span more than one partition).  partition_tokens == 0 selects the automatic
+ * size.  Layout, P = ceil(max_seq_len / partition_tokens):
+ *   float acc[num_seqs][num_q_heads][P][head_dim]   unnormalised sum_t w_t v_t
+ *   float ml [num_seqs][num_q_heads][P][2]          (m, l)
+ * with s_t = scale * q.k_t, m = log2(e) * max_t s_t (base-2 units),
+ * w_t = exp(s_t - max_t s_t), l = sum_t w_t, all over the partition's tokens.
+ * Cells of sequences that fit one partition are not written.
+ */
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                 int32_t max_seq_len, int32_t partition_tokens,
+                                 const pa_cache_desc* cache);
+
+/*
+ * pa_decode -- out[i][h] = sum_{t < T_i} softmax_t(scale * q[i][h].k_t) v_t,
+ * with k_t, v_t the cache rows of kv head floor(h / (Hq/Hkv)) at slot
+ * table[i][t / B] * B + t % B, and T_i = seq_lens[i].  T_i == 0 gives a zero
+ * row.
+ *
+ * q              device [num_seqs][num_q_heads][head_dim], cache dtype.
+ * block_tables   device int32 [num_seqs][max_blocks_per_seq]; entries at or
+ *                beyond ceil(T_i / B) are never read (pad with -1).
+ * seq_lens       device int32 [num_seqs].
+ * max_seq_len    host upper bound of seq_lens (sizes the grid; no device
+ *                read-back).  Must satisfy max_seq_len <= max_blocks_per_seq*B.
+ * scale          softmax scale (1/sqrt(head_dim) for standard attention).
+ * partition_tokens  split-K partition (multiple of B), or 0 for automatic.
+ *                Sequences longer than one partition are computed per
+ *                partition and merged with a log-sum-exp reduction.
+ * out            device [num_seqs][num_q_heads][head_dim], cache dtype,
+ *                round-to-nearest-even from fp32.
+ * workspace      device, >= pa_decode_workspace_bytes(...) bytes, 256-byte
+ *                aligned; may be NULL when that size is 0.
+ * The result is bitwise reproducible for fixed arguments on a fixed device.
+ */
+pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                    int32_t num_q_heads, float scale, int32_t partition_tokens,
+                    void* out, void* workspace, size_t workspace_bytes,
+                    const pa_cache_desc* cache, void* stream);
+
+/*
+ * Which decode kernel these arguments select: 1 = the TMA + tensor-core
+ * kernel (bf16, head_dim 64 or 128, block_size in {16, 32, 64} with
+ * block_size * head_dim <= 4096, group size <= 16), 0 = the portable kernel
+ * (any other valid shape, and every fp32 cache), < 0 = invalid arguments.
+ */
+int32_t pa_decode_path(int32_t num_q_heads, const pa_cache_desc* cache);
+
+/* Human-readable name of a status code (static string). */
+const char* pa_status_str(pa_status status);
+
+/* Synchronises the current device, returns the PA_DEVERR_* bits raised since
+ * the last call, and clears them.  Returns -1 if the read itself failed. */
+int32_t pa_last_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,195 @@
+"""Paged-attention decode for GB300: Python binding of libpa.so.
+
+Every function here marshals tensors into the C ABI declared in
+``include/pa.h``; all computation runs in the library's CUDA kernels.  There
+is no CPU path: every call raises ``ImportError`` when ``libpa.so`` has not
+been built, and the calls only accept CUDA tensors.
+
+    import paged_kv_cache_109_gb300 as pa
+    pa.write_kv(k, v, slot_mapping, k_cache, v_cache)
+    out = pa.decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from ._build import LIB as LIBRARY_PATH
+from ._build import build
+from .block_pool import BlockPool, SharedTailWrite
+
+__all__ = ["write_kv", "decode", "decode_workspace_bytes", "decode_partition_tokens",
+           "decode_path", "last_device_error", "PaError", "build", "BlockPool",
+           "SharedTailWrite", "LIBRARY_PATH", "load_library", "CacheDesc"]
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+PA_F32, PA_BF16 = 0, 1
+DEVERR_TABLE_ENTRY, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_status_str(status)} (status {status})")
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libpa.so (built in-tree by ``build()``); raises if it is absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    target = path or LIBRARY_PATH
+    if not os.path.exists(target):
+        raise ImportError(f"{target} is not built; run paged_kv_cache_109_gb300.build()")
+    lib = ctypes.CDLL(target)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    DP = ctypes.POINTER(CacheDesc)
+    lib.pa_write_kv.argtypes = [P, P, P, I32, P, P, DP, P]
+    lib.pa_write_kv.restype = ctypes.c_int
+    lib.pa_decode_partition_tokens.argtypes = [I32, I32, I32, DP]
+    lib.pa_decode_partition_tokens.restype = I32
+    lib.pa_decode_workspace_bytes.argtypes = [I32, I32, I32, I32, DP]
+    lib.pa_decode_workspace_bytes.restype = SZ
+    lib.pa_decode.argtypes = [P, P, P, P, I32, P, I32, I32, I32, ctypes.c_float, I32, P, P, SZ,
+                              DP, P]
+    lib.pa_decode.restype = ctypes.c_int
+    lib.pa_decode_path.argtypes = [I32, DP]
+    lib.pa_decode_path.restype = I32
+    lib.pa_status_str.argtypes = [ctypes.c_int]
+    lib.pa_status_str.restype = ctypes.c_char_p
+    lib.pa_last_device_error.argtypes = []
+    lib.pa_last_device_error.restype = I32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _status_str(status: int) -> str:
+    try:
+        return load_library().pa_status_str(status).decode()
+    except ImportError:
+        return "unknown"
+
+
+# ---- marshalling helpers ----------------------------------------------------
+
+_DTYPES = {torch.float32: PA_F32, torch.bfloat16: PA_BF16}
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    if k_cache.dim() != 4:
+        raise ValueError("caches are [num_blocks, num_kv_heads, block_size, head_dim]")
+    if k_cache.dtype not in _DTYPES:
+        raise ValueError(f"unsupported cache dtype {k_cache.dtype}")
+    nb, hkv, bs, d = k_cache.shape
+    return CacheDesc(nb, bs, hkv, d, _DTYPES[k_cache.dtype])
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _dev(*ts: torch.Tensor) -> None:
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != PA_OK:
+        raise PaError(status, where)
+
+
+# ---- public calls -------------------------------------------------------------
+
+def write_kv(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """Scatter k, v [n_tok, Hkv, D] into the caches at slot_mapping [n_tok] (int64)."""
+    _dev(k, v, slot_mapping, k_cache, v_cache)
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k, v and caches must share one dtype")
+    desc = cache_desc(k_cache)
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache shapes differ")
+    n = slot_mapping.numel()
+    if k.shape != (n, desc.num_kv_heads, desc.head_dim) or v.shape != k.shape:
+        raise ValueError(f"k, v must be [{n}, {desc.num_kv_heads}, {desc.head_dim}]")
+    st = load_library().pa_write_kv(_ptr(k), _ptr(v), _ptr(slot_mapping), n, _ptr(k_cache),
+                                    _ptr(v_cache), ctypes.byref(desc), _stream(stream))
+    _check(st, "pa_write_kv")
+
+
+def decode_partition_tokens(num_seqs: int, num_q_heads: int, max_seq_len: int,
+                            k_cache) -> int:
+    desc = k_cache if isinstance(k_cache, CacheDesc) else cache_desc(k_cache)
+    return int(load_library().pa_decode_partition_tokens(num_seqs, num_q_heads, max_seq_len,
+                                                         ctypes.byref(desc)))
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, max_seq_len: int, k_cache,
+                           partition_tokens: int = 0) -> int:
+    desc = k_cache if isinstance(k_cache, CacheDesc) else cache_desc(k_cache)
+    return int(load_library().pa_decode_workspace_bytes(num_seqs, num_q_heads, max_seq_len,
+                                                        partition_tokens, ctypes.byref(desc)))
+
+
+def decode_path(num_q_heads: int, k_cache) -> int:
+    desc = k_cache if isinstance(k_cache, CacheDesc) else cache_desc(k_cache)
+    return int(load_library().pa_decode_path(num_q_heads, ctypes.byref(desc)))
+
+
+def decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int,
+           scale: float | None = None, out=None, workspace=None, partition_tokens: int = 0,
+           stream=None) -> torch.Tensor:
+    """Single-query paged attention; returns out [N, Hq, D] in the cache dtype.
+
+    ``max_seq_len`` is a host-side upper bound of ``seq_lens`` (no device
+    read-back).  ``workspace`` (uint8, device) is allocated if not given and
+    split-K needs one.
+    """
+    _dev(q, k_cache, v_cache, block_tables, seq_lens)
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_tables and seq_lens must be int32")
+    desc = cache_desc(k_cache)
+    n, hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out)
+    need = decode_workspace_bytes(n, hq, max_seq_len, desc, partition_tokens)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().pa_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), n, max_seq_len, hq, float(scale), partition_tokens, _ptr(out),
+        _ptr(workspace), ws_bytes, ctypes.byref(desc), _stream(stream))
+    _check(st, "pa_decode")
+    return out
+
+
+def last_device_error() -> int:
+    """PA_DEVERR_* bits raised since the last call (synchronises the device)."""
+    return int(load_library().pa_last_device_error())

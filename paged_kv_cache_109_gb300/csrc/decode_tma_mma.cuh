@@ -1,0 +1,376 @@
+// decode_tma_mma.cuh -- bf16 paged decode: TMA tile loads driven by the block
+// table, tensor-core score and value contractions, online softmax.
+//
+// Work split.  One CTA per (partition p, kv head g, sequence i); four warps.
+// The partition's block ids are read from the table once into shared memory.
+// Warp w takes the partition's logical blocks w, w+4, w+8, ... and keeps a
+// private ring of kStages shared-memory stages; one stage holds the K tile
+// and the V tile of one (physical block, kv head), each block_size x head_dim
+// contiguous in the cache.  Lane 0 issues 3-D bulk-tensor copies (TMA,
+// 128-byte swizzle) for the block kStages ahead, completion counted on the
+// stage's mbarrier, so the table walk doubles as the prefetch schedule
+// ("vLLM source walkthrough: PagedAttention and Continuous Batching" §1.8:
+// block_table[block_idx] gives the physical block whose K/V the kernel loads;
+// the kernel walks the table's blocks).
+//
+// Per block, with the G <= 16 query heads of the kv group as the 16 rows of
+// an m16n8k16 tile (rows >= G are zero), the warp computes
+//   S[16 x B]   = Q[16 x D] . K_tile^T          (ldmatrix from the swizzled tile)
+//   online softmax on S in base 2 (scale * log2 e folded into one multiply):
+//   m' = max(m, rowmax S), acc *= 2^(m - m'), P = 2^(S - m'), l = l 2^(m-m') + rowsum P
+//   acc[16 x D] += P[16 x B] . V_tile             (P re-used from the S registers)
+// so every K/V tile is read from HBM once for all heads of its group
+// (the glossary page's expand_kv grouping: head h reads kv head h / G).
+// Positions at or past T_i inside the last block are masked to -inf (nxmr.cn
+// article §2.2: whole-block loads, padding masked).
+//
+// At the end the four warps' (m, l, acc) are combined through shared memory;
+// a sequence that fits one partition writes its output, otherwise the
+// partition's (acc, m, l) go to the workspace for merge_kernel.
+#pragma once
+
+#include <cuda.h>
+
+#include "decode_generic.cuh"
+#include "ptx.cuh"
+
+namespace pa {
+
+template <int D, int BS, bool G16>
+struct TmaMmaCfg {
+    static constexpr int kWarps = 4;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kBoxCols = 64;                   // 64 bf16 = 128 bytes (swizzle span)
+    static constexpr int kBoxes = D / kBoxCols;
+    static constexpr int kBoxBytes = BS * 128;
+    static constexpr int kTileBytes = kBoxes * kBoxBytes;  // = BS * D * 2
+    static constexpr int kStageBytes = 2 * kTileBytes;    // K tile + V tile
+    static constexpr int kStagesRaw = 32768 / kStageBytes;
+    static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+    static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+    static constexpr int kRows = G16 ? 16 : 8;              // query-head rows carried
+    static constexpr int kKSteps = D / 16;
+    static constexpr int kDTiles = D / 8;
+    static constexpr int kSub = BS / 16;
+    static constexpr int kMaxTableSlice = 2048;            // block ids per partition
+    static_assert(D % 64 == 0 && BS % 16 == 0, "tile shape");
+    static_assert(kStageBytes <= 16384, "stage too large for the shared-memory ring");
+    static_assert(kWarps * kRows * (D + 2) * 4 <= kRingBytes, "combine area");
+    static size_t smem_bytes() {
+        return 1024 + kRingBytes + 8 * kWarps * kStages + 4 * kMaxTableSlice;
+    }
+};
+
+template <int D, int BS, bool G16>
+__global__ void __launch_bounds__(128, 1)
+decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
+    using C = TmaMmaCfg<D, BS, G16>;
+    extern __shared__ uint8_t sm_raw[];
+    __shared__ int s_fail;
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+
+    const int32_t p = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
+    const int32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t grp = lane >> 2, tig = lane & 3;
+    const int32_t G = a.group;
+    const int32_t T = checked_len(a, i);
+    const int32_t P = a.part_tokens;
+    const int32_t nparts = (T + P - 1) / P;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    const int64_t head0 = (int64_t)i * a.num_q_heads + (int64_t)g * G;
+
+    if (T == 0) {
+        if (p == 0)
+            for (int32_t x = tid; x < G * D; x += C::kThreads)
+                out[head0 * D + x] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    if (p >= nparts) return;
+
+    const int32_t t0 = p * P;
+    const int32_t n = min(P, T - t0);
+    const int32_t nblk = (n + BS - 1) / BS;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kRingBytes);
+    int32_t* ids = reinterpret_cast<int32_t*>(bars + C::kWarps * C::kStages);
+
+    const int32_t* table = a.block_tables + (int64_t)i * a.max_blocks + t0 / BS;
+    for (int32_t b = tid; b < nblk; b += C::kThreads) {
+        int32_t id = table[b];
+        if (id < 0 || id >= a.num_blocks) {
+            raise_error(PA_DEVERR_TABLE_ENTRY);
+            id = -1;
+        }
+        ids[b] = id;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < C::kWarps * C::kStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+        mbar_fence_init();
+        s_fail = 0;
+    }
+    if (tid == 32) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+    }
+    __syncthreads();
+
+    // Q fragments (A operand): rows = the group's query heads, k = head dim.
+    uint32_t qa[C::kKSteps][4];
+    {
+        const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+        const bool r0 = grp < G, r1 = G16 && (grp + 8) < G;
+        const __nv_bfloat16* q0 = q + (head0 + grp) * D;
+        const __nv_bfloat16* q1 = q + (head0 + grp + 8) * D;
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+            const int d0 = ks * 16 + 2 * tig;
+            qa[ks][0] = r0 ? *reinterpret_cast<const uint32_t*>(q0 + d0) : 0u;
+            qa[ks][1] = r1 ? *reinterpret_cast<const uint32_t*>(q1 + d0) : 0u;
+            qa[ks][2] = r0 ? *reinterpret_cast<const uint32_t*>(q0 + d0 + 8) : 0u;
+            qa[ks][3] = r1 ? *reinterpret_cast<const uint32_t*>(q1 + d0 + 8) : 0u;
+        }
+    }
+
+    const int32_t my_count = nblk > warp ? (nblk - warp + C::kWarps - 1) / C::kWarps : 0;
+    const uint32_t ring_u = smem_u32(sm) + warp * C::kStages * C::kStageBytes;
+    const uint32_t bar0 = smem_u32(&bars[warp * C::kStages]);
+    const int32_t hkv = a.num_kv_heads;
+    const uint64_t policy = l2_policy_evict_first();
+
+    auto issue = [&](int32_t k) {   // lane 0 only
+        const int32_t j = warp + k * C::kWarps;
+        const int32_t st = k % C::kStages;
+        const uint32_t bar = bar0 + 8 * st;
+        const int32_t id = ids[j];
+        if (id >= 0) {
+            const uint32_t dst = ring_u + st * C::kStageBytes;
+            const int32_t z = id * hkv + g;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, C::kStageBytes);
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b)
+                tma_load_3d_hint(dst + b * C::kBoxBytes, &tmap_k, b * C::kBoxCols, 0, z, bar,
+                                 policy);
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b)
+                tma_load_3d_hint(dst + C::kTileBytes + b * C::kBoxBytes, &tmap_v,
+                                 b * C::kBoxCols, 0, z, bar, policy);
+        } else {
+            mbar_arrive(bar);
+        }
+    };
+    if (lane == 0) {
+        const int32_t pre = my_count < C::kStages ? my_count : C::kStages;
+        for (int32_t k = 0; k < pre; ++k) issue(k);
+    }
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float acc[C::kDTiles][4];
+#pragma unroll
+    for (int nd = 0; nd < C::kDTiles; ++nd) acc[nd][0] = acc[nd][1] = acc[nd][2] = acc[nd][3] = 0.f;
+
+    const int32_t lm = lane >> 3, lr = lane & 7;   // ldmatrix: matrix index, row in matrix
+    int32_t k = 0;
+    bool failed = false;
+    for (; k < my_count; ++k) {
+        const int32_t st = k % C::kStages;
+        const bool ok = mbar_wait_bounded(bar0 + 8 * st, (k / C::kStages) & 1, kWaitLimitCycles);
+        if (__any_sync(0xffffffffu, !ok)) {
+            failed = true;
+            break;
+        }
+        const int32_t j = warp + k * C::kWarps;
+        if (ids[j] >= 0) {
+            const uint32_t kb = ring_u + st * C::kStageBytes;
+            const uint32_t vb = kb + C::kTileBytes;
+            const int32_t nvalid = min(BS, n - j * BS);
+            if (nvalid < BS) {
+                // Unused rows of a sequence's last block may hold anything
+                // (even NaN); their weights are 0, so clear their V rows.
+                uint8_t* vt = sm + warp * C::kStages * C::kStageBytes + st * C::kStageBytes +
+                              C::kTileBytes;
+                const int32_t chunks = (BS - nvalid) * 8;   // 16-byte chunks per box
+                for (int32_t c = lane; c < C::kBoxes * chunks; c += 32) {
+                    const int32_t b = c / chunks, r = c - b * chunks;
+                    *reinterpret_cast<uint4*>(vt + b * C::kBoxBytes + nvalid * 128 + r * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+
+            float s[C::kSub][2][4];
+#pragma unroll
+            for (int u = 0; u < C::kSub; ++u) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) s[u][nt][0] = s[u][nt][1] = s[u][nt][2] = s[u][nt][3] = 0.f;
+                const int tok = u * 16 + (lm >> 1) * 8 + lr;
+#pragma unroll
+                for (int ks = 0; ks < C::kKSteps; ++ks) {
+                    const int ch = ((ks & 3) << 1) + (lm & 1);
+                    const uint32_t addr =
+                        kb + (ks >> 2) * C::kBoxBytes + tok * 128 + ((ch ^ (tok & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(addr, b0, b1, b2, b3);
+                    mma_bf16_16816(s[u][0], qa[ks], b0, b1);
+                    mma_bf16_16816(s[u][1], qa[ks], b2, b3);
+                }
+            }
+            // scale, mask, row max
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < C::kSub; ++u)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const bool valid = u * 16 + nt * 8 + 2 * tig + e < nvalid;
+                        s[u][nt][e] = valid ? s[u][nt][e] * a.scale_log2 : -INFINITY;
+                        mx0 = fmaxf(mx0, s[u][nt][e]);
+                        if (G16) {
+                            s[u][nt][2 + e] = valid ? s[u][nt][2 + e] * a.scale_log2 : -INFINITY;
+                            mx1 = fmaxf(mx1, s[u][nt][2 + e]);
+                        }
+                    }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            const float mn0 = fmaxf(m0, mx0);
+            const float al0 = exp2f(m0 - mn0);
+            m0 = mn0;
+            float al1 = 1.f;
+            if (G16) {
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                const float mn1 = fmaxf(m1, mx1);
+                al1 = exp2f(m1 - mn1);
+                m1 = mn1;
+            }
+            float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < C::kSub; ++u)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        s[u][nt][e] = exp2f(s[u][nt][e] - m0);
+                        rs0 += s[u][nt][e];
+                        if (G16) {
+                            s[u][nt][2 + e] = exp2f(s[u][nt][2 + e] - m1);
+                            rs1 += s[u][nt][2 + e];
+                        }
+                    }
+            l0 = l0 * al0 + rs0;
+            if (G16) l1 = l1 * al1 + rs1;
+#pragma unroll
+            for (int nd = 0; nd < C::kDTiles; ++nd) {
+                acc[nd][0] *= al0;
+                acc[nd][1] *= al0;
+                if (G16) {
+                    acc[nd][2] *= al1;
+                    acc[nd][3] *= al1;
+                }
+            }
+            // acc += P . V
+#pragma unroll
+            for (int u = 0; u < C::kSub; ++u) {
+                uint32_t pf[4];
+                pf[0] = pack_bf16x2(s[u][0][0], s[u][0][1]);
+                pf[1] = G16 ? pack_bf16x2(s[u][0][2], s[u][0][3]) : 0u;
+                pf[2] = pack_bf16x2(s[u][1][0], s[u][1][1]);
+                pf[3] = G16 ? pack_bf16x2(s[u][1][2], s[u][1][3]) : 0u;
+                const int tok = u * 16 + (lm & 1) * 8 + lr;
+#pragma unroll
+                for (int dp = 0; dp < D / 16; ++dp) {
+                    const int chunk = 2 * dp + (lm >> 1);
+                    const uint32_t addr = vb + (chunk >> 3) * C::kBoxBytes + tok * 128 +
+                                          (((chunk & 7) ^ (tok & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(addr, b0, b1, b2, b3);
+                    mma_bf16_16816(acc[2 * dp], pf, b0, b1);
+                    mma_bf16_16816(acc[2 * dp + 1], pf, b2, b3);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && k + C::kStages < my_count) issue(k + C::kStages);
+    }
+
+    if (failed) {
+        // drain this warp's copies still in flight (bounded), then report
+        const int32_t last = min(my_count, k + C::kStages);
+        for (int32_t kk = k; kk < last; ++kk)
+            mbar_wait_bounded(bar0 + 8 * (kk % C::kStages), (kk / C::kStages) & 1,
+                              kWaitLimitCycles);
+        if (lane == 0) {
+            raise_error(PA_DEVERR_TIMEOUT);
+            atomicOr(&s_fail, 1);
+        }
+    }
+
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    if (G16) {
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    }
+    __syncthreads();   // every warp is done with its ring
+
+    float* cm = reinterpret_cast<float*>(sm);      // [kWarps][kRows]
+    float* cl = cm + C::kWarps * C::kRows;          // [kWarps][kRows]
+    float* ca = cl + C::kWarps * C::kRows;          // [kWarps][kRows][D]
+    const bool fail = s_fail != 0;
+    if (!fail) {
+        if (tig == 0) {
+            cm[warp * C::kRows + grp] = m0;
+            cl[warp * C::kRows + grp] = l0;
+            if (G16) {
+                cm[warp * C::kRows + grp + 8] = m1;
+                cl[warp * C::kRows + grp + 8] = l1;
+            }
+        }
+#pragma unroll
+        for (int nd = 0; nd < C::kDTiles; ++nd) {
+            const int d = nd * 8 + 2 * tig;
+            float* r0 = ca + (warp * C::kRows + grp) * D + d;
+            r0[0] = acc[nd][0];
+            r0[1] = acc[nd][1];
+            if (G16) {
+                float* r1 = ca + (warp * C::kRows + grp + 8) * D + d;
+                r1[0] = acc[nd][2];
+                r1[1] = acc[nd][3];
+            }
+        }
+    }
+    __syncthreads();
+
+    for (int32_t x = tid; x < G * D; x += C::kThreads) {
+        const int32_t h = x / D, d = x - h * D;
+        float M = -INFINITY, L = 0.f, A = 0.f;
+        if (!fail) {
+#pragma unroll
+            for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, cm[w * C::kRows + h]);
+#pragma unroll
+            for (int w = 0; w < C::kWarps; ++w) {
+                const float mw = cm[w * C::kRows + h];
+                if (mw != -INFINITY) {
+                    const float e = exp2f(mw - M);
+                    L += e * cl[w * C::kRows + h];
+                    A += e * ca[(w * C::kRows + h) * D + d];
+                }
+            }
+        }
+        if (nparts == 1) {
+            out[(head0 + h) * D + d] = __float2bfloat16_rn(L > 0.f ? A / L : 0.f);
+        } else {
+            const int64_t cell = (head0 + h) * a.max_parts + p;
+            a.ws_acc[cell * D + d] = A;
+            if (d == 0) {
+                a.ws_ml[2 * cell] = M;
+                a.ws_ml[2 * cell + 1] = L;
+            }
+        }
+    }
+}
+
+}  // namespace pa

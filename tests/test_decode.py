@@ -1,0 +1,330 @@
+"""pa_decode on the GPU against the fp64 CPU oracle.
+
+Tolerances: fp32 caches, max abs error 1e-5; bf16 caches (the oracle reads the
+same bf16 values, widened exactly), |gpu - ref| <= 3e-3 + 1e-2 |ref| per
+element.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_109_gb300 as pa
+from paged_kv_cache_109_gb300 import workloads
+from tests._gpu import (BF16_ATOL, BF16_RTOL, F32_ATOL, DeviceState, HostState, assert_close,
+                        sample_pairs, tolerance)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def clear_device_error(cuda_device):
+    pa.last_device_error()
+    yield
+
+
+def run_step(wl, dev, step_index=0, **kw):
+    d, h = DeviceState(wl, dev), HostState(wl)
+    st = wl.steps[step_index]
+    d.write(st)
+    h.write(st)
+    out = d.decode(st, **kw)
+    torch.cuda.synchronize()
+    return out.cpu(), h.decode(st), d, h
+
+
+def synthetic(hq, hkv, d, bs, lengths, dtype=torch.bfloat16, seed=0, num_blocks=None,
+              shuffle=True):
+    """Random caches/tables for given lengths (tables from a shuffled pool)."""
+    g = torch.Generator().manual_seed(seed)
+    need = [-(-t // bs) for t in lengths]
+    nb = num_blocks or sum(need) + 3
+    perm = torch.randperm(nb, generator=g).tolist() if shuffle else list(range(nb))
+    width = max(max(need), 1)
+    tables, pos = [], 0
+    for k in need:
+        tables.append(perm[pos:pos + k] + [-1] * (width - k))
+        pos += k
+    kc = torch.randn(nb, hkv, bs, d, generator=g).to(dtype)
+    vc = torch.randn(nb, hkv, bs, d, generator=g).to(dtype)
+    q = torch.randn(len(lengths), hq, d, generator=g).to(dtype)
+    return q, kc, vc, torch.tensor(tables, dtype=torch.int32), torch.tensor(lengths,
+                                                                            dtype=torch.int32)
+
+
+def gpu_decode(dev, q, kc, vc, bt, sl, scale, **kw):
+    out = pa.decode(q.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), sl.to(dev),
+                    int(sl.max()) if sl.numel() else 0, scale, **kw)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+# ---- the worked example (fp32, portable kernel) ------------------------------
+
+def test_worked_example_fp32(cuda_device):
+    wl = workloads.tiny()
+    assert pa.decode_path(4, wl.k_cache) == 0
+    out, ref, d, h = run_step(wl, cuda_device)
+    assert_close(out.double().numpy(), ref, F32_ATOL, 0.0, "tiny")
+    # paged == contiguous: dense attention on the contiguous K/V
+    for s in range(2):
+        ek = wl.contiguous_k[s].double().repeat_interleave(2, dim=0)
+        ev = wl.contiguous_v[s].double().repeat_interleave(2, dim=0)
+        for hh in range(4):
+            dense = torch.softmax(ek[hh] @ wl.steps[0].q[s, hh].double() * wl.scale, 0) @ ev[hh]
+            assert np.abs(out[s, hh].double().numpy() - dense.numpy()).max() <= F32_ATOL
+    assert pa.last_device_error() == 0
+
+
+# ---- TMA + tensor-core kernel, small ragged cases ------------------------------
+
+FAST_CASES = [
+    # (Hq, Hkv, D, B, lengths)
+    (32, 32, 128, 16, (1, 15, 16, 17, 63, 64, 65, 200)),         # MHA, G=1
+    (32, 8, 128, 16, (1, 5, 129, 300, 1000, 47)),                  # G=4
+    (64, 8, 128, 32, (1, 31, 32, 33, 700, 1500)),                  # G=8, B=32
+    (16, 1, 128, 16, (3, 77, 512)),                                # G=16
+    (12, 3, 128, 16, (40, 9, 333)),                                # G=4, odd head count
+    (10, 2, 64, 32, (1, 64, 65, 250)),                             # G=5, D=64
+    (8, 4, 64, 64, (1, 63, 64, 65, 129, 400)),                     # G=2, B=64
+    (9, 1, 64, 16, (2, 100)),                                      # G=9
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,lengths", FAST_CASES)
+@pytest.mark.parametrize("part", [0, "B", "3B", "4B", "64B"])
+def test_fast_kernel_matches_oracle(cuda_device, hq, hkv, d, bs, lengths, part):
+    q, kc, vc, bt, sl = synthetic(hq, hkv, d, bs, lengths, seed=hq * 7 + bs)
+    assert pa.decode_path(hq, kc) == 1
+    scale = 1.0 / math.sqrt(d)
+    ptok = 0 if part == 0 else bs * int(part[:-1] or 1)
+    out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=ptok)
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, f"fast {hq}/{hkv}/{d}/{bs}")
+    assert pa.last_device_error() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,lengths,dtype", [
+    (8, 2, 8, 4, (10, 7, 1, 33), torch.float32),
+    (32, 8, 128, 16, (1, 200, 1000), torch.float32),
+    (64, 2, 128, 16, (5, 300), torch.bfloat16),           # G=32: portable kernel
+    (6, 2, 96, 8, (1, 8, 9, 100), torch.bfloat16),       # D=96, B=8
+    (4, 4, 256, 16, (17, 64), torch.bfloat16),           # D=256
+])
+@pytest.mark.parametrize("part", [0, "B", "5B"])
+def test_portable_kernel_matches_oracle(cuda_device, hq, hkv, d, bs, lengths, dtype, part):
+    q, kc, vc, bt, sl = synthetic(hq, hkv, d, bs, lengths, dtype=dtype, seed=d + bs)
+    assert pa.decode_path(hq, kc) == 0
+    scale = 0.9 / math.sqrt(d)
+    ptok = 0 if part == 0 else bs * int(part[:-1] or 1)
+    out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=ptok)
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    atol, rtol = tolerance(dtype)
+    assert_close(out.double().numpy(), ref, atol, rtol, "portable")
+
+
+# ---- split-K partials and merge --------------------------------------------------
+
+@pytest.mark.parametrize("hq,hkv,d,bs,part", [(32, 8, 128, 16, 64), (64, 8, 128, 32, 256),
+                                               (8, 2, 8, 4, 8)])
+def test_workspace_partials_match_oracle(cuda_device, hq, hkv, d, bs, part):
+    dtype = torch.float32 if d == 8 else torch.bfloat16
+    lengths = (1, part - 1, part, part + 1, 5 * part + 3)
+    q, kc, vc, bt, sl = synthetic(hq, hkv, d, bs, lengths, dtype=dtype, seed=5)
+    scale = 1.0 / math.sqrt(d)
+    n = len(lengths)
+    maxlen = int(sl.max())
+    need = pa.decode_workspace_bytes(n, hq, maxlen, kc, part)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=cuda_device)
+    out = pa.decode(q.to(cuda_device), kc.to(cuda_device), vc.to(cuda_device),
+                    bt.to(cuda_device), sl.to(cuda_device), maxlen, scale, workspace=ws,
+                    partition_tokens=part)
+    torch.cuda.synchronize()
+    P = -(-maxlen // part)
+    cells = n * hq * P
+    acc = ws[: cells * d * 4].view(torch.float32).view(n, hq, P, d).cpu().double().numpy()
+    off = (cells * d * 4 + 255) // 256 * 256
+    ml = ws[off: off + cells * 8].view(torch.float32).view(n, hq, P, 2).cpu().double().numpy()
+    m_ref, l_ref, acc_ref = oracle.decode_partials(q, kc, vc, bt, sl, scale, part, P)
+    atol, rtol = tolerance(dtype)
+    for s, t in enumerate(lengths):
+        parts = -(-t // part)
+        if parts <= 1:
+            continue
+        m_gpu = ml[s, :, :parts, 0] / math.log2(math.e)
+        assert_close(m_gpu, m_ref[s, :, :parts], 1e-4, 1e-5, "m")
+        assert_close(ml[s, :, :parts, 1], l_ref[s, :, :parts], 1e-4, 1e-3, "l")
+        # acc grows with l (up to the partition length): compare acc / l,
+        # the partition's own normalised output, at the output tolerance
+        assert_close(acc[s, :, :parts] / ml[s, :, :parts, 1:],
+                     acc_ref[s, :, :parts] / l_ref[s, :, :parts, None], atol, rtol, "acc/l")
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    assert_close(out.cpu().double().numpy(), ref, atol, rtol, "merged out")
+
+
+def test_split_on_off_agree_and_runs_are_deterministic(cuda_device):
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (3000, 1, 777, 4096, 2048), seed=9)
+    scale = 1 / math.sqrt(128)
+    outs = [gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=p)
+            for p in (16, 64, 256, 1024, 4096)]
+    for o in outs[1:]:
+        assert_close(o.double().numpy(), outs[0].double().numpy(), 2 * BF16_ATOL, 2 * BF16_RTOL,
+                     "split sizes")
+    again = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=256)
+    assert torch.equal(again, outs[2])
+    auto1 = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale)
+    auto2 = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale)
+    assert torch.equal(auto1, auto2)
+
+
+def test_relabelling_physical_blocks_changes_nothing(cuda_device):
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (500, 33, 1200), seed=3, num_blocks=200)
+    scale = 1 / math.sqrt(128)
+    out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=128)
+    perm = torch.randperm(200, generator=torch.Generator().manual_seed(4))
+    kp, vp = torch.empty_like(kc), torch.empty_like(vc)
+    kp[perm], vp[perm] = kc, vc
+    btp = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+    out2 = gpu_decode(cuda_device, q, kp, vp, btp, sl, scale, partition_tokens=128)
+    assert torch.equal(out, out2)
+
+
+def test_closed_forms_on_gpu(cuda_device):
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (1, 100, 900), seed=6)
+    scale = 1 / math.sqrt(128)
+    # constant V rows -> that constant; q = 0 -> mean of V; T = 1 -> v_0
+    out = gpu_decode(cuda_device, q, kc, torch.full_like(vc, 0.75), bt, sl, scale)
+    assert torch.all(out == 0.75)
+    out = gpu_decode(cuda_device, torch.zeros_like(q), kc, vc, bt, sl, scale)
+    ref = oracle.decode(torch.zeros_like(q), kc, vc, bt, sl, scale)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "q=0")
+    out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale)
+    v0 = vc[int(bt[0, 0])].repeat_interleave(4, dim=0)[:, 0]        # [Hq, D]
+    assert torch.equal(out[0], v0)
+
+
+def test_garbage_in_unused_tail_rows_is_ignored(cuda_device):
+    """Rows past T_i in a sequence's last block are never weighted, even when
+    they hold NaN or Inf."""
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (37, 5, 200), seed=14)
+    ref = oracle.decode(q, kc, vc, bt, sl, 1 / math.sqrt(128))
+    for i, t in enumerate(sl.tolist()):
+        last = int(bt[i, (t - 1) // 16])
+        kc[last, :, t % 16:] = float("nan")
+        vc[last, :, t % 16:] = float("inf")
+    for part in (0, 16, 64):
+        out = gpu_decode(cuda_device, q, kc, vc, bt, sl, 1 / math.sqrt(128),
+                         partition_tokens=part)
+        assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "nan tail")
+
+
+def test_zero_length_sequences(cuda_device):
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (0, 50, 0, 300), seed=8)
+    out = gpu_decode(cuda_device, q, kc, vc, bt, sl, 1 / math.sqrt(128), partition_tokens=64)
+    assert not out[0].any() and not out[2].any()
+    ref = oracle.decode(q, kc, vc, bt, sl, 1 / math.sqrt(128))
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "zero-length")
+
+
+# ---- device-side bounds checks (host-planted bad inputs; nothing faults) --------
+
+def test_bad_table_entry_is_reported_not_faulting(cuda_device):
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (100, 200), seed=10, num_blocks=40)
+    bt = bt.clone()
+    bt[1, 3] = 40            # == num_blocks: out of range
+    bt[0, 1] = -5
+    gpu_decode(cuda_device, q, kc, vc, bt, sl, 0.1, partition_tokens=64)
+    assert pa.last_device_error() & pa.DEVERR_TABLE_ENTRY
+
+
+def test_seq_len_beyond_bound_is_reported(cuda_device):
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (100, 200), seed=11)
+    out = pa.decode(q.to(cuda_device), kc.to(cuda_device), vc.to(cuda_device),
+                    bt.to(cuda_device), sl.to(cuda_device), 150, 0.1)
+    torch.cuda.synchronize()
+    assert pa.last_device_error() & pa.DEVERR_SEQ_LEN
+    assert torch.isfinite(out.float()).all()
+
+
+def test_workspace_too_small_is_refused(cuda_device):
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (1000, 2000), seed=12)
+    ws = torch.empty(16, dtype=torch.uint8, device=cuda_device)
+    with pytest.raises(pa.PaError) as e:
+        pa.decode(q.to(cuda_device), kc.to(cuda_device), vc.to(cuda_device),
+                  bt.to(cuda_device), sl.to(cuda_device), 2000, 0.1, workspace=ws,
+                  partition_tokens=64)
+    assert e.value.status == pa.PA_ERR_WORKSPACE
+
+
+def test_bad_partition_is_refused(cuda_device):
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (100,), seed=13)
+    with pytest.raises(pa.PaError) as e:
+        pa.decode(q.to(cuda_device), kc.to(cuda_device), vc.to(cuda_device),
+                  bt.to(cuda_device), sl.to(cuda_device), 100, 0.1, partition_tokens=24)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+
+
+# ---- serving-shaped workloads: reduced sizes in full, full sizes sampled ----------
+
+@pytest.mark.parametrize("name,kw", [
+    ("mha", dict(num_seqs=8, min_len=128, max_len=700, num_blocks=1024)),
+    ("gqa", dict(num_seqs=24, median_len=300, max_len=2000, num_shared=6, prefix_len=128,
+                 num_blocks=4096)),
+    ("long", dict(num_seqs=2, seq_len=9000)),
+])
+def test_workload_reduced(cuda_device, name, kw):
+    wl = workloads.make(name, **kw)
+    out, ref, _, _ = run_step(wl, cuda_device)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, name)
+    assert pa.last_device_error() == 0
+
+
+def test_continuous_batching_reduced(cuda_device):
+    wl = workloads.cb(num_seqs=32, max_len0=600, chunk=256, num_steps=4, num_blocks=4096)
+    d, h = DeviceState(wl, cuda_device), HostState(wl)
+    for st in wl.steps:
+        d.write(st)
+        h.write(st)
+        out = d.decode(st)
+        torch.cuda.synchronize()
+        assert_close(out.cpu().double().numpy(), h.decode(st), BF16_ATOL, BF16_RTOL, "cb")
+    assert torch.equal(d.k_cache.cpu(), h.k_cache)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mha", "gqa", "long"])
+def test_workload_full_size_sampled(cuda_device, name):
+    wl = workloads.make(name)
+    st = wl.steps[0]
+    d, h = DeviceState(wl, cuda_device), HostState(wl)
+    d.write(st)
+    h.write(st)
+    out = d.decode(st).cpu()
+    pairs = sample_pairs(st, wl.num_q_heads, 48, seed=1)
+    ref = h.decode(st, pairs=pairs)
+    got = out.double().numpy()
+    assert_close(got[pairs[:, 0], pairs[:, 1]], ref[pairs[:, 0], pairs[:, 1]],
+                 BF16_ATOL, BF16_RTOL, f"{name} full")
+    assert torch.isfinite(out.float()).all()
+    assert pa.last_device_error() == 0
+    if name == "gqa":
+        assert wl.stats["prefix_ref_cnt"] == 32
+
+
+@pytest.mark.slow
+def test_continuous_batching_full_size_sampled(cuda_device):
+    wl = workloads.cb()
+    d, h = DeviceState(wl, cuda_device), HostState(wl)
+    for k, st in enumerate(wl.steps):
+        d.write(st)
+        h.write(st)
+        out = d.decode(st).cpu()
+        if k in (0, len(wl.steps) - 1):
+            pairs = sample_pairs(st, wl.num_q_heads, 32, seed=k)
+            ref = h.decode(st, pairs=pairs)
+            got = out.double().numpy()
+            assert_close(got[pairs[:, 0], pairs[:, 1]], ref[pairs[:, 0], pairs[:, 1]],
+                         BF16_ATOL, BF16_RTOL, f"cb step {k}")
+    assert pa.last_device_error() == 0
