@@ -148,6 +148,35 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  */
 int32_t pa_decode_path(int32_t num_q_heads, const pa_cache_desc* cache);
 
+/*
+ * pa_decode_no_alloc -- pa_decode for callers that cannot allocate device
+ * memory when they run attention (for example a plugin hook of an inference
+ * engine that forbids allocation during execution, or a process working in a
+ * fixed, pre-reserved memory budget).  The pages have no counterpart to it.
+ *
+ * Same arguments and result as pa_decode, minus the workspace: the split-K
+ * workspace is a fixed array of PA_NO_ALLOC_WORKSPACE_BYTES (32 MiB) inside
+ * the library, held by every GPU that loads libpa.so until the process exits.
+ * The call allocates nothing itself.
+ * - The first call on each device looks the array's device address up (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.
+ * - A request whose workspace (pa_decode_workspace_bytes with the same
+ *   arguments) exceeds PA_NO_ALLOC_WORKSPACE_BYTES returns PA_ERR_WORKSPACE
+ *   and launches nothing.
+ * - All calls on a device share the one array, which keeps the last call's
+ *   contents.  Nothing in it needs to start at zero: every cell the merge reads
+ *   is written earlier in the same call.  Calls whose execution overlaps on the
+ *   GPU (different streams without ordering between them) race on the array;
+ *   order them on one stream or synchronise between them.
+ */
+#define PA_NO_ALLOC_WORKSPACE_BYTES (32u << 20)
+pa_status pa_decode_no_alloc(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                             int32_t num_q_heads, float scale, int32_t partition_tokens,
+                             void* out, const pa_cache_desc* cache, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* pa_status_str(pa_status status);
 

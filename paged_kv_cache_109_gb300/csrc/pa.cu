@@ -385,3 +385,59 @@ int32_t pa_last_device_error(void) {
 }
 
 }  // extern "C"
+
+// ---- decode without any caller-provided workspace -------------------------------
+//
+// Some callers cannot allocate device memory at the point where they run
+// attention: a plugin hook of an inference engine that forbids allocation once
+// execution has started, or a process with a fixed, pre-reserved memory budget
+// that has no room to grow.  pa_decode_no_alloc serves them by keeping the
+// split-K workspace in a fixed array inside the library itself.  The array is
+// a file-scope device variable, so every GPU that loads libpa.so holds it
+// until the process exits.  In host code the name g_no_alloc_workspace is
+// only a host-side stand-in, not a device address: the real address is looked
+// up once per device with cudaGetSymbolAddress and cached.
+
+static __device__ __align__(256) unsigned char g_no_alloc_workspace[PA_NO_ALLOC_WORKSPACE_BYTES];
+
+namespace pa {
+namespace {
+
+void* g_no_alloc_ptr[kMaxDevices] = {nullptr};
+std::mutex g_no_alloc_mutex;
+
+// Device address of the static workspace for the current device, or nullptr
+// if the lookup failed.  Runs cudaGetSymbolAddress on the first use per device.
+void* no_alloc_workspace() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_no_alloc_mutex);
+    if (g_no_alloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_no_alloc_workspace) != cudaSuccess) return nullptr;
+        g_no_alloc_ptr[dev] = p;
+    }
+    return g_no_alloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_decode_no_alloc(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* seq_lens, int32_t num_seqs,
+                                        int32_t max_seq_len, int32_t num_q_heads, float scale,
+                                        int32_t partition_tokens, void* out,
+                                        const pa_cache_desc* cache, void* stream) {
+    if (pa_decode_path(num_q_heads, cache) < 0 || num_seqs < 0 || max_seq_len < 0 ||
+        partition_tokens < 0)
+        return PA_ERR_INVALID_ARG;
+    const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, max_seq_len,
+                                                  partition_tokens, cache);
+    if (need > PA_NO_ALLOC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;
+    void* ws = pa::no_alloc_workspace();
+    if (ws == nullptr) return PA_ERR_CUDA;
+    return pa_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                     max_seq_len, num_q_heads, scale, partition_tokens, out, ws,
+                     PA_NO_ALLOC_WORKSPACE_BYTES, cache, stream);
+}
