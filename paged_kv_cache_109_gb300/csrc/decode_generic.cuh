@@ -13,6 +13,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace pa {
 
@@ -39,10 +40,9 @@ struct DecodeArgs {
     float scale_log2;     // scale * log2(e)
 };
 
-// Effective length of sequence i: clamps (and reports) lengths the table or
-// the host bound cannot cover.
-__device__ __forceinline__ int32_t checked_len(const DecodeArgs& a, int32_t i) {
-    int32_t t = a.seq_lens[i];
+// Effective length from a raw seq_lens value: clamps (and reports) lengths
+// the table or the host bound cannot cover.
+__device__ __forceinline__ int32_t clamp_len(const DecodeArgs& a, int32_t t) {
     const int64_t cap64 = (int64_t)a.max_blocks * a.block_size;
     const int32_t cap = (int32_t)min((int64_t)a.max_seq_len, cap64);
     if (t < 0 || t > cap) {
@@ -52,10 +52,16 @@ __device__ __forceinline__ int32_t checked_len(const DecodeArgs& a, int32_t i) {
     return t;
 }
 
+// Effective length of sequence i.
+__device__ __forceinline__ int32_t checked_len(const DecodeArgs& a, int32_t i) {
+    return clamp_len(a, a.seq_lens[i]);
+}
+
 template <typename E>
 __global__ void __launch_bounds__(128)
 decode_generic_kernel(const DecodeArgs a) {
     extern __shared__ float sm_generic[];
+    griddep_wait();                 // inputs may come from the previous kernel
     const int32_t p = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
     const int32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t G = a.group, D = a.head_dim, Bs = a.block_size, P = a.part_tokens;
@@ -132,6 +138,7 @@ decode_generic_kernel(const DecodeArgs a) {
     __syncthreads();
 
     // (3) weighted V rows
+    griddep_launch_dependents();    // the merge may be scheduled now
     for (int32_t x = tid; x < G * D; x += blockDim.x) {
         const int32_t h = x / D, d = x - h * D;
         float acc = 0.f;

@@ -3,25 +3,27 @@
 //
 // Work split.  One CTA per (partition p, kv head g, sequence i); four warps.
 // The partition's block ids are read from the table once into shared memory.
-// Warp w takes the partition's logical blocks w, w+4, w+8, ... and keeps a
-// private ring of kStages shared-memory stages; one stage holds the K tile
-// and the V tile of one (physical block, kv head), each block_size x head_dim
-// contiguous in the cache.  Lane 0 issues 3-D bulk-tensor copies (TMA,
-// 128-byte swizzle) for the block kStages ahead, completion counted on the
-// stage's mbarrier, so the table walk doubles as the prefetch schedule
+// The partition's tokens are cut into 16-token chunks (a block of B tokens,
+// B a multiple of 16, is B/16 chunks).  Warp w takes chunks w, w+4, w+8, ...
+// and keeps a private ring of kStages shared-memory stages; one stage holds
+// the K rows and the V rows of one chunk of one (physical block, kv head)
+// tile, 16 x head_dim contiguous in the cache.  Lane 0 issues 3-D
+// bulk-tensor copies (TMA, 128-byte swizzle) for the chunk kStages ahead,
+// completion counted on the stage's mbarrier, so the table walk doubles as
+// the prefetch schedule
 // ("vLLM source walkthrough: PagedAttention and Continuous Batching" §1.8:
 // block_table[block_idx] gives the physical block whose K/V the kernel loads;
 // the kernel walks the table's blocks).
 //
-// Per block, with the G <= 16 query heads of the kv group as the 16 rows of
+// Per chunk, with the G <= 16 query heads of the kv group as the 16 rows of
 // an m16n8k16 tile (rows >= G are zero), the warp computes
-//   S[16 x B]   = Q[16 x D] . K_tile^T          (ldmatrix from the swizzled tile)
+//   S[16 x 16]  = Q[16 x D] . K_chunk^T         (ldmatrix from the swizzled tile)
 //   online softmax on S in base 2 (scale * log2 e folded into one multiply):
 //   m' = max(m, rowmax S), acc *= 2^(m - m'), P = 2^(S - m'), l = l 2^(m-m') + rowsum P
-//   acc[16 x D] += P[16 x B] . V_tile             (P re-used from the S registers)
+//   acc[16 x D] += P[16 x 16] . V_chunk           (P re-used from the S registers)
 // so every K/V tile is read from HBM once for all heads of its group
 // (the glossary page's expand_kv grouping: head h reads kv head h / G).
-// Positions at or past T_i inside the last block are masked to -inf (nxmr.cn
+// Positions at or past T_i inside the last chunk are masked to -inf (nxmr.cn
 // article §2.2: whole-block loads, padding masked).
 //
 // At the end the four warps' (m, l, acc) are combined through shared memory;
@@ -36,36 +38,50 @@
 
 namespace pa {
 
-template <int D, int BS, bool G16>
+// Shared-memory ring per warp (bytes) and the CTAs per SM the launch bounds
+// ask for.  Two 8 KiB stages per warp (D = 128) and three CTAs per SM keep
+// 96-192 KiB of K/V in flight per SM, and one CTA's prologue or epilogue
+// overlaps the others' streaming (measured best of 1-3 CTAs x 2-4 stages).
+#ifndef PA_RING_BYTES_PER_WARP
+#define PA_RING_BYTES_PER_WARP 16384
+#endif
+#ifndef PA_MIN_CTAS_PER_SM
+#define PA_MIN_CTAS_PER_SM 3
+#endif
+
+template <int D, bool G16>
 struct TmaMmaCfg {
     static constexpr int kWarps = 4;
     static constexpr int kThreads = kWarps * 32;
+    static constexpr int kChunk = 16;                     // tokens per pipeline stage
     static constexpr int kBoxCols = 64;                   // 64 bf16 = 128 bytes (swizzle span)
     static constexpr int kBoxes = D / kBoxCols;
-    static constexpr int kBoxBytes = BS * 128;
-    static constexpr int kTileBytes = kBoxes * kBoxBytes;  // = BS * D * 2
-    static constexpr int kStageBytes = 2 * kTileBytes;    // K tile + V tile
-    static constexpr int kStagesRaw = 32768 / kStageBytes;
+    static constexpr int kBoxBytes = kChunk * 128;        // 16 rows x 128 bytes
+    static constexpr int kTileBytes = kBoxes * kBoxBytes;  // = 16 * D * 2
+    static constexpr int kStageBytes = 2 * kTileBytes;    // K chunk + V chunk
+    static constexpr int kStagesRaw = PA_RING_BYTES_PER_WARP / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
     static constexpr int kRows = G16 ? 16 : 8;              // query-head rows carried
     static constexpr int kKSteps = D / 16;
     static constexpr int kDTiles = D / 8;
-    static constexpr int kSub = BS / 16;
     static constexpr int kMaxTableSlice = 2048;            // block ids per partition
-    static_assert(D % 64 == 0 && BS % 16 == 0, "tile shape");
-    static_assert(kStageBytes <= 16384, "stage too large for the shared-memory ring");
+    static_assert(D % 64 == 0, "tile shape");
     static_assert(kWarps * kRows * (D + 2) * 4 <= kRingBytes, "combine area");
-    static size_t smem_bytes() {
-        return 1024 + kRingBytes + 8 * kWarps * kStages + 4 * kMaxTableSlice;
+    // dynamic shared bytes for a partition of part_tokens tokens
+    static size_t smem_bytes(int32_t part_tokens, int32_t block_size) {
+        const size_t ids =
+            ((size_t)(part_tokens + block_size - 1) / block_size * 4 + 15) / 16 * 16;
+        return 1024 + kRingBytes + 8 * kWarps * kStages + ids;
     }
+    static size_t smem_bytes_max() { return smem_bytes(kMaxTableSlice, 1); }
 };
 
-template <int D, int BS, bool G16>
-__global__ void __launch_bounds__(128, 1)
+template <int D, bool G16>
+__global__ void __launch_bounds__(128, PA_MIN_CTAS_PER_SM)
 decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
-    using C = TmaMmaCfg<D, BS, G16>;
+    using C = TmaMmaCfg<D, G16>;
     extern __shared__ uint8_t sm_raw[];
     __shared__ int s_fail;
     uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -75,38 +91,21 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t grp = lane >> 2, tig = lane & 3;
     const int32_t G = a.group;
-    const int32_t T = checked_len(a, i);
+    const int32_t BS = a.block_size;
+    const int32_t cpb = BS / C::kChunk;                    // chunks per block
     const int32_t P = a.part_tokens;
-    const int32_t nparts = (T + P - 1) / P;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    const int64_t head0 = (int64_t)i * a.num_q_heads + (int64_t)g * G;
-
-    if (T == 0) {
-        if (p == 0)
-            for (int32_t x = tid; x < G * D; x += C::kThreads)
-                out[head0 * D + x] = __float2bfloat16_rn(0.f);
-        return;
-    }
-    if (p >= nparts) return;
-
     const int32_t t0 = p * P;
-    const int32_t n = min(P, T - t0);
-    const int32_t nblk = (n + BS - 1) / BS;
+    const int64_t head0 = (int64_t)i * a.num_q_heads + (int64_t)g * G;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kRingBytes);
     int32_t* ids = reinterpret_cast<int32_t*>(bars + C::kWarps * C::kStages);
 
-    const int32_t* table = a.block_tables + (int64_t)i * a.max_blocks + t0 / BS;
-    for (int32_t b = tid; b < nblk; b += C::kThreads) {
-        int32_t id = table[b];
-        if (id < 0 || id >= a.num_blocks) {
-            raise_error(PA_DEVERR_TABLE_ENTRY);
-            id = -1;
-        }
-        ids[b] = id;
-    }
+    // Barrier set-up reads no input, so it runs before waiting for the
+    // previous kernel in the stream (programmatic dependent launch); every
+    // input read comes after griddep_wait().
     if (tid == 0) {
-        for (int s = 0; s < C::kWarps * C::kStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+        for (int s2 = 0; s2 < C::kWarps * C::kStages; ++s2) mbar_init(smem_u32(&bars[s2]), 1);
         mbar_fence_init();
         s_fail = 0;
     }
@@ -114,8 +113,26 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
     }
-    __syncthreads();
+    griddep_wait();
 
+    // Prologue.  Partition 0 of a sequence always has work (unless T = 0), so
+    // its CTA issues the length, its slice of the block table (read
+    // speculatively up to the partition's end, clamped to the row) and the
+    // query fragments together: one memory round trip before the first tile
+    // copy.  CTAs of later partitions are often empty (short sequences in a
+    // batch sized by max_seq_len): they read the length first and leave at
+    // once when there is nothing to do.
+    const int32_t T_raw = a.seq_lens[i];
+    if (p > 0 && T_raw <= t0 && T_raw <= a.max_seq_len) return;
+    const int32_t slice = max(0, min((P + BS - 1) / BS, a.max_blocks - t0 / BS));
+    const int32_t* table = a.block_tables + (int64_t)i * a.max_blocks + t0 / BS;
+    constexpr int kIdsPerThread = (C::kMaxTableSlice + C::kThreads - 1) / C::kThreads;
+    int32_t raw_ids[kIdsPerThread];
+#pragma unroll
+    for (int r = 0; r < kIdsPerThread; ++r) {
+        const int32_t b = tid + r * C::kThreads;
+        raw_ids[r] = b < slice ? table[b] : -1;
+    }
     // Q fragments (A operand): rows = the group's query heads, k = head dim.
     uint32_t qa[C::kKSteps][4];
     {
@@ -133,30 +150,60 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
 
-    const int32_t my_count = nblk > warp ? (nblk - warp + C::kWarps - 1) / C::kWarps : 0;
+    const int32_t T = clamp_len(a, T_raw);
+    const int32_t nparts = (T + P - 1) / P;
+    if (T == 0) {
+        if (p == 0)
+            for (int32_t x = tid; x < G * D; x += C::kThreads)
+                out[head0 * D + x] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    if (p >= nparts) return;
+
+    const int32_t n = min(P, T - t0);
+    const int32_t nblk = (n + BS - 1) / BS;
+    const int32_t nchunk = (n + C::kChunk - 1) / C::kChunk;
+#pragma unroll
+    for (int r = 0; r < kIdsPerThread; ++r) {
+        const int32_t b = tid + r * C::kThreads;
+        if (b < nblk) {
+            int32_t id = raw_ids[r];
+            if (id < 0 || id >= a.num_blocks) {
+                raise_error(PA_DEVERR_TABLE_ENTRY);
+                id = -1;
+            }
+            ids[b] = id;
+        }
+    }
+    __syncthreads();
+
+    // warp w takes chunks w, w + 4, w + 8, ... of the partition
+    const int32_t my_count = nchunk > warp ? (nchunk - warp + C::kWarps - 1) / C::kWarps : 0;
     const uint32_t ring_u = smem_u32(sm) + warp * C::kStages * C::kStageBytes;
     const uint32_t bar0 = smem_u32(&bars[warp * C::kStages]);
     const int32_t hkv = a.num_kv_heads;
     const uint64_t policy = l2_policy_evict_first();
 
     auto issue = [&](int32_t k) {   // lane 0 only
-        const int32_t j = warp + k * C::kWarps;
+        const int32_t c = warp + k * C::kWarps;
         const int32_t st = k % C::kStages;
         const uint32_t bar = bar0 + 8 * st;
-        const int32_t id = ids[j];
+        const int32_t blk = c / cpb;
+        const int32_t id = ids[blk];
         if (id >= 0) {
             const uint32_t dst = ring_u + st * C::kStageBytes;
+            const int32_t y = (c - blk * cpb) * C::kChunk;
             const int32_t z = id * hkv + g;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar, C::kStageBytes);
 #pragma unroll
             for (int b = 0; b < C::kBoxes; ++b)
-                tma_load_3d_hint(dst + b * C::kBoxBytes, &tmap_k, b * C::kBoxCols, 0, z, bar,
+                tma_load_3d_hint(dst + b * C::kBoxBytes, &tmap_k, b * C::kBoxCols, y, z, bar,
                                  policy);
 #pragma unroll
             for (int b = 0; b < C::kBoxes; ++b)
                 tma_load_3d_hint(dst + C::kTileBytes + b * C::kBoxBytes, &tmap_v,
-                                 b * C::kBoxCols, 0, z, bar, policy);
+                                 b * C::kBoxCols, y, z, bar, policy);
         } else {
             mbar_arrive(bar);
         }
@@ -181,31 +228,31 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             failed = true;
             break;
         }
-        const int32_t j = warp + k * C::kWarps;
-        if (ids[j] >= 0) {
+        const int32_t c = warp + k * C::kWarps;
+        if (ids[c / cpb] >= 0) {
             const uint32_t kb = ring_u + st * C::kStageBytes;
             const uint32_t vb = kb + C::kTileBytes;
-            const int32_t nvalid = min(BS, n - j * BS);
-            if (nvalid < BS) {
+            const int32_t nvalid = min(C::kChunk, n - c * C::kChunk);
+            if (nvalid < C::kChunk) {
                 // Unused rows of a sequence's last block may hold anything
                 // (even NaN); their weights are 0, so clear their V rows.
                 uint8_t* vt = sm + warp * C::kStages * C::kStageBytes + st * C::kStageBytes +
                               C::kTileBytes;
-                const int32_t chunks = (BS - nvalid) * 8;   // 16-byte chunks per box
-                for (int32_t c = lane; c < C::kBoxes * chunks; c += 32) {
-                    const int32_t b = c / chunks, r = c - b * chunks;
+                const int32_t chunks = (C::kChunk - nvalid) * 8;   // 16-byte pieces per box
+                for (int32_t x = lane; x < C::kBoxes * chunks; x += 32) {
+                    const int32_t b = x / chunks, r = x - b * chunks;
                     *reinterpret_cast<uint4*>(vt + b * C::kBoxBytes + nvalid * 128 + r * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 __syncwarp();
             }
 
-            float s[C::kSub][2][4];
+            // S = Q . K^T for the 16 tokens of the chunk (two n-tiles of 8)
+            float s[2][4];
 #pragma unroll
-            for (int u = 0; u < C::kSub; ++u) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) s[u][nt][0] = s[u][nt][1] = s[u][nt][2] = s[u][nt][3] = 0.f;
-                const int tok = u * 16 + (lm >> 1) * 8 + lr;
+            for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            {
+                const int tok = (lm >> 1) * 8 + lr;
 #pragma unroll
                 for (int ks = 0; ks < C::kKSteps; ++ks) {
                     const int ch = ((ks & 3) << 1) + (lm & 1);
@@ -213,26 +260,24 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         kb + (ks >> 2) * C::kBoxBytes + tok * 128 + ((ch ^ (tok & 7)) << 4);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(addr, b0, b1, b2, b3);
-                    mma_bf16_16816(s[u][0], qa[ks], b0, b1);
-                    mma_bf16_16816(s[u][1], qa[ks], b2, b3);
+                    mma_bf16_16816(s[0], qa[ks], b0, b1);
+                    mma_bf16_16816(s[1], qa[ks], b2, b3);
                 }
             }
             // scale, mask, row max
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int u = 0; u < C::kSub; ++u)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const bool valid = u * 16 + nt * 8 + 2 * tig + e < nvalid;
-                        s[u][nt][e] = valid ? s[u][nt][e] * a.scale_log2 : -INFINITY;
-                        mx0 = fmaxf(mx0, s[u][nt][e]);
-                        if (G16) {
-                            s[u][nt][2 + e] = valid ? s[u][nt][2 + e] * a.scale_log2 : -INFINITY;
-                            mx1 = fmaxf(mx1, s[u][nt][2 + e]);
-                        }
+                for (int e = 0; e < 2; ++e) {
+                    const bool valid = nt * 8 + 2 * tig + e < nvalid;
+                    s[nt][e] = valid ? s[nt][e] * a.scale_log2 : -INFINITY;
+                    mx0 = fmaxf(mx0, s[nt][e]);
+                    if (G16) {
+                        s[nt][2 + e] = valid ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
+                        mx1 = fmaxf(mx1, s[nt][2 + e]);
                     }
+                }
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             const float mn0 = fmaxf(m0, mx0);
@@ -248,18 +293,16 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
             float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-            for (int u = 0; u < C::kSub; ++u)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        s[u][nt][e] = exp2f(s[u][nt][e] - m0);
-                        rs0 += s[u][nt][e];
-                        if (G16) {
-                            s[u][nt][2 + e] = exp2f(s[u][nt][2 + e] - m1);
-                            rs1 += s[u][nt][2 + e];
-                        }
+                for (int e = 0; e < 2; ++e) {
+                    s[nt][e] = exp2f(s[nt][e] - m0);
+                    rs0 += s[nt][e];
+                    if (G16) {
+                        s[nt][2 + e] = exp2f(s[nt][2 + e] - m1);
+                        rs1 += s[nt][2 + e];
                     }
+                }
             l0 = l0 * al0 + rs0;
             if (G16) l1 = l1 * al1 + rs1;
 #pragma unroll
@@ -271,15 +314,14 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     acc[nd][3] *= al1;
                 }
             }
-            // acc += P . V
-#pragma unroll
-            for (int u = 0; u < C::kSub; ++u) {
-                uint32_t pf[4];
-                pf[0] = pack_bf16x2(s[u][0][0], s[u][0][1]);
-                pf[1] = G16 ? pack_bf16x2(s[u][0][2], s[u][0][3]) : 0u;
-                pf[2] = pack_bf16x2(s[u][1][0], s[u][1][1]);
-                pf[3] = G16 ? pack_bf16x2(s[u][1][2], s[u][1][3]) : 0u;
-                const int tok = u * 16 + (lm & 1) * 8 + lr;
+            // acc += P . V (P reused from the S registers as the A operand)
+            uint32_t pf[4];
+            pf[0] = pack_bf16x2(s[0][0], s[0][1]);
+            pf[1] = G16 ? pack_bf16x2(s[0][2], s[0][3]) : 0u;
+            pf[2] = pack_bf16x2(s[1][0], s[1][1]);
+            pf[3] = G16 ? pack_bf16x2(s[1][2], s[1][3]) : 0u;
+            {
+                const int tok = (lm & 1) * 8 + lr;
 #pragma unroll
                 for (int dp = 0; dp < D / 16; ++dp) {
                     const int chunk = 2 * dp + (lm >> 1);
@@ -296,6 +338,7 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (lane == 0 && k + C::kStages < my_count) issue(k + C::kStages);
     }
 
+    griddep_launch_dependents();   // the merge kernel may be scheduled now
     if (failed) {
         // drain this warp's copies still in flight (bounded), then report
         const int32_t last = min(my_count, k + C::kStages);

@@ -10,12 +10,23 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "decode_generic.cuh"
 #include "decode_tma_mma.cuh"
 #include "merge.cuh"
 #include "write_kv.cuh"
+
+#ifndef PA_USE_PDL
+#define PA_USE_PDL 1   // launch with programmatic stream serialization
+#endif
+#ifndef PA_TARGET_CTAS_PER_SM
+#define PA_TARGET_CTAS_PER_SM 8
+#endif
+#ifndef PA_MAX_PARTITION_TOKENS
+#define PA_MAX_PARTITION_TOKENS 1024
+#endif
 
 namespace pa {
 namespace {
@@ -49,8 +60,7 @@ bool fast_shape(const pa_cache_desc* c, int32_t group) {
     if (c->dtype != PA_BF16 || group < 1 || group > 16) return false;
     const int D = c->head_dim, B = c->block_size;
     if (D != 64 && D != 128) return false;
-    if (B != 16 && B != 32 && B != 64) return false;
-    return B * D <= 4096;
+    return B % 16 == 0 && B <= 256;
 }
 
 // Largest partition (tokens) the generic kernel's shared memory holds.
@@ -77,14 +87,16 @@ int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_le
         int32_t want = std::max(B, (512 / B) * B);
         return std::max(B, std::min(cap, want));
     }
-    // one block per warp per step; aim for about 8 CTAs per SM over the
-    // batch (counted at max_seq_len), between 4 blocks and 1024 tokens
+    // one block per warp per step; aim for about PA_TARGET_CTAS_PER_SM CTAs
+    // per SM over the batch (counted at max_seq_len), between 4 blocks and
+    // PA_MAX_PARTITION_TOKENS tokens
     const int64_t unit = 4LL * B;
     const int64_t sms = std::max(1, device_sm_count());
     const int64_t work = (int64_t)num_seqs * c->num_kv_heads * std::max(max_seq_len, 1);
-    int64_t p = (work + 8 * sms - 1) / (8 * sms);
+    const int64_t target = (int64_t)PA_TARGET_CTAS_PER_SM * sms;
+    int64_t p = (work + target - 1) / target;
     p = (p + unit - 1) / unit * unit;
-    const int64_t cap = std::max<int64_t>(unit, 1024 / unit * unit);
+    const int64_t cap = std::max<int64_t>(unit, PA_MAX_PARTITION_TOKENS / unit * unit);
     p = std::min(std::max(p, unit), cap);
     p = std::min<int64_t>(p, fast_max_partition(c));
     return (int32_t)p;
@@ -121,7 +133,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Cache viewed as 3-D: (head_dim, block_size, num_blocks * Hkv); one box is a
-// 64-column (128-byte) slice of one (block, head) tile, swizzled 128 B.
+// 64-column (128-byte) slice of 16 rows of one (block, head) tile, swizzled
+// 128 B.
 bool encode_cache_map(CUtensorMap* map, const void* base, const pa_cache_desc* c) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -129,7 +142,7 @@ bool encode_cache_map(CUtensorMap* map, const void* base, const pa_cache_desc* c
                           (cuuint64_t)c->num_blocks * (cuuint64_t)c->num_kv_heads};
     cuuint64_t strides[2] = {(cuuint64_t)c->head_dim * 2,
                              (cuuint64_t)c->head_dim * 2 * (cuuint64_t)c->block_size};
-    cuuint32_t box[3] = {64, (cuuint32_t)c->block_size, 1};
+    cuuint32_t box[3] = {64, 16, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -160,6 +173,25 @@ bool cached_map(CUtensorMap* out, const void* base, const pa_cache_desc* c, int 
 
 // ---- launches ------------------------------------------------------------------
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel in the stream finishes; it waits for that kernel
+// (griddepcontrol.wait) before reading any input.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PA_USE_PDL ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <typename Kern>
 bool set_smem(Kern kern, size_t bytes) {
     if (bytes <= 48 * 1024) return true;
@@ -167,32 +199,24 @@ bool set_smem(Kern kern, size_t bytes) {
                                 (int)bytes) == cudaSuccess;
 }
 
-template <int D, int BS, bool G16>
+template <int D, bool G16>
 cudaError_t launch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
                         const DecodeArgs& a, cudaStream_t st) {
-    using C = TmaMmaCfg<D, BS, G16>;
-    auto kern = decode_tma_mma_kernel<D, BS, G16>;
-    const size_t smem = C::smem_bytes();
-    if (!set_smem(kern, smem)) return cudaErrorInvalidValue;
-    kern<<<grid, C::kThreads, smem, st>>>(mk, mv, a);
-    return cudaGetLastError();
-}
-
-template <int D, int BS>
-cudaError_t launch_fast_g(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
-                          const DecodeArgs& a, cudaStream_t st) {
-    return a.group > 8 ? launch_fast<D, BS, true>(grid, mk, mv, a, st)
-                       : launch_fast<D, BS, false>(grid, mk, mv, a, st);
+    using C = TmaMmaCfg<D, G16>;
+    auto kern = decode_tma_mma_kernel<D, G16>;
+    if (!set_smem(kern, C::smem_bytes_max())) return cudaErrorInvalidValue;
+    const size_t smem = C::smem_bytes(a.part_tokens, a.block_size);
+    return launch_pdl(kern, grid, dim3(C::kThreads), smem, st, mk, mv, a);
 }
 
 cudaError_t dispatch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
                           const DecodeArgs& a, cudaStream_t st) {
-    switch (a.head_dim * 1000 + a.block_size) {
-        case 64016: return launch_fast_g<64, 16>(grid, mk, mv, a, st);
-        case 64032: return launch_fast_g<64, 32>(grid, mk, mv, a, st);
-        case 64064: return launch_fast_g<64, 64>(grid, mk, mv, a, st);
-        case 128016: return launch_fast_g<128, 16>(grid, mk, mv, a, st);
-        case 128032: return launch_fast_g<128, 32>(grid, mk, mv, a, st);
+    const bool g16 = a.group > 8;
+    switch (a.head_dim) {
+        case 64: return g16 ? launch_fast<64, true>(grid, mk, mv, a, st)
+                            : launch_fast<64, false>(grid, mk, mv, a, st);
+        case 128: return g16 ? launch_fast<128, true>(grid, mk, mv, a, st)
+                             : launch_fast<128, false>(grid, mk, mv, a, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -229,29 +253,30 @@ pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
     const uint8_t* vp = static_cast<const uint8_t*>(v);
     uint8_t* kc = static_cast<uint8_t*>(k_cache);
     uint8_t* vc = static_cast<uint8_t*>(v_cache);
+    cudaError_t err;
     switch (vec) {
         case 16:
-            write_kv_kernel<16><<<(unsigned)blocks, threads, 0, st>>>(
-                kp, vp, slot_mapping, num_tokens, kc, vc, cache->num_kv_heads,
-                cache->block_size, num_slots, row);
+            err = launch_pdl(write_kv_kernel<16>, dim3((unsigned)blocks), dim3(threads), 0, st,
+                             kp, vp, slot_mapping, (int64_t)num_tokens, kc, vc,
+                             cache->num_kv_heads, cache->block_size, num_slots, row);
             break;
         case 8:
-            write_kv_kernel<8><<<(unsigned)blocks, threads, 0, st>>>(
-                kp, vp, slot_mapping, num_tokens, kc, vc, cache->num_kv_heads,
-                cache->block_size, num_slots, row);
+            err = launch_pdl(write_kv_kernel<8>, dim3((unsigned)blocks), dim3(threads), 0, st,
+                             kp, vp, slot_mapping, (int64_t)num_tokens, kc, vc,
+                             cache->num_kv_heads, cache->block_size, num_slots, row);
             break;
         case 4:
-            write_kv_kernel<4><<<(unsigned)blocks, threads, 0, st>>>(
-                kp, vp, slot_mapping, num_tokens, kc, vc, cache->num_kv_heads,
-                cache->block_size, num_slots, row);
+            err = launch_pdl(write_kv_kernel<4>, dim3((unsigned)blocks), dim3(threads), 0, st,
+                             kp, vp, slot_mapping, (int64_t)num_tokens, kc, vc,
+                             cache->num_kv_heads, cache->block_size, num_slots, row);
             break;
         default:
-            write_kv_kernel<2><<<(unsigned)blocks, threads, 0, st>>>(
-                kp, vp, slot_mapping, num_tokens, kc, vc, cache->num_kv_heads,
-                cache->block_size, num_slots, row);
+            err = launch_pdl(write_kv_kernel<2>, dim3((unsigned)blocks), dim3(threads), 0, st,
+                             kp, vp, slot_mapping, (int64_t)num_tokens, kc, vc,
+                             cache->num_kv_heads, cache->block_size, num_slots, row);
             break;
     }
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int32_t pa_decode_path(int32_t num_q_heads, const pa_cache_desc* cache) {
@@ -345,22 +370,21 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
         const size_t smem = generic_smem_bytes(group, cache->head_dim, part, B);
         if (cache->dtype == PA_F32) {
             if (!set_smem(decode_generic_kernel<float>, smem)) return PA_ERR_UNSUPPORTED;
-            decode_generic_kernel<float><<<grid, 128, smem, st>>>(a);
+            err = launch_pdl(decode_generic_kernel<float>, grid, dim3(128), smem, st, a);
         } else {
             if (!set_smem(decode_generic_kernel<__nv_bfloat16>, smem)) return PA_ERR_UNSUPPORTED;
-            decode_generic_kernel<__nv_bfloat16><<<grid, 128, smem, st>>>(a);
+            err = launch_pdl(decode_generic_kernel<__nv_bfloat16>, grid, dim3(128), smem, st, a);
         }
-        err = cudaGetLastError();
     }
     if (err != cudaSuccess) return PA_ERR_CUDA;
     if (max_parts > 1) {
-        const int warps = 4;
-        const unsigned mblocks = (unsigned)(((int64_t)num_seqs * num_q_heads + warps - 1) / warps);
-        if (cache->dtype == PA_F32)
-            merge_kernel<float><<<mblocks, 32 * warps, 0, st>>>(a);
-        else
-            merge_kernel<__nv_bfloat16><<<mblocks, 32 * warps, 0, st>>>(a);
-        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+        const unsigned mblocks = (unsigned)((int64_t)num_seqs * num_q_heads);
+        const cudaError_t merr =
+            cache->dtype == PA_F32
+                ? launch_pdl(merge_kernel<float>, dim3(mblocks), dim3(kMergeThreads), 0, st, a)
+                : launch_pdl(merge_kernel<__nv_bfloat16>, dim3(mblocks), dim3(kMergeThreads), 0,
+                             st, a);
+        if (merr != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
 }

@@ -95,6 +95,21 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------------
+
+// Blocks until every grid this launch depends on has completed and its memory
+// is visible.  Kernels launched with programmatic stream serialization call
+// this before reading anything an earlier kernel may have written.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream (launched with programmatic stream
+// serialization) be scheduled before this grid finishes.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- ldmatrix / mma -----------------------------------------------------------
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,

@@ -9,6 +9,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace pa {
 
@@ -31,6 +32,8 @@ write_kv_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
                 int32_t num_kv_heads, int32_t block_size, int64_t num_slots,
                 int32_t row_bytes) {
     using V = typename VecType<VEC>::T;
+    griddep_wait();                 // inputs may come from the previous kernel
+    griddep_launch_dependents();    // the next kernel may start its prologue
     const int64_t vecs_per_row = row_bytes / VEC;
     const int64_t per_token = 2LL * num_kv_heads * vecs_per_row;
     const int64_t total = num_tokens * per_token;

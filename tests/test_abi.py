@@ -55,7 +55,10 @@ def test_path_selection(lib):
     assert path(128, desc(bs=32)) == 1                 # G=16
     assert path(256, desc()) == 0                      # G=32: portable kernel
     assert path(32, desc(dtype=pa.PA_F32)) == 0        # fp32: portable kernel
-    assert path(32, desc(bs=64)) == 0                  # B*D > 4096
+    assert path(32, desc(bs=64)) == 1                  # B=64: four 16-token chunks
+    assert path(32, desc(bs=48)) == 1
+    assert path(32, desc(bs=8)) == 0                   # B not a multiple of 16
+    assert path(32, desc(bs=512)) == 0
     assert path(16, desc(d=64, bs=64, hkv=4)) == 1
     assert path(8, desc(d=8, bs=4, hkv=2, dtype=pa.PA_F32)) == 0
     assert path(30, desc()) == -1                      # Hq not a multiple of Hkv

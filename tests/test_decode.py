@@ -90,6 +90,9 @@ FAST_CASES = [
     (10, 2, 64, 32, (1, 64, 65, 250)),                             # G=5, D=64
     (8, 4, 64, 64, (1, 63, 64, 65, 129, 400)),                     # G=2, B=64
     (9, 1, 64, 16, (2, 100)),                                      # G=9
+    (32, 8, 128, 48, (1, 47, 48, 49, 300)),                        # B=48: 3 chunks/block
+    (32, 8, 128, 128, (5, 127, 128, 129, 1000)),                   # B=128
+    (64, 8, 128, 64, (64, 65, 777)),                               # G=8, B=64
 ]
 
 
@@ -177,6 +180,20 @@ def test_split_on_off_agree_and_runs_are_deterministic(cuda_device):
     auto1 = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale)
     auto2 = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale)
     assert torch.equal(auto1, auto2)
+
+
+@pytest.mark.parametrize("dtype,d,hq,hkv", [(torch.bfloat16, 128, 32, 8),
+                                             (torch.float32, 64, 8, 4)])
+def test_many_partitions_merge(cuda_device, dtype, d, hq, hkv):
+    """More partitions than the merge stages per pass (>512 here), and the
+    few-partition path, on both kernels."""
+    q, kc, vc, bt, sl = synthetic(hq, hkv, d, 16, (9000, 33, 17 * 16 + 5), dtype=dtype, seed=15)
+    scale = 1 / math.sqrt(d)
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    atol, rtol = tolerance(dtype)
+    for part in (16, 48, 560):
+        out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=part)
+        assert_close(out.double().numpy(), ref, atol, rtol, f"partitions of {part}")
 
 
 def test_relabelling_physical_blocks_changes_nothing(cuda_device):
