@@ -47,6 +47,11 @@ WORKLOAD_TEXT = {
     "cb": "continuous batching bf16: 256 seqs, Hq=32, Hkv=8, D=128, B=16, T0~U[1,4096]; "
           "step = write 2304 tokens (1 per seq + 2048-token chunk) + decode all 256; "
           "10 distinct steps cycled",
+    "copy": "block copy inside one pool (copy-on-write), bf16: 8192 disjoint (src, dst) pairs "
+            "of B=16, Hkv=8, D=128 blocks (64 KiB of K+V each) in a 65536-block pool; "
+            "step = one pa_copy_blocks call",
+    "swap": "swap through page-locked host memory, bf16: 2048 blocks of B=16, Hkv=8, D=128 "
+            "out to a host pool and 2048 back; step = two pa_copy_blocks calls",
 }
 
 
@@ -150,7 +155,7 @@ class ClockSampler:
 
 
 KERNEL_SOURCES = ("decode_tma_mma.cuh", "ptx.cuh", "merge.cuh", "decode_generic.cuh",
-                  "common.cuh", "pa.cu")
+                  "common.cuh", "decode_config.cuh")
 
 
 def kernel_source_hash() -> str:
@@ -211,6 +216,24 @@ def time_oracle(wl, budget_s: float, max_reps: int = 50) -> dict:
                       f"{elapsed:.1f} s"}
 
 
+def time_oracle_copy(args) -> dict:
+    """The oracle's block copy on the host, repeated for ~cpu_seconds."""
+    import oracle
+    wl = workloads.copy_pairs() if args.workload == "copy" else \
+        workloads.copy_pairs(num_blocks=8192, num_pairs=2048)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.copy_blocks(wl.k_cache, wl.v_cache, wl.k_cache, wl.v_cache, wl.pairs)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= args.cpu_seconds or reps >= max(1, args.steps):
+            break
+    return {"value": reps * wl.copy_bytes() / el / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "seconds": round(el, 3), "steps": reps,
+            "sample": f"{reps} oracle block-copy call(s) of {wl.pairs.shape[0]} pairs "
+                      "(sequential memcpy), 1 thread"}
+
+
 # ---- GPU arm ------------------------------------------------------------------------
 
 def run_ours(args, rank, world, device):
@@ -223,7 +246,8 @@ def run_ours(args, rank, world, device):
     dsteps = []
     for st in wl.steps:
         dsteps.append({k: getattr(st, k).to(device) for k in
-                       ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens")})
+                       ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens",
+                        "seq_ids", "positions")})
     bytes_ = [step_bytes(wl, k) for k in range(nsteps_wl)]
     maxlens = [int(st.seq_lens.max()) for st in wl.steps]
     part = args.partition or 0
@@ -235,7 +259,11 @@ def run_ours(args, rank, world, device):
 
     def step(k, ev=None):
         d = dsteps[k]
-        pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
+        if args.positions:
+            pa.write_kv_positions(d["k_new"], d["v_new"], d["seq_ids"], d["positions"],
+                                  d["block_tables"], kc, vc)
+        else:
+            pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
         if ev is not None:
             ev[0].record(stream)
         pa.decode(d["q"], kc, vc, d["block_tables"], d["seq_lens"], maxlens[k], wl.scale,
@@ -308,6 +336,8 @@ def run_ours(args, rank, world, device):
         "data": "synthetic (seeded N(0,1) K/V/q; tables from a shuffled block pool)",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
                    "overrides": overrides(args) or None,
+                   "write": "device slots from (seq, position)" if args.positions
+                            else "slot_mapping",
                    "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
                    "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                    "block_size": wl.block_size, "max_seq_len": max(maxlens),
@@ -334,6 +364,102 @@ def run_ours(args, rank, world, device):
         "cpu_baseline": cpu,
     }
     return result
+
+
+def run_copy(args, rank, world, device):
+    """Block copies: `copy` inside the device pool (HBM read + write), `swap`
+    out to page-locked host memory and back (bound by the host link)."""
+    import paged_kv_cache_109_gb300 as pa
+    pa.load_library()
+    stream = torch.cuda.current_stream(device)
+    if args.workload == "copy":
+        wl = workloads.copy_pairs()
+        kc, vc = wl.k_cache.to(device), wl.v_cache.to(device)
+        pairs = wl.pairs.to(device)
+        calls = [(kc, vc, kc, vc, pairs)]
+        step_bytes_ = wl.copy_bytes()
+    else:
+        wl = workloads.copy_pairs(num_blocks=8192, num_pairs=2048, fill=True)
+        kc, vc = wl.k_cache.to(device), wl.v_cache.to(device)
+        host_k = torch.empty((2048,) + tuple(wl.k_cache.shape[1:]), dtype=wl.k_cache.dtype)
+        host_k = host_k.pin_memory()
+        host_v = torch.empty_like(host_k).pin_memory()
+        to_host = torch.stack([wl.pairs[:, 0], torch.arange(2048)], 1).to(device)
+        from_host = torch.stack([torch.arange(2048), wl.pairs[:, 1]], 1).to(device)
+        calls = [(kc, vc, host_k, host_v, to_host), (host_k, host_v, kc, vc, from_host)]
+        step_bytes_ = 2 * wl.copy_bytes()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        for c in calls:
+            pa.copy_blocks(*c)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    K = args.steps
+    sampled = list(range(0, K, DEC_SAMPLE))
+    evs = {it: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for it in sampled}
+    with ClockSampler(device.index or 0) as clocks:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for it in range(K):
+            step(evs.get(it))
+        end.record(stream)
+        torch.cuda.synchronize(device)
+    total_ms = start.elapsed_time(end)
+    if pa.last_device_error() != 0:
+        raise RuntimeError("device error flag raised in the timed region")
+    call_ms = [evs[it][0].elapsed_time(evs[it][1]) for it in sampled]
+    achieved = step_bytes_ / (statistics.mean(call_ms) / 1e3) / 1e9
+    value = world * K * step_bytes_ / (total_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    if args.workload == "copy":
+        roof = {"bound": "hbm", "kernel": "pa_copy_blocks call", "achieved": round(achieved, 2),
+                "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind} (a copy, like this kernel)",
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None}
+    else:
+        roof = {"bound": "host link", "kernel": "pa_copy_blocks calls (out + in)",
+                "achieved": round(achieved, 2), "peak": None, "unit": "GB/s", "frac": None,
+                "traffic": None, "note": "device <-> page-locked host copies; no HBM roofline"}
+    # end to end: pairs from pinned host memory each step, one block read back
+    host_pairs = [c[4].cpu().pin_memory() for c in calls]
+    dev_pairs = [torch.empty_like(c[4]) for c in calls]
+    probe = torch.empty(calls[0][2][0].shape, dtype=calls[0][2].dtype).pin_memory()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K2 = max(1, min(K, 200))
+    s2.record(stream)
+    for _ in range(K2):
+        for c, hp, dp in zip(calls, host_pairs, dev_pairs):
+            dp.copy_(hp, non_blocking=True)
+            pa.copy_blocks(c[0], c[1], c[2], c[3], dp)
+        probe.copy_(calls[-1][2][0], non_blocking=True)
+    e2.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = s2.elapsed_time(e2) / K2
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) blocks, shuffled pool)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+                   "pairs_per_call": int(calls[0][4].shape[0]),
+                   "l2": f"inputs larger than L2: {step_bytes_ / 2 / 2**20:.0f} MiB read per step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "bytes_per_step": step_bytes_,
+        "roofline": roof,
+        "e2e": {"value": round(step_bytes_ / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": sum(h.numel() * 8 for h in host_pairs),
+                "d2h_bytes_per_step": probe.numel() * probe.element_size(), "steps": K2},
+        "gpu_launches": K * len(calls),
+        "clocks": clocks.summary(),
+        "cpu_baseline": None,
+    }
 
 
 def run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_):
@@ -392,6 +518,17 @@ def run_reference(args, rank):
     """The oracle as the reference arm: bounded full steps on the host cores."""
     if rank != 0:
         return None
+    if args.workload in ("copy", "swap"):
+        cpu = time_oracle_copy(args)
+        return {"impl": "reference", "metric": METRIC, "value": round(cpu["value"], 4),
+                "unit": "GB/s", "n_gpus": 0, "steps": cpu["steps"], "warmup": 0,
+                "ms_per_step": round(1e3 * cpu["seconds"] / cpu["steps"], 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+                "cpu_baseline": cpu,
+                "e2e": {"value": round(cpu["value"], 4), "unit": "GB/s",
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     wl = workloads.make(args.workload, **overrides(args))
     steps = max(1, args.steps)
     cpu = time_oracle(wl, args.cpu_seconds, max_reps=steps)
@@ -419,6 +556,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="smaller batch (profiling); the JSON line then has no traffic")
     ap.add_argument("--num-blocks", type=int, default=0, help="smaller block pool (profiling)")
+    ap.add_argument("--positions", action="store_true",
+                    help="write with slots computed on the device from (seq, position)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -435,7 +574,7 @@ def main():
     torch.cuda.set_device(device)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
-    res = run_ours(args, rank, world, device)
+    res = (run_copy if args.workload in ("copy", "swap") else run_ours)(args, rank, world, device)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -71,6 +71,7 @@ typedef struct {
 #define PA_DEVERR_SEQ_LEN     2u  /* seq_lens[i] > max_seq_len or > max_blocks*B     */
 #define PA_DEVERR_SLOT        4u  /* a slot was >= num_blocks * block_size            */
 #define PA_DEVERR_TIMEOUT     8u  /* a pipeline wait gave up after its bound          */
+#define PA_DEVERR_BLOCK_PAIR 16u  /* a copy pair named a block outside its cache       */
 
 /*
  * pa_write_kv -- cache write through slot_mapping.
@@ -88,6 +89,51 @@ typedef struct {
 pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
                       int32_t num_tokens, void* k_cache, void* v_cache,
                       const pa_cache_desc* cache, void* stream);
+
+/*
+ * pa_write_kv_positions -- the same cache write, with each token's slot
+ * computed on the device from its sequence and position through the block
+ * table ("vLLM PagedAttention: from memory fragmentation to slot mapping" §6:
+ * positions and the device block table give the slot mapping; §3: slot =
+ * table[pos / B] * B + pos % B).
+ *
+ * seq_ids, positions  device int32 [num_tokens]; token j belongs to sequence
+ *               seq_ids[j] at position positions[j].  A negative id or
+ *               position means "skip"; an id >= num_seqs, a position past the
+ *               table, or a table entry outside [0, num_blocks) is skipped and
+ *               reported (PA_DEVERR_TABLE_ENTRY).
+ * block_tables  device int32 [num_seqs][max_blocks_per_seq].
+ * Other arguments as pa_write_kv.
+ */
+pa_status pa_write_kv_positions(const void* k, const void* v, const int32_t* seq_ids,
+                                const int32_t* positions, int32_t num_tokens,
+                                const int32_t* block_tables, int32_t num_seqs,
+                                int32_t max_blocks_per_seq, void* k_cache, void* v_cache,
+                                const pa_cache_desc* cache, void* stream);
+
+/*
+ * pa_copy_blocks -- whole-block copies for copy-on-write and swapping
+ * (PagedAttention engineering notes, nxmr.cn, §4.2: before a shared, partly
+ * filled block is written, take a new block and copy the old block's K/V into
+ * it; paper notes on swapping: a preempted sequence's blocks move to CPU
+ * memory and back).
+ *
+ * src_k, src_v  source caches, src_num_blocks blocks of the geometry `cache`
+ *               describes (its num_blocks field is not used here).
+ * dst_k, dst_v  destination caches, dst_num_blocks blocks; may be the source
+ *               caches themselves (copy-on-write inside one pool).
+ * block_pairs   int64 [num_pairs][2] of (src block, dst block), copied as if in
+ *               order; a destination must not appear twice nor be a source in
+ *               the same call (those copies race).  Pairs outside either pool
+ *               are skipped and reported (PA_DEVERR_BLOCK_PAIR).
+ * Every pointer may be device memory or page-locked host memory (a swap pool
+ * allocated with cudaHostAlloc or registered with cudaHostRegister); pageable
+ * host memory is refused with PA_ERR_INVALID_ARG.  Bit-exact.
+ */
+pa_status pa_copy_blocks(const void* src_k, const void* src_v, int32_t src_num_blocks,
+                         void* dst_k, void* dst_v, int32_t dst_num_blocks,
+                         const int64_t* block_pairs, int32_t num_pairs,
+                         const pa_cache_desc* cache, void* stream);
 
 /*
  * Partition size (tokens, a multiple of block_size) that pa_decode uses when

@@ -73,6 +73,10 @@ def load(path: str | None = None):
     lib.oracle_merge.restype = None
     lib.oracle_write_kv.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, I32]
     lib.oracle_write_kv.restype = I64
+    lib.oracle_copy_blocks.argtypes = [P, P, I32, P, P, I32, P, I64, I64]
+    lib.oracle_copy_blocks.restype = I64
+    lib.oracle_slots_from_positions.argtypes = [P, P, I64, P, I32, I32, I32, P]
+    lib.oracle_slots_from_positions.restype = None
     lib.oracle_set_threads.argtypes = [I32]
     lib.oracle_set_threads.restype = None
     lib.oracle_max_threads.argtypes = []
@@ -256,6 +260,36 @@ def write_kv(k, v, slot_mapping, k_cache, v_cache) -> int:
     nb, hkv, bs, d = _cache_geometry(k_cache)
     return int(load().oracle_write_kv(_ptr(ka), _ptr(va), _ptr(sm), sm.shape[0], _ptr(kc),
                                       _ptr(vc), nb, bs, hkv, d, ka.itemsize))
+
+
+def copy_blocks(src_k, src_v, dst_k, dst_v, pairs) -> int:
+    """Copy whole blocks src -> dst for each (src, dst) row of ``pairs`` (in
+    order), from the source caches into the destination caches (host, written
+    in place; may be the same tensors).  Returns the count of rejected pairs."""
+    for c in (dst_k, dst_v):
+        contiguous = c.is_contiguous() if hasattr(c, "is_contiguous") else c.flags.c_contiguous
+        if not contiguous:
+            raise ValueError("destination caches must be contiguous host buffers")
+    sk, _ = _as_array(src_k)
+    sv, _ = _as_array(src_v)
+    dk, _ = _as_array(dst_k)
+    dv, _ = _as_array(dst_v)
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    block_bytes = sk.itemsize * int(np.prod(src_k.shape[1:]))
+    return int(load().oracle_copy_blocks(_ptr(sk), _ptr(sv), int(src_k.shape[0]), _ptr(dk),
+                                         _ptr(dv), int(dst_k.shape[0]), _ptr(pr), pr.shape[0],
+                                         block_bytes))
+
+
+def slots_from_positions(seq_ids, positions, block_tables, block_size: int) -> np.ndarray:
+    """int64 slots of tokens given by (sequence id, position) through the tables."""
+    si = _i32(seq_ids)
+    po = _i32(positions)
+    bt = _i32(block_tables)
+    out = np.empty(si.shape[0], dtype=np.int64)
+    load().oracle_slots_from_positions(_ptr(si), _ptr(po), si.shape[0], _ptr(bt), bt.shape[0],
+                                       bt.shape[1], block_size, _ptr(out))
+    return out
 
 
 def set_threads(n: int) -> None:

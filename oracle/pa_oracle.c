@@ -15,6 +15,8 @@
  *        reference": K/V are gathered by table into contiguous rows
  *        (gather_paged), then plain attention runs on them (attend_one);
  *        query heads are grouped with repeat_interleave (expand_kv).
+ *   [P3] PagedAttention engineering notes (nxmr.cn) §4.2: copy-on-write
+ *        copies a shared, partly filled block before it is written.
  *   [P4] "vLLM source walkthrough: PagedAttention and Continuous Batching"
  *        §1.8: the V2 kernel splits a sequence's blocks into partitions and
  *        a reduce step merges them.
@@ -297,6 +299,60 @@ int64_t oracle_write_kv(const void* k, const void* v, const int64_t* slot_mappin
         }
     }
     return rejected;
+}
+
+/* ---- block copy for copy-on-write and swap ------------------------------ */
+
+/*
+ * For each pair (src, dst) in index order, every byte of physical block src
+ * of the source K and V caches is copied to block dst of the destination
+ * caches.  A block is block_bytes contiguous bytes of a [num_blocks][...]
+ * cache.  This is the copy a copy-on-write performs before a shared, partly
+ * filled block is written (nxmr.cn article §4.2: take a new block, copy the
+ * old block's K/V into it, point the table at it), and the copy that swaps a
+ * preempted sequence's blocks between GPU and CPU memory (paper notes,
+ * swapping).  Pairs naming a block outside either cache are skipped and
+ * counted; the count is returned.
+ */
+int64_t oracle_copy_blocks(const void* src_k, const void* src_v, int32_t src_blocks,
+                           void* dst_k, void* dst_v, int32_t dst_blocks, const int64_t* pairs,
+                           int64_t num_pairs, int64_t block_bytes) {
+    int64_t rejected = 0;
+    for (int64_t j = 0; j < num_pairs; ++j) {
+        int64_t s = pairs[2 * j], d = pairs[2 * j + 1];
+        if (s < 0 || s >= src_blocks || d < 0 || d >= dst_blocks) {
+            rejected += 1;
+            continue;
+        }
+        memcpy((char*)dst_k + d * block_bytes, (const char*)src_k + s * block_bytes,
+               (size_t)block_bytes);
+        memcpy((char*)dst_v + d * block_bytes, (const char*)src_v + s * block_bytes,
+               (size_t)block_bytes);
+    }
+    return rejected;
+}
+
+/* ---- slots from (sequence, position) ------------------------------------ */
+
+/*
+ * slot of token j = table[seq_ids[j]][positions[j] / B] * B + positions[j] % B
+ * ("vLLM PagedAttention: from memory fragmentation to slot mapping" §3, §6:
+ * positions plus the block table give the slot mapping).  -1 when the
+ * sequence id or position is negative or outside the table, or the entry is
+ * negative.
+ */
+void oracle_slots_from_positions(const int32_t* seq_ids, const int32_t* positions,
+                                 int64_t num_tokens, const int32_t* block_tables,
+                                 int32_t num_seqs, int32_t max_blocks, int32_t block_size,
+                                 int64_t* slots) {
+    for (int64_t j = 0; j < num_tokens; ++j) {
+        int64_t s = seq_ids[j], p = positions[j];
+        if (s < 0 || s >= num_seqs || p < 0 || p >= (int64_t)max_blocks * block_size) {
+            slots[j] = -1;
+            continue;
+        }
+        slots[j] = oracle_slot(block_tables + s * max_blocks, block_size, p);
+    }
 }
 
 /* ---- threading --------------------------------------------------------- */

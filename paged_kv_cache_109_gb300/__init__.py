@@ -21,13 +21,13 @@ from ._build import LIB as LIBRARY_PATH
 from ._build import build
 from .block_pool import BlockPool, SharedTailWrite
 
-__all__ = ["write_kv", "decode", "decode_workspace_bytes", "decode_partition_tokens",
+__all__ = ["write_kv", "write_kv_positions", "copy_blocks", "decode", "decode_workspace_bytes", "decode_partition_tokens",
            "decode_path", "last_device_error", "PaError", "build", "BlockPool",
            "SharedTailWrite", "LIBRARY_PATH", "load_library", "CacheDesc"]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
 PA_F32, PA_BF16 = 0, 1
-DEVERR_TABLE_ENTRY, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_TABLE_ENTRY, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_BLOCK_PAIR = 1, 2, 4, 8, 16
 
 
 class CacheDesc(ctypes.Structure):
@@ -58,6 +58,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     DP = ctypes.POINTER(CacheDesc)
     lib.pa_write_kv.argtypes = [P, P, P, I32, P, P, DP, P]
     lib.pa_write_kv.restype = ctypes.c_int
+    lib.pa_write_kv_positions.argtypes = [P, P, P, P, I32, P, I32, I32, P, P, DP, P]
+    lib.pa_write_kv_positions.restype = ctypes.c_int
+    lib.pa_copy_blocks.argtypes = [P, P, I32, P, P, I32, P, I32, DP, P]
+    lib.pa_copy_blocks.restype = ctypes.c_int
     lib.pa_decode_partition_tokens.argtypes = [I32, I32, I32, DP]
     lib.pa_decode_partition_tokens.restype = I32
     lib.pa_decode_workspace_bytes.argtypes = [I32, I32, I32, I32, DP]
@@ -138,6 +142,52 @@ def write_kv(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
     st = load_library().pa_write_kv(_ptr(k), _ptr(v), _ptr(slot_mapping), n, _ptr(k_cache),
                                     _ptr(v_cache), ctypes.byref(desc), _stream(stream))
     _check(st, "pa_write_kv")
+
+
+def write_kv_positions(k, v, seq_ids, positions, block_tables, k_cache, v_cache,
+                       stream=None) -> None:
+    """Scatter k, v [n_tok, Hkv, D] to the slots of (seq_ids[j], positions[j])
+    through block_tables [N, max_blocks]; slots are computed on the device."""
+    _dev(k, v, seq_ids, positions, block_tables, k_cache, v_cache)
+    for t in (seq_ids, positions, block_tables):
+        if t.dtype != torch.int32:
+            raise ValueError("seq_ids, positions and block_tables must be int32")
+    if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k, v and caches must share one dtype")
+    desc = cache_desc(k_cache)
+    n = seq_ids.numel()
+    if positions.numel() != n or k.shape != (n, desc.num_kv_heads, desc.head_dim) \
+            or v.shape != k.shape:
+        raise ValueError("k, v, seq_ids and positions disagree on the token count")
+    st = load_library().pa_write_kv_positions(
+        _ptr(k), _ptr(v), _ptr(seq_ids), _ptr(positions), n, _ptr(block_tables),
+        block_tables.shape[0], block_tables.shape[1], _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(desc), _stream(stream))
+    _check(st, "pa_write_kv_positions")
+
+
+def _dev_or_pinned(*ts: torch.Tensor) -> None:
+    for t in ts:
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError("tensors must be on a CUDA device or in page-locked host memory")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def copy_blocks(src_k, src_v, dst_k, dst_v, pairs, stream=None) -> None:
+    """Copy whole blocks src -> dst for each row (src, dst) of ``pairs``
+    (int64 [n, 2]).  Caches may be device tensors or pinned host tensors
+    (swap space); the destination may be the source (copy-on-write)."""
+    _dev_or_pinned(src_k, src_v, dst_k, dst_v, pairs)
+    if pairs.dtype != torch.int64 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int64 [n, 2]")
+    if tuple(src_k.shape[1:]) != tuple(dst_k.shape[1:]) or src_k.dtype != dst_k.dtype:
+        raise ValueError("source and destination caches differ in block geometry")
+    desc = cache_desc(src_k)
+    st = load_library().pa_copy_blocks(
+        _ptr(src_k), _ptr(src_v), src_k.shape[0], _ptr(dst_k), _ptr(dst_v), dst_k.shape[0],
+        _ptr(pairs), pairs.shape[0], ctypes.byref(desc), _stream(stream))
+    _check(st, "pa_copy_blocks")
 
 
 def decode_partition_tokens(num_seqs: int, num_q_heads: int, max_seq_len: int,

@@ -16,8 +16,10 @@ Behaviour follows the pages:
 * position p of a sequence lives in slot table[p // B] * B + p % B
   (first page §3).
 
-Copy-on-write of a shared, partly filled tail block is refused here with
-``SharedTailWrite``: the device copy that would resolve it is a later step.
+A write into a shared, partly filled tail block is refused with
+``SharedTailWrite`` until ``copy_on_write`` has given the sequence a private
+copy; ``copy_on_write``, ``swap_out`` and ``swap_in`` return the block pairs
+the device copy (``pa_copy_blocks``) must move.
 """
 from __future__ import annotations
 
@@ -97,6 +99,63 @@ class BlockPool:
         table.extend(fresh)
         self.lengths[seq] = old_len + int(new_tokens)
         return fresh
+
+    def fork(self, parent: Hashable, child: Hashable) -> list[int]:
+        """``child`` starts as a copy of ``parent`` sharing every block,
+        including a partly filled tail (parallel sampling / beam search
+        branches: nxmr.cn article §4.1; paper notes, copy-on-write)."""
+        if child in self.tables:
+            raise KeyError(f"sequence {child!r} already present")
+        table = list(self.tables[parent])
+        for b in table:
+            self.ref_cnt[b] += 1
+        self.tables[child] = table
+        self.lengths[child] = self.lengths[parent]
+        return table
+
+    def copy_on_write(self, seq: Hashable) -> tuple[int, int] | None:
+        """Before ``seq`` appends into a partly filled tail block that other
+        sequences share, give it a private copy: take a fresh block, point the
+        table at it and drop one reference to the old block (nxmr.cn article
+        §4.2).  Returns the (old, new) pair whose K/V the device must copy,
+        or None when the tail is full or already private."""
+        n = self.lengths[seq]
+        table = self.tables[seq]
+        if n % self.block_size == 0 or not table:
+            return None
+        tail = table[-1]
+        if self.ref_cnt[tail] <= 1:
+            return None
+        fresh = self._take_fresh(1)[0]
+        self.ref_cnt[tail] -= 1
+        table[-1] = fresh
+        return tail, fresh
+
+    def swap_out(self, seq: Hashable, host: "BlockPool") -> list[tuple[int, int]]:
+        """Move ``seq``'s blocks to the host pool (paper notes, swapping):
+        returns the (device block, host block) pairs to copy; the device blocks
+        go back to this pool's free queue.  Every block must be private to
+        ``seq``.  All-or-nothing: MemoryError leaves both pools unchanged."""
+        table = self.tables[seq]
+        if any(self.ref_cnt[b] != 1 for b in table):
+            raise SharedTailWrite(f"sequence {seq!r} shares blocks; it cannot be swapped alone")
+        host_blocks = host._take_fresh(len(table))
+        host.tables[seq] = host_blocks
+        host.lengths[seq] = self.lengths[seq]
+        pairs = list(zip(table, host_blocks))
+        self.release(seq)
+        return pairs
+
+    def swap_in(self, seq: Hashable, host: "BlockPool") -> list[tuple[int, int]]:
+        """Bring ``seq`` back from the host pool: returns the (host block,
+        device block) pairs to copy; the host blocks are released."""
+        host_table = host.tables[seq]
+        fresh = self._take_fresh(len(host_table))
+        self.tables[seq] = fresh
+        self.lengths[seq] = host.lengths[seq]
+        pairs = list(zip(host_table, fresh))
+        host.release(seq)
+        return pairs
 
     def release(self, seq: Hashable) -> list[int]:
         """Drop ``seq``; blocks whose count reaches zero rejoin the free queue

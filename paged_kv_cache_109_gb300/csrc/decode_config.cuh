@@ -1,0 +1,104 @@
+// decode_config.cuh -- decode tuning knobs, kernel selection and split-K
+// sizing (host side).  The automatic partition size decides how many CTAs a
+// call launches and how many split partials it writes, so it belongs with
+// the kernels it configures.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "pa.h"
+
+#ifndef PA_USE_PDL
+#define PA_USE_PDL 1   // launch with programmatic stream serialization
+#endif
+#ifndef PA_TARGET_CTAS_PER_SM
+#define PA_TARGET_CTAS_PER_SM 8
+#endif
+#ifndef PA_MAX_PARTITION_TOKENS
+#define PA_MAX_PARTITION_TOKENS 1024
+#endif
+
+namespace pa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int device_sm_count() {
+    static int cached[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// ---- kernel selection --------------------------------------------------------
+
+bool fast_shape(const pa_cache_desc* c, int32_t group) {
+    if (c->dtype != PA_BF16 || group < 1 || group > 16) return false;
+    const int D = c->head_dim, B = c->block_size;
+    if (D != 64 && D != 128) return false;
+    return B % 16 == 0 && B <= 256;
+}
+
+// Largest partition (tokens) the generic kernel's shared memory holds.
+int32_t generic_max_partition(const pa_cache_desc* c, int32_t group) {
+    const size_t budget = 96 * 1024;
+    int32_t B = c->block_size;
+    int64_t fixed = 4LL * ((int64_t)group * c->head_dim + 2 * group);
+    int64_t per_tok = 4LL * group;
+    int64_t p = (int64_t(budget) - fixed) / per_tok;
+    p = p / B * B;
+    return (int32_t)std::max<int64_t>(p, 0);
+}
+
+int32_t fast_max_partition(const pa_cache_desc* c) {
+    return 2048 * c->block_size;   // TmaMmaCfg::kMaxTableSlice blocks
+}
+
+int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
+                       const pa_cache_desc* c) {
+    const int32_t B = c->block_size;
+    const int32_t group = num_q_heads / c->num_kv_heads;
+    if (!fast_shape(c, group)) {
+        int32_t cap = generic_max_partition(c, group);
+        int32_t want = std::max(B, (512 / B) * B);
+        return std::max(B, std::min(cap, want));
+    }
+    // one block per warp per step; aim for about PA_TARGET_CTAS_PER_SM CTAs
+    // per SM over the batch (counted at max_seq_len), between 4 blocks and
+    // PA_MAX_PARTITION_TOKENS tokens
+    const int64_t unit = 4LL * B;
+    const int64_t sms = std::max(1, device_sm_count());
+    const int64_t work = (int64_t)num_seqs * c->num_kv_heads * std::max(max_seq_len, 1);
+    const int64_t target = (int64_t)PA_TARGET_CTAS_PER_SM * sms;
+    int64_t p = (work + target - 1) / target;
+    p = (p + unit - 1) / unit * unit;
+    const int64_t cap = std::max<int64_t>(unit, PA_MAX_PARTITION_TOKENS / unit * unit);
+    p = std::min(std::max(p, unit), cap);
+    p = std::min<int64_t>(p, fast_max_partition(c));
+    return (int32_t)p;
+}
+
+int32_t num_parts(int32_t max_seq_len, int32_t part) {
+    return std::max(1, (max_seq_len + part - 1) / part);
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+size_t workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
+                       int32_t part, const pa_cache_desc* c) {
+    const int32_t P = num_parts(max_seq_len, part);
+    if (P <= 1) return 0;
+    const size_t cells = (size_t)num_seqs * num_q_heads * P;
+    return align256(cells * c->head_dim * sizeof(float)) + align256(cells * 2 * sizeof(float));
+}
+
+}  // namespace
+}  // namespace pa

@@ -14,36 +14,13 @@
 
 #include "common.cuh"
 #include "decode_generic.cuh"
+#include "decode_config.cuh"
 #include "decode_tma_mma.cuh"
 #include "merge.cuh"
 #include "write_kv.cuh"
 
-#ifndef PA_USE_PDL
-#define PA_USE_PDL 1   // launch with programmatic stream serialization
-#endif
-#ifndef PA_TARGET_CTAS_PER_SM
-#define PA_TARGET_CTAS_PER_SM 8
-#endif
-#ifndef PA_MAX_PARTITION_TOKENS
-#define PA_MAX_PARTITION_TOKENS 1024
-#endif
-
 namespace pa {
 namespace {
-
-constexpr int kMaxDevices = 64;
-
-int device_sm_count() {
-    static int cached[kMaxDevices] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-    if (cached[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cached[dev] = n;
-    }
-    return cached[dev];
-}
 
 bool desc_ok(const pa_cache_desc* c) {
     return c && c->num_blocks > 0 && c->block_size > 0 && c->num_kv_heads > 0 &&
@@ -53,68 +30,6 @@ bool desc_ok(const pa_cache_desc* c) {
 int elem_bytes(const pa_cache_desc* c) { return c->dtype == PA_F32 ? 4 : 2; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// ---- kernel selection --------------------------------------------------------
-
-bool fast_shape(const pa_cache_desc* c, int32_t group) {
-    if (c->dtype != PA_BF16 || group < 1 || group > 16) return false;
-    const int D = c->head_dim, B = c->block_size;
-    if (D != 64 && D != 128) return false;
-    return B % 16 == 0 && B <= 256;
-}
-
-// Largest partition (tokens) the generic kernel's shared memory holds.
-int32_t generic_max_partition(const pa_cache_desc* c, int32_t group) {
-    const size_t budget = 96 * 1024;
-    int32_t B = c->block_size;
-    int64_t fixed = 4LL * ((int64_t)group * c->head_dim + 2 * group);
-    int64_t per_tok = 4LL * group;
-    int64_t p = (int64_t(budget) - fixed) / per_tok;
-    p = p / B * B;
-    return (int32_t)std::max<int64_t>(p, 0);
-}
-
-int32_t fast_max_partition(const pa_cache_desc* c) {
-    return 2048 * c->block_size;   // TmaMmaCfg::kMaxTableSlice blocks
-}
-
-int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
-                       const pa_cache_desc* c) {
-    const int32_t B = c->block_size;
-    const int32_t group = num_q_heads / c->num_kv_heads;
-    if (!fast_shape(c, group)) {
-        int32_t cap = generic_max_partition(c, group);
-        int32_t want = std::max(B, (512 / B) * B);
-        return std::max(B, std::min(cap, want));
-    }
-    // one block per warp per step; aim for about PA_TARGET_CTAS_PER_SM CTAs
-    // per SM over the batch (counted at max_seq_len), between 4 blocks and
-    // PA_MAX_PARTITION_TOKENS tokens
-    const int64_t unit = 4LL * B;
-    const int64_t sms = std::max(1, device_sm_count());
-    const int64_t work = (int64_t)num_seqs * c->num_kv_heads * std::max(max_seq_len, 1);
-    const int64_t target = (int64_t)PA_TARGET_CTAS_PER_SM * sms;
-    int64_t p = (work + target - 1) / target;
-    p = (p + unit - 1) / unit * unit;
-    const int64_t cap = std::max<int64_t>(unit, PA_MAX_PARTITION_TOKENS / unit * unit);
-    p = std::min(std::max(p, unit), cap);
-    p = std::min<int64_t>(p, fast_max_partition(c));
-    return (int32_t)p;
-}
-
-int32_t num_parts(int32_t max_seq_len, int32_t part) {
-    return std::max(1, (max_seq_len + part - 1) / part);
-}
-
-size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-
-size_t workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
-                       int32_t part, const pa_cache_desc* c) {
-    const int32_t P = num_parts(max_seq_len, part);
-    if (P <= 1) return 0;
-    const size_t cells = (size_t)num_seqs * num_q_heads * P;
-    return align256(cells * c->head_dim * sizeof(float)) + align256(cells * 2 * sizeof(float));
-}
 
 // ---- TMA descriptors -----------------------------------------------------------
 
@@ -221,6 +136,65 @@ cudaError_t dispatch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& m
     }
 }
 
+// Address through which kernels reach `p`: device and managed memory as is,
+// page-locked host memory through its mapped device pointer.  nullptr for
+// pageable host memory (or a null pointer), which a kernel must not touch.
+const void* device_view(const void* p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    switch (at.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged:
+            return p;
+        case cudaMemoryTypeHost:
+            return at.devicePointer;
+        default:
+            return nullptr;
+    }
+}
+
+// Launch the cache-write kernel with the widest vector the row size and the
+// pointers' alignment allow.
+template <typename SlotFn>
+pa_status launch_write(const void* k, const void* v, SlotFn slot_of, int32_t num_tokens,
+                       void* k_cache, void* v_cache, const pa_cache_desc* cache,
+                       cudaStream_t st) {
+    if (!k || !v || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+    const int32_t row = cache->head_dim * elem_bytes(cache);
+    int vec = 16;
+    while (vec > 2 && (row % vec || !aligned(k, vec) || !aligned(v, vec) ||
+                       !aligned(k_cache, vec) || !aligned(v_cache, vec)))
+        vec >>= 1;
+    if (row % vec || !aligned(k, vec) || !aligned(v, vec) || !aligned(k_cache, vec) ||
+        !aligned(v_cache, vec))
+        return PA_ERR_INVALID_ARG;
+    const int64_t total = (int64_t)num_tokens * 2 * cache->num_kv_heads * (row / vec);
+    const int threads = 256;
+    const int64_t sms = std::max(1, device_sm_count());
+    const unsigned blocks = (unsigned)std::max<int64_t>(
+        1, std::min<int64_t>((total + threads - 1) / threads, sms * 16));
+    const int64_t num_slots = (int64_t)cache->num_blocks * cache->block_size;
+    auto go = [&](auto kern) {
+        return launch_pdl(kern, dim3(blocks), dim3(threads), 0, st,
+                          static_cast<const uint8_t*>(k), static_cast<const uint8_t*>(v), slot_of,
+                          (int64_t)num_tokens, static_cast<uint8_t*>(k_cache),
+                          static_cast<uint8_t*>(v_cache), cache->num_kv_heads,
+                          cache->block_size, num_slots, row);
+    };
+    cudaError_t err;
+    switch (vec) {
+        case 16: err = go(write_kv_kernel<16, SlotFn>); break;
+        case 8: err = go(write_kv_kernel<8, SlotFn>); break;
+        case 4: err = go(write_kv_kernel<4, SlotFn>); break;
+        default: err = go(write_kv_kernel<2, SlotFn>); break;
+    }
+    return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace pa
 
@@ -233,48 +207,69 @@ pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
                       const pa_cache_desc* cache, void* stream) {
     if (!desc_ok(cache) || num_tokens < 0) return PA_ERR_INVALID_ARG;
     if (num_tokens == 0) return PA_OK;
-    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
-    const int32_t row = cache->head_dim * elem_bytes(cache);
-    int vec = 16;
-    while (vec > 2 && (row % vec || !aligned(k, vec) || !aligned(v, vec) ||
-                       !aligned(k_cache, vec) || !aligned(v_cache, vec)))
-        vec >>= 1;
-    if (row % vec || !aligned(k, vec) || !aligned(v, vec) || !aligned(k_cache, vec) ||
-        !aligned(v_cache, vec) || !aligned(slot_mapping, 8))
+    if (!slot_mapping || !aligned(slot_mapping, 8)) return PA_ERR_INVALID_ARG;
+    return launch_write(k, v, SlotFromMapping{slot_mapping}, num_tokens, k_cache, v_cache, cache,
+                        static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_write_kv_positions(const void* k, const void* v, const int32_t* seq_ids,
+                                const int32_t* positions, int32_t num_tokens,
+                                const int32_t* block_tables, int32_t num_seqs,
+                                int32_t max_blocks_per_seq, void* k_cache, void* v_cache,
+                                const pa_cache_desc* cache, void* stream) {
+    if (!desc_ok(cache) || num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq < 0)
         return PA_ERR_INVALID_ARG;
-    const int64_t total = (int64_t)num_tokens * 2 * cache->num_kv_heads * (row / vec);
+    if (num_tokens == 0) return PA_OK;
+    if (!seq_ids || !positions || !block_tables || !aligned(seq_ids, 4) ||
+        !aligned(positions, 4) || !aligned(block_tables, 4))
+        return PA_ERR_INVALID_ARG;
+    SlotFromPosition fn{seq_ids, positions, block_tables, num_seqs, max_blocks_per_seq,
+                        cache->block_size, cache->num_blocks};
+    return launch_write(k, v, fn, num_tokens, k_cache, v_cache, cache,
+                        static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_copy_blocks(const void* src_k, const void* src_v, int32_t src_num_blocks,
+                         void* dst_k, void* dst_v, int32_t dst_num_blocks,
+                         const int64_t* block_pairs, int32_t num_pairs,
+                         const pa_cache_desc* cache, void* stream) {
+    if (!desc_ok(cache) || num_pairs < 0 || src_num_blocks < 0 || dst_num_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    const void* sk = device_view(src_k);
+    const void* sv = device_view(src_v);
+    void* dk = const_cast<void*>(device_view(dst_k));
+    void* dv = const_cast<void*>(device_view(dst_v));
+    const int64_t* pairs = static_cast<const int64_t*>(device_view(block_pairs));
+    if (!sk || !sv || !dk || !dv || !pairs || !aligned(pairs, 8)) return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes = (int64_t)cache->num_kv_heads * cache->block_size *
+                                cache->head_dim * elem_bytes(cache);
+    int vec = 16;
+    while (vec > 2 && (block_bytes % vec || !aligned(sk, vec) || !aligned(sv, vec) ||
+                       !aligned(dk, vec) || !aligned(dv, vec)))
+        vec >>= 1;
+    if (block_bytes % vec || !aligned(sk, vec) || !aligned(sv, vec) || !aligned(dk, vec) ||
+        !aligned(dv, vec))
+        return PA_ERR_INVALID_ARG;
+    const int64_t total = (int64_t)num_pairs * 2 * (block_bytes / vec);
     const int threads = 256;
     const int64_t sms = std::max(1, device_sm_count());
-    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((total + threads - 1) / threads,
-                                                                  sms * 16));
-    const int64_t num_slots = (int64_t)cache->num_blocks * cache->block_size;
+    const unsigned blocks = (unsigned)std::max<int64_t>(
+        1, std::min<int64_t>((total + threads - 1) / threads, sms * 16));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const uint8_t* kp = static_cast<const uint8_t*>(k);
-    const uint8_t* vp = static_cast<const uint8_t*>(v);
-    uint8_t* kc = static_cast<uint8_t*>(k_cache);
-    uint8_t* vc = static_cast<uint8_t*>(v_cache);
+    auto go = [&](auto kern) {
+        return launch_pdl(kern, dim3(blocks), dim3(threads), 0, st,
+                          static_cast<const uint8_t*>(sk), static_cast<const uint8_t*>(sv),
+                          (int64_t)src_num_blocks, static_cast<uint8_t*>(dk),
+                          static_cast<uint8_t*>(dv), (int64_t)dst_num_blocks, pairs,
+                          (int64_t)num_pairs, block_bytes);
+    };
     cudaError_t err;
     switch (vec) {
-        case 16:
-            err = launch_pdl(write_kv_kernel<16>, dim3((unsigned)blocks), dim3(threads), 0, st,
-                             kp, vp, slot_mapping, (int64_t)num_tokens, kc, vc,
-                             cache->num_kv_heads, cache->block_size, num_slots, row);
-            break;
-        case 8:
-            err = launch_pdl(write_kv_kernel<8>, dim3((unsigned)blocks), dim3(threads), 0, st,
-                             kp, vp, slot_mapping, (int64_t)num_tokens, kc, vc,
-                             cache->num_kv_heads, cache->block_size, num_slots, row);
-            break;
-        case 4:
-            err = launch_pdl(write_kv_kernel<4>, dim3((unsigned)blocks), dim3(threads), 0, st,
-                             kp, vp, slot_mapping, (int64_t)num_tokens, kc, vc,
-                             cache->num_kv_heads, cache->block_size, num_slots, row);
-            break;
-        default:
-            err = launch_pdl(write_kv_kernel<2>, dim3((unsigned)blocks), dim3(threads), 0, st,
-                             kp, vp, slot_mapping, (int64_t)num_tokens, kc, vc,
-                             cache->num_kv_heads, cache->block_size, num_slots, row);
-            break;
+        case 16: err = go(copy_blocks_kernel<16>); break;
+        case 8: err = go(copy_blocks_kernel<8>); break;
+        case 4: err = go(copy_blocks_kernel<4>); break;
+        default: err = go(copy_blocks_kernel<2>); break;
     }
     return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -69,6 +69,8 @@ class Step:
     slot_mapping: torch.Tensor   # [n_tok] int64
     block_tables: torch.Tensor   # [N, width] int32, -1 padded
     seq_lens: torch.Tensor       # [N] int32, lengths after this step's writes
+    seq_ids: torch.Tensor = None     # [n_tok] int32: sequence of each new token
+    positions: torch.Tensor = None   # [n_tok] int32: its position in that sequence
 
 
 @dataclass
@@ -136,7 +138,9 @@ def _decode_step(pool: BlockPool, seqs, hq: int, hkv: int, d: int, width: int, d
                 v_new=normal((n, hkv, d), seed, tag + 2, dtype),
                 slot_mapping=torch.tensor(slots, dtype=torch.int64),
                 block_tables=torch.tensor(pool.table_rows(seqs, width), dtype=torch.int32),
-                seq_lens=torch.tensor(lens, dtype=torch.int32))
+                seq_lens=torch.tensor(lens, dtype=torch.int32),
+                seq_ids=torch.arange(n, dtype=torch.int32),
+                positions=torch.tensor(lens, dtype=torch.int32) - 1)
 
 
 def _stats(pool: BlockPool, seqs) -> dict:
@@ -168,7 +172,9 @@ def tiny() -> Workload:
     step = Step(q=q, k_new=k_new, v_new=v_new,
                 slot_mapping=torch.tensor(slots, dtype=torch.int64),
                 block_tables=torch.tensor(tables, dtype=torch.int32),
-                seq_lens=torch.tensor(lengths, dtype=torch.int32))
+                seq_lens=torch.tensor(lengths, dtype=torch.int32),
+                seq_ids=torch.tensor([s_ for s_, _ in written], dtype=torch.int32),
+                positions=torch.tensor([p_ for _, p_ in written], dtype=torch.int32))
     zeros = torch.zeros(7, hkv, bs, d, dtype=torch.float32)
     wl = Workload("tiny", torch.float32, 7, bs, hq, hkv, d, 1.0 / math.sqrt(d),
                   zeros, zeros.clone(), [step], 53,
@@ -261,12 +267,14 @@ def cb(num_seqs=256, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16
     steps = []
     for k in range(num_steps):
         pick = int(rng.integers(num_seqs))
-        slots = []
+        slots, tok_seq, tok_pos = [], [], []
         for s in seqs:
             start = pool.lengths[s]
             count = chunk + 1 if s == pick else 1
             pool.grow(s, count)
             slots.extend(pool.slots(s, start, count))
+            tok_seq.extend([s] * count)
+            tok_pos.extend(range(start, start + count))
         n_tok = len(slots)
         tag = 100 + 10 * k
         steps.append(Step(q=normal((num_seqs, num_q_heads, head_dim), seed, tag, dtype),
@@ -276,9 +284,46 @@ def cb(num_seqs=256, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16
                           block_tables=torch.tensor(pool.table_rows(seqs, width),
                                                     dtype=torch.int32),
                           seq_lens=torch.tensor([pool.lengths[s] for s in seqs],
-                                                dtype=torch.int32)))
+                                                dtype=torch.int32),
+                          seq_ids=torch.tensor(tok_seq, dtype=torch.int32),
+                          positions=torch.tensor(tok_pos, dtype=torch.int32)))
     return Workload("cb", dtype, num_blocks, block_size, num_q_heads, num_kv_heads, head_dim,
                     1.0 / math.sqrt(head_dim), kc, vc, steps, seed, _stats(pool, seqs))
+
+
+@dataclass
+class CopyWorkload:
+    """Whole-block copies inside one pool: num_pairs disjoint (src, dst) pairs
+    over a shuffled pool (the copy-on-write / swap copy)."""
+    name: str
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    pairs: torch.Tensor          # int64 [num_pairs, 2]
+    seed: int
+
+    @property
+    def block_bytes(self) -> int:
+        return self.k_cache[0].numel() * self.k_cache.element_size()
+
+    def copy_bytes(self) -> int:
+        """Bytes one call moves: K and V blocks, each read once and written once."""
+        return 2 * 2 * self.pairs.shape[0] * self.block_bytes
+
+
+def copy_pairs(num_blocks=65536, num_pairs=8192, num_kv_heads=8, head_dim=128, block_size=16,
+               seed=6, dtype=torch.bfloat16, fill=True) -> CopyWorkload:
+    rng = np.random.default_rng(seed)
+    perm = rng.permutation(num_blocks)
+    pairs = torch.tensor(np.stack([perm[:num_pairs], perm[num_pairs:2 * num_pairs]], 1),
+                         dtype=torch.int64)
+    shape = (num_blocks, num_kv_heads, block_size, head_dim)
+    if fill:
+        k = normal(shape, seed, 1, dtype)
+        v = normal(shape, seed, 2, dtype)
+    else:
+        k = torch.zeros(shape, dtype=dtype)
+        v = torch.zeros(shape, dtype=dtype)
+    return CopyWorkload("copy", k, v, pairs, seed)
 
 
 BUILDERS = {"tiny": tiny, "mha": mha, "gqa": gqa, "long": long, "cb": cb}

@@ -223,3 +223,48 @@ def test_full_size_shapes_are_as_specified():
     lens = rng.integers(128, 2049, size=32)
     assert lens.min() >= 128 and lens.max() <= 2048
     assert math.ceil(4096 + 10 * 2049) / 16 <= 1537
+
+
+def test_fork_copy_on_write_and_swap():
+    pool = BlockPool(10, 4)
+    pool.add("A", 6)                                   # [0, 1], tail half full
+    pool.fork("A", "B")
+    assert pool.ref_cnt[:2] == [2, 2]
+    with pytest.raises(SharedTailWrite):
+        pool.grow("B", 1)
+    assert pool.copy_on_write("B") == (1, 2)
+    assert pool.tables["B"] == [0, 2] and pool.ref_cnt[:3] == [2, 1, 1]
+    assert pool.copy_on_write("B") is None             # already private
+    pool.grow("B", 3)                                  # fills block 2, takes block 3
+    assert pool.tables["B"] == [0, 2, 3]
+    # swap: private blocks only
+    host = BlockPool(6, 4)
+    with pytest.raises(SharedTailWrite):
+        pool.swap_out("B", host)                       # block 0 shared with A
+    pool.add("C", 9)                                   # [4, 5, 6]
+    pairs = pool.swap_out("C", host)
+    assert pairs == [(4, 0), (5, 1), (6, 2)] and "C" not in pool.tables
+    assert list(pool.free_queue)[-3:] == [4, 5, 6] and host.lengths["C"] == 9
+    back = pool.swap_in("C", host)
+    assert [h for h, _ in back] == [0, 1, 2] and pool.lengths["C"] == 9
+    assert host.num_free == 6
+    # all-or-nothing on a full host pool
+    small = BlockPool(2, 4)
+    before = (list(pool.free_queue), dict(pool.tables))
+    with pytest.raises(MemoryError):
+        pool.swap_out("C", small)
+    assert (list(pool.free_queue), dict(pool.tables)) == before
+
+
+def test_positions_give_the_slot_mapping():
+    """Every workload's (seq_id, position) per new token maps, through the
+    oracle's addressing, to the slot mapping the host pool produced."""
+    for wl in (workloads.tiny(),
+               workloads.mha(num_seqs=6, num_heads=4, head_dim=32, min_len=20, max_len=90,
+                             num_blocks=64),
+               workloads.cb(num_seqs=8, num_q_heads=4, num_kv_heads=2, head_dim=32,
+                            max_len0=70, chunk=40, num_steps=3, num_blocks=512)):
+        for st in wl.steps:
+            got = oracle.slots_from_positions(st.seq_ids, st.positions, st.block_tables,
+                                              wl.block_size)
+            assert got.tolist() == st.slot_mapping.tolist()

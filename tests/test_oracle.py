@@ -321,11 +321,84 @@ def check_zero_length():
     assert not out[0].any() and np.isfinite(out[1]).all()
 
 
+def check_copy_blocks():
+    """Whole-block copies, in pair order; out-of-range pairs are skipped."""
+    gen = torch.Generator().manual_seed(17)
+    src_k = torch.randn(6, 2, 4, 8, generator=gen).to(torch.bfloat16)
+    src_v = torch.randn(6, 2, 4, 8, generator=gen).to(torch.bfloat16)
+    dst_k = torch.zeros(3, 2, 4, 8, dtype=torch.bfloat16)
+    dst_v = torch.zeros_like(dst_k)
+    pairs = [[4, 0], [1, 2], [7, 1], [0, 3], [2, -1]]
+    assert oracle.copy_blocks(src_k, src_v, dst_k, dst_v, pairs) == 3
+    assert torch.equal(dst_k[0], src_k[4]) and torch.equal(dst_v[0], src_v[4])
+    assert torch.equal(dst_k[2], src_k[1]) and torch.equal(dst_v[2], src_v[1])
+    assert not dst_k[1].any() and not dst_v[1].any()
+    # inside one pool, in order: block 5 <- 0, then block 3 <- 5 (now block 0's data)
+    k, v = src_k.clone(), src_v.clone()
+    assert oracle.copy_blocks(k, v, k, v, [[0, 5], [5, 3]]) == 0
+    assert torch.equal(k[3], src_k[0]) and torch.equal(v[5], src_v[0])
+    assert torch.equal(k[1], src_k[1])
+
+
+def check_slots_from_positions():
+    """Slots from (sequence, position) agree with the pages' addressing values."""
+    cases = golden("addressing.json")["cases"]
+    for case in cases:
+        bs = case["block_size"]
+        width = max(len(c["table"]) for c in cases if c["block_size"] == bs)
+        tables = [c["table"] + [-1] * (width - len(c["table"]))
+                  for c in cases if c["block_size"] == bs]
+        row = tables.index(case["table"] + [-1] * (width - len(case["table"])))
+        n = len(case["positions"])
+        got = oracle.slots_from_positions([row] * n, case["positions"], tables, bs)
+        assert got.tolist() == case["slots"], case["cite"]
+    got = oracle.slots_from_positions([0, -1, 0, 2, 0], [1, 3, -2, 0, 12],
+                                      [[7, 3, 11], [1, 2, 3]], 4)
+    assert got.tolist() == [29, -1, -1, -1, -1]   # skip, skip, bad seq, past the table
+
+
+def check_copy_on_write_scenario():
+    """nxmr.cn article §4.2: two branches share a partly filled last block;
+    the writing branch first copies it into a fresh block and re-points its
+    table; the other branch's data and output are unchanged."""
+    from paged_kv_cache_109_gb300.block_pool import BlockPool
+    gen = torch.Generator().manual_seed(18)
+    hq, hkv, d, bs = 4, 2, 8, 4
+    pool = BlockPool(8, bs, free_order=[6, 2, 5, 0, 1, 3, 4, 7])
+    pool.add("A", 6)                        # blocks [6, 2], last one half full
+    pool.fork("A", "B")                     # B shares both
+    kc = torch.randn(8, hkv, bs, d, generator=gen)
+    vc = torch.randn(8, hkv, bs, d, generator=gen)
+    q = torch.randn(2, hq, d, generator=gen)
+    before = oracle.decode(q[:1], kc, vc, torch.tensor([pool.tables["A"]], dtype=torch.int32),
+                           torch.tensor([6], dtype=torch.int32), 0.5)
+    pair = pool.copy_on_write("B")
+    assert pair == (2, 5) and pool.tables["B"] == [6, 5] and pool.ref_cnt[2] == 1
+    assert oracle.copy_blocks(kc, vc, kc, vc, [pair]) == 0
+    pool.grow("B", 1)
+    new_k = torch.randn(1, hkv, d, generator=gen)
+    new_v = torch.randn(1, hkv, d, generator=gen)
+    slot = pool.slot("B", 6)
+    assert slot == 5 * bs + 2
+    oracle.write_kv(new_k, new_v, torch.tensor([slot]), kc, vc)
+    tables = torch.tensor([pool.tables["A"], pool.tables["B"]], dtype=torch.int32)
+    out = oracle.decode(q, kc, vc, tables, torch.tensor([6, 7], dtype=torch.int32), 0.5)
+    assert np.array_equal(out[0], before[0])            # A untouched
+    # B = dense attention over A's 6 rows plus its own new row
+    rows_k = torch.cat([kc[6], kc[2, :, :2], new_k.permute(1, 0, 2)], 1)   # [Hkv, 7, D]
+    rows_v = torch.cat([vc[6], vc[2, :, :2], new_v.permute(1, 0, 2)], 1)
+    for h in range(hq):
+        ref = oracle.attend(q[1, h].numpy(), expand_kv(rows_k, hq)[h].numpy(),
+                            expand_kv(rows_v, hq)[h].numpy(), 0.5)
+        assert np.abs(out[1, h] - ref).max() < 1e-14
+
+
 CHECKS = [check_addressing, check_block_counts, check_worked_example_write,
           check_worked_example_paged_equals_contiguous, check_sdpa_special_case,
           check_gqa_grouping, check_closed_forms, check_relabel_invariance,
           check_brute_force_tables, check_partition_merge, check_write_semantics,
-          check_write_then_read_roundtrip, check_bf16_widening, check_zero_length]
+          check_write_then_read_roundtrip, check_bf16_widening, check_zero_length,
+          check_copy_blocks, check_slots_from_positions, check_copy_on_write_scenario]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -354,6 +427,9 @@ MUTANTS = [
     ("query head of group", "(i * num_q_heads + h) * head_dim + d",
      "(i * num_q_heads + h / group * group) * head_dim + d"),
     ("partition max missing", "if (scale * dot > m) m = scale * dot;", "m = 0.0;"),
+    ("block copy V from K", "(const char*)src_v + s * block_bytes", "(const char*)src_k + s * block_bytes"),
+    ("slots from the first table", "oracle_slot(block_tables + s * max_blocks,",
+     "oracle_slot(block_tables + 0 * max_blocks,"),
 ]
 
 
