@@ -511,6 +511,13 @@ def overrides(args) -> dict:
             out["num_shared"] = max(1, args.num_seqs // 4)
     if args.num_blocks:
         out["num_blocks"] = args.num_blocks
+    if args.block_size:
+        # same pool bytes at every block size
+        out["block_size"] = args.block_size
+        base = {"mha": (8192, 16), "gqa": (65536, 16), "cb": (65536, 16), "long": (16384, 32)}
+        nb, bs = base[args.workload]
+        if "num_blocks" not in out:
+            out["num_blocks"] = nb * bs // args.block_size
     return out
 
 
@@ -556,6 +563,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="smaller batch (profiling); the JSON line then has no traffic")
     ap.add_argument("--num-blocks", type=int, default=0, help="smaller block pool (profiling)")
+    ap.add_argument("--block-size", type=int, default=0,
+                    help="block-size sweep: tokens per block (pool bytes kept constant)")
     ap.add_argument("--positions", action="store_true",
                     help="write with slots computed on the device from (seq, position)")
     args = ap.parse_args()

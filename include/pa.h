@@ -188,8 +188,8 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
 
 /*
  * Which decode kernel these arguments select: 1 = the TMA + tensor-core
- * kernel (bf16, head_dim 64 or 128, block_size a multiple of 16 up to 256,
- * group size <= 16), 0 = the portable kernel
+ * kernel (bf16, head_dim 64 or 128, block_size 8 or a multiple of 16 up to
+ * 256, group size <= 16), 0 = the portable kernel
  * (any other valid shape, and every fp32 cache), < 0 = invalid arguments.
  */
 int32_t pa_decode_path(int32_t num_q_heads, const pa_cache_desc* cache);

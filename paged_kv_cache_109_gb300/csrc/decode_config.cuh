@@ -44,7 +44,7 @@ bool fast_shape(const pa_cache_desc* c, int32_t group) {
     if (c->dtype != PA_BF16 || group < 1 || group > 16) return false;
     const int D = c->head_dim, B = c->block_size;
     if (D != 64 && D != 128) return false;
-    return B % 16 == 0 && B <= 256;
+    return B == 8 || (B % 16 == 0 && B <= 256);
 }
 
 // Largest partition (tokens) the generic kernel's shared memory holds.

@@ -92,7 +92,9 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int32_t grp = lane >> 2, tig = lane & 3;
     const int32_t G = a.group;
     const int32_t BS = a.block_size;
-    const int32_t cpb = BS / C::kChunk;                    // chunks per block
+    // B >= 16: a block is cpb = B/16 chunks.  B = 8: a chunk is two blocks,
+    // loaded as two 8-row boxes (the 128-byte swizzle atom is 8 rows).
+    const int32_t cpb = BS >= C::kChunk ? BS / C::kChunk : 1;
     const int32_t P = a.part_tokens;
     const int32_t t0 = p * P;
     const int64_t head0 = (int64_t)i * a.num_q_heads + (int64_t)g * G;
@@ -184,17 +186,27 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int32_t hkv = a.num_kv_heads;
     const uint64_t policy = l2_policy_evict_first();
 
+    // A chunk is usable when its block(s) passed the table check; a chunk
+    // touching a bad entry is skipped whole (its output is undefined anyway,
+    // and the error bit is set).
+    auto chunk_ok = [&](int32_t c) -> bool {
+        if (BS >= C::kChunk) return ids[c / cpb] >= 0;
+        return ids[2 * c] >= 0 && (2 * c + 1 >= nblk || ids[2 * c + 1] >= 0);
+    };
     auto issue = [&](int32_t k) {   // lane 0 only
         const int32_t c = warp + k * C::kWarps;
         const int32_t st = k % C::kStages;
         const uint32_t bar = bar0 + 8 * st;
-        const int32_t blk = c / cpb;
-        const int32_t id = ids[blk];
-        if (id >= 0) {
-            const uint32_t dst = ring_u + st * C::kStageBytes;
+        if (!chunk_ok(c)) {
+            mbar_arrive(bar);
+            return;
+        }
+        const uint32_t dst = ring_u + st * C::kStageBytes;
+        fence_proxy_async_smem();
+        if (BS >= C::kChunk) {
+            const int32_t blk = c / cpb;
             const int32_t y = (c - blk * cpb) * C::kChunk;
-            const int32_t z = id * hkv + g;
-            fence_proxy_async_smem();
+            const int32_t z = ids[blk] * hkv + g;
             mbar_arrive_expect_tx(bar, C::kStageBytes);
 #pragma unroll
             for (int b = 0; b < C::kBoxes; ++b)
@@ -205,7 +217,20 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 tma_load_3d_hint(dst + C::kTileBytes + b * C::kBoxBytes, &tmap_v,
                                  b * C::kBoxCols, y, z, bar, policy);
         } else {
-            mbar_arrive(bar);
+            // B = 8: rows 0-7 from block 2c, rows 8-15 from block 2c+1 (if any)
+            const int32_t halves = 2 * c + 1 < nblk ? 2 : 1;
+            mbar_arrive_expect_tx(bar, halves * (C::kStageBytes / 2));
+            for (int h = 0; h < halves; ++h) {
+                const int32_t z = ids[2 * c + h] * hkv + g;
+#pragma unroll
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d_hint(dst + b * C::kBoxBytes + h * 1024, &tmap_k,
+                                     b * C::kBoxCols, 0, z, bar, policy);
+#pragma unroll
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d_hint(dst + C::kTileBytes + b * C::kBoxBytes + h * 1024, &tmap_v,
+                                     b * C::kBoxCols, 0, z, bar, policy);
+            }
         }
     };
     if (lane == 0) {
@@ -229,7 +254,7 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             break;
         }
         const int32_t c = warp + k * C::kWarps;
-        if (ids[c / cpb] >= 0) {
+        if (chunk_ok(c)) {
             const uint32_t kb = ring_u + st * C::kStageBytes;
             const uint32_t vb = kb + C::kTileBytes;
             const int32_t nvalid = min(C::kChunk, n - c * C::kChunk);

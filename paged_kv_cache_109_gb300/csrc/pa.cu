@@ -57,7 +57,7 @@ bool encode_cache_map(CUtensorMap* map, const void* base, const pa_cache_desc* c
                           (cuuint64_t)c->num_blocks * (cuuint64_t)c->num_kv_heads};
     cuuint64_t strides[2] = {(cuuint64_t)c->head_dim * 2,
                              (cuuint64_t)c->head_dim * 2 * (cuuint64_t)c->block_size};
-    cuuint32_t box[3] = {64, 16, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)std::min(16, c->block_size), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

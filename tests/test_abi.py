@@ -57,7 +57,9 @@ def test_path_selection(lib):
     assert path(32, desc(dtype=pa.PA_F32)) == 0        # fp32: portable kernel
     assert path(32, desc(bs=64)) == 1                  # B=64: four 16-token chunks
     assert path(32, desc(bs=48)) == 1
-    assert path(32, desc(bs=8)) == 0                   # B not a multiple of 16
+    assert path(32, desc(bs=8)) == 1                   # B=8: two blocks per chunk
+    assert path(32, desc(bs=24)) == 0                  # neither 8 nor a multiple of 16
+    assert path(32, desc(bs=4)) == 0
     assert path(32, desc(bs=512)) == 0
     assert path(16, desc(d=64, bs=64, hkv=4)) == 1
     assert path(8, desc(d=8, bs=4, hkv=2, dtype=pa.PA_F32)) == 0

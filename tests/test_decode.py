@@ -93,6 +93,8 @@ FAST_CASES = [
     (32, 8, 128, 48, (1, 47, 48, 49, 300)),                        # B=48: 3 chunks/block
     (32, 8, 128, 128, (5, 127, 128, 129, 1000)),                   # B=128
     (64, 8, 128, 64, (64, 65, 777)),                               # G=8, B=64
+    (32, 8, 128, 8, (1, 7, 8, 9, 15, 16, 17, 300)),                # B=8: 2 blocks/chunk
+    (16, 16, 64, 8, (3, 24, 25, 130)),                             # B=8, D=64, MHA
 ]
 
 
