@@ -73,6 +73,9 @@ def load(path: str | None = None):
     lib.oracle_merge.restype = None
     lib.oracle_write_kv.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, I32]
     lib.oracle_write_kv.restype = I64
+    lib.oracle_prefill.argtypes = [P, P, P, P, ctypes.c_int, I32, I32, I32, I32, P, I32, P,
+                                   I32, I32, D, P]
+    lib.oracle_prefill.restype = I64
     lib.oracle_copy_blocks.argtypes = [P, P, I32, P, P, I32, P, I64, I64]
     lib.oracle_copy_blocks.restype = I64
     lib.oracle_slots_from_positions.argtypes = [P, P, I64, P, I32, I32, I32, P]
@@ -204,6 +207,31 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, scale: float, pairs=None
                             bt.shape[1], _ptr(sl), n, hq, scale, pp, npairs, _ptr(out))
     if bad:
         raise ValueError(f"{bad} (seq, head) rows met an invalid block-table entry")
+    return out
+
+
+def prefill(q, query_start_loc, k_cache, v_cache, block_tables, seq_lens,
+            scale: float) -> np.ndarray:
+    """fp64 out[total_q, Hq, D] of causal multi-query attention: sequence i's
+    rows query_start_loc[i]..query_start_loc[i+1] are its last positions."""
+    qa, dt = _as_array(q)
+    ka, dk = _as_array(k_cache)
+    va, dv = _as_array(v_cache)
+    if dt is None or dt != dk or dt != dv:
+        raise ValueError("q and caches must share one dtype (float32 or bfloat16)")
+    qs = _i32(query_start_loc)
+    bt = _i32(block_tables)
+    sl = _i32(seq_lens)
+    total, hq, d = (int(s) for s in q.shape)
+    nb, hkv, bs, _ = _cache_geometry(k_cache)
+    n = sl.shape[0]
+    if qs.shape[0] != n + 1 or qs[-1] != total:
+        raise ValueError("query_start_loc must have num_seqs + 1 entries ending at total_q")
+    out = np.full((total, hq, d), np.nan, dtype=np.float64)
+    bad = load().oracle_prefill(_ptr(qa), _ptr(qs), _ptr(ka), _ptr(va), dt, nb, bs, hkv, d,
+                                _ptr(bt), bt.shape[1], _ptr(sl), n, hq, scale, _ptr(out))
+    if bad:
+        raise ValueError(f"{bad} (row, head) results met an invalid length or table entry")
     return out
 
 

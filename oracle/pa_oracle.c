@@ -301,6 +301,70 @@ int64_t oracle_write_kv(const void* k, const void* v, const int64_t* slot_mappin
     return rejected;
 }
 
+/* ---- multi-query (chunked prefill) attention ---------------------------- */
+
+/*
+ * Sequence i owns the packed query rows [query_start[i], query_start[i+1]):
+ * its last L_i = query_start[i+1] - query_start[i] positions, so row r sits
+ * at position p = T_i - L_i + (r - query_start[i]) and attends to keys
+ * 0..p of its sequence (causal).  Prefill and decode rows share one batch,
+ * a decode row being a sequence with L_i = 1 ("vLLM source walkthrough"
+ * §2.8: chunked prefill processes part of a prompt per step, decode one
+ * token; "vLLM PagedAttention: from memory fragmentation to slot mapping"
+ * §6: query start locations slice the flat tokens per request, positions set
+ * the causal boundary).  q and out are [total_q][Hq][D].  For each row and
+ * head: gather keys 0..p through the table, then dense attention.  Returns
+ * the number of (row, head) results left NaN because L_i > T_i or a needed
+ * table entry was invalid.
+ */
+int64_t oracle_prefill(const void* q, const int32_t* query_start, const void* k_cache,
+                       const void* v_cache, int dtype, int32_t num_blocks, int32_t block_size,
+                       int32_t num_kv_heads, int32_t head_dim, const int32_t* block_tables,
+                       int32_t max_blocks, const int32_t* seq_lens, int32_t num_seqs,
+                       int32_t num_q_heads, double scale, double* out) {
+    int32_t group = num_q_heads / num_kv_heads;
+    int64_t total_rows = query_start[num_seqs];
+    int64_t bad = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+#endif
+    for (int64_t u = 0; u < total_rows * num_q_heads; ++u) {
+        int64_t r = u / num_q_heads, h = u % num_q_heads;
+        int64_t i = 0;
+        while (i + 1 < num_seqs && query_start[i + 1] <= r) ++i;
+        int64_t L = query_start[i + 1] - query_start[i];
+        int64_t T = seq_lens[i];
+        double* row = out + (r * num_q_heads + h) * head_dim;
+        int64_t p = T - L + (r - query_start[i]);
+        if (L > T || p < 0) {
+            for (int32_t d = 0; d < head_dim; ++d) row[d] = NAN;
+            bad += 1;
+            continue;
+        }
+        int64_t n = p + 1;
+        int32_t g = (int32_t)(h / group);
+        double* K = (double*)malloc(sizeof(double) * (size_t)n * (size_t)head_dim);
+        double* V = (double*)malloc(sizeof(double) * (size_t)n * (size_t)head_dim);
+        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        const int32_t* table = block_tables + i * (int64_t)max_blocks;
+        if (gather_rows(k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, table,
+                        n, g, K) == 0 &&
+            gather_rows(v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, table,
+                        n, g, V) == 0) {
+            for (int32_t d = 0; d < head_dim; ++d)
+                qv[d] = widen(q, (r * num_q_heads + h) * head_dim + d, dtype);
+            oracle_attend(qv, K, V, n, head_dim, scale, row);
+        } else {
+            for (int32_t d = 0; d < head_dim; ++d) row[d] = NAN;
+            bad += 1;
+        }
+        free(K);
+        free(V);
+        free(qv);
+    }
+    return bad;
+}
+
 /* ---- block copy for copy-on-write and swap ------------------------------ */
 
 /*

@@ -393,12 +393,49 @@ def check_copy_on_write_scenario():
         assert np.abs(out[1, h] - ref).max() < 1e-14
 
 
+def check_prefill_causal_sdpa():
+    """Multi-query rows are the last L_i positions of T_i and see keys up to
+    their own position: torch SDPA (fp64) with an explicit bottom-right
+    causal mask on the contiguous K/V is the library special case."""
+    gen = torch.Generator().manual_seed(19)
+    hq, hkv, d, bs = 8, 2, 16, 4
+    lengths = (9, 21, 1, 40)
+    qlens = (9, 5, 1, 17)              # a whole prompt, a chunk, a decode row, a chunk
+    _, kc, vc, bt, sl, ck, cv = random_case(gen, 4, hq, hkv, d, bs, lengths, 64)
+    qs = [0]
+    for L in qlens:
+        qs.append(qs[-1] + L)
+    q = torch.randn(qs[-1], hq, d, generator=gen)
+    out = oracle.prefill(q, qs, kc, vc, bt, sl, 0.3)
+    for i, (T, L) in enumerate(zip(lengths, qlens)):
+        rows = q[qs[i]:qs[i + 1]].double().permute(1, 0, 2)            # [Hq, L, D]
+        pos = torch.arange(T - L, T)
+        mask = torch.arange(T)[None, :] <= pos[:, None]                # [L, T]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            rows, expand_kv(ck[i].double(), hq), expand_kv(cv[i].double(), hq),
+            attn_mask=mask, scale=0.3).permute(1, 0, 2)
+        assert np.abs(out[qs[i]:qs[i + 1]] - ref.numpy()).max() < 1e-12
+
+
+def check_prefill_last_row_is_decode():
+    """The last query row of every sequence is the single-query decode."""
+    gen = torch.Generator().manual_seed(20)
+    _, kc, vc, bt, sl, _, _ = random_case(gen, 3, 4, 2, 8, 4, (13, 6, 30), 32)
+    qs = [0, 4, 5, 12]
+    q = torch.randn(12, 4, 8, generator=gen)
+    out = oracle.prefill(q, qs, kc, vc, bt, sl, 0.4)
+    last = [qs[i + 1] - 1 for i in range(3)]
+    dec = oracle.decode(q[last], kc, vc, bt, sl, 0.4)
+    assert np.array_equal(out[last], dec)
+
+
 CHECKS = [check_addressing, check_block_counts, check_worked_example_write,
           check_worked_example_paged_equals_contiguous, check_sdpa_special_case,
           check_gqa_grouping, check_closed_forms, check_relabel_invariance,
           check_brute_force_tables, check_partition_merge, check_write_semantics,
           check_write_then_read_roundtrip, check_bf16_widening, check_zero_length,
-          check_copy_blocks, check_slots_from_positions, check_copy_on_write_scenario]
+          check_copy_blocks, check_slots_from_positions, check_copy_on_write_scenario,
+          check_prefill_causal_sdpa, check_prefill_last_row_is_decode]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -430,6 +467,10 @@ MUTANTS = [
     ("block copy V from K", "(const char*)src_v + s * block_bytes", "(const char*)src_k + s * block_bytes"),
     ("slots from the first table", "oracle_slot(block_tables + s * max_blocks,",
      "oracle_slot(block_tables + 0 * max_blocks,"),
+    ("causal mask drops the diagonal", "int64_t n = p + 1;", "int64_t n = p;"),
+    ("no causal mask", "int64_t n = p + 1;", "int64_t n = T;"),
+    ("query position off by one", "int64_t p = T - L + (r - query_start[i]);",
+     "int64_t p = T - L + (r - query_start[i]) - 1;"),
 ]
 
 
