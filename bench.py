@@ -47,6 +47,9 @@ WORKLOAD_TEXT = {
     "cb": "continuous batching bf16: 256 seqs, Hq=32, Hkv=8, D=128, B=16, T0~U[1,4096]; "
           "step = write 2304 tokens (1 per seq + 2048-token chunk) + decode all 256; "
           "10 distinct steps cycled",
+    "prefill": "chunked prefill bf16: 8 seqs with history T0~U[1,4096] each taking a "
+               "2048-token chunk, Hq=32, Hkv=8, D=128, B=16; step = write the 16384 chunk "
+               "tokens + causal multi-query attention from every chunk token",
     "copy": "block copy inside one pool (copy-on-write), bf16: 8192 disjoint (src, dst) pairs "
             "of B=16, Hkv=8, D=128 blocks (64 KiB of K+V each) in a 65536-block pool; "
             "step = one pa_copy_blocks call",
@@ -366,6 +369,94 @@ def run_ours(args, rank, world, device):
     return result
 
 
+def prefill_flops(wl) -> int:
+    """4 * D * Hq flops per (query row, visible key): QK^T and PV."""
+    st = wl.steps[0]
+    total = 0
+    for i in range(st.seq_lens.numel()):
+        T = int(st.seq_lens[i])
+        L = int(st.query_start[i + 1] - st.query_start[i])
+        # keys visible from positions T-L .. T-1: sum of (p + 1)
+        total += (T * (T + 1) - (T - L) * (T - L + 1)) // 2
+    return 4 * wl.head_dim * wl.num_q_heads * total
+
+
+def run_prefill(args, rank, world, device):
+    """Chunked prefill step: pa_write_kv of the chunk tokens + pa_prefill."""
+    import paged_kv_cache_109_gb300 as pa
+    pa.load_library()
+    wl = workloads.make("prefill", **overrides(args))
+    st = wl.steps[0]
+    kc, vc = wl.k_cache.to(device), wl.v_cache.to(device)
+    d = {k: getattr(st, k).to(device) for k in ("q", "k_new", "v_new", "slot_mapping",
+                                                "block_tables", "seq_lens", "query_start")}
+    out = torch.empty_like(d["q"])
+    max_q = int((st.query_start[1:] - st.query_start[:-1]).max())
+    max_len = int(st.seq_lens.max())
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
+        if ev is not None:
+            ev[0].record(stream)
+        pa.prefill(d["q"], d["query_start"], kc, vc, d["block_tables"], d["seq_lens"], max_q,
+                   max_len, wl.scale, out=out)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    K = args.steps
+    sampled = list(range(0, K, DEC_SAMPLE))
+    evs = {it: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for it in sampled}
+    with ClockSampler(device.index or 0) as clocks:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for it in range(K):
+            step(evs.get(it))
+        end.record(stream)
+        torch.cuda.synchronize(device)
+    total_ms = start.elapsed_time(end)
+    if pa.last_device_error() != 0:
+        raise RuntimeError("device error flag raised in the timed region")
+    pre_ms = [evs[it][0].elapsed_time(evs[it][1]) for it in sampled]
+    flops = prefill_flops(wl)
+    by = step_bytes(wl, 0, split_traffic=False)
+    step_b = by["decode"] + by["write"]
+    tflops = flops / (statistics.mean(pre_ms) / 1e3) / 1e12
+    peak_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        peak = float(json.load(open(peak_path))["bf16_tflops_sustained"])
+        peak_kind = "bf16_tflops_sustained of measured"
+    except (OSError, KeyError, ValueError):
+        peak, peak_kind = 1700.0, "fallback sustained bf16"
+    hbm_peak, _ = measured_peak()
+    value = world * K * step_b / (total_ms / 1e3) / 1e9
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) K/V/q; tables from a shuffled block pool)",
+        "config": {"workload": WORKLOAD_TEXT["prefill"], "name": "prefill",
+                   "overrides": overrides(args) or None, "num_seqs": wl.num_seqs,
+                   "query_rows": int(st.query_start[-1]), "max_seq_len": max_len,
+                   "l2": f"inputs larger than L2: {by['unique_kv'] / 2**20:.0f} MiB of K/V",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2),
+        "prefill_tflops": round(tflops, 1),
+        "roofline": {"bound": "tensor", "kernel": "pa_prefill call (mma.sync bf16)",
+                     "achieved": round(tflops, 1), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                     "flops_per_call": flops, "prefill_ms_mean": round(statistics.mean(pre_ms), 4)},
+        "e2e": None,
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+        "cpu_baseline": None,
+    }
+
+
 def run_copy(args, rank, world, device):
     """Block copies: `copy` inside the device pool (HBM read + write), `swap`
     out to page-locked host memory and back (bound by the host link)."""
@@ -583,7 +674,9 @@ def main():
     torch.cuda.set_device(device)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
-    res = (run_copy if args.workload in ("copy", "swap") else run_ours)(args, rank, world, device)
+    runner = {"copy": run_copy, "swap": run_copy, "prefill": run_prefill}.get(args.workload,
+                                                                          run_ours)
+    res = runner(args, rank, world, device)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

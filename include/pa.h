@@ -187,6 +187,38 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     const pa_cache_desc* cache, void* stream);
 
 /*
+ * pa_prefill -- multi-query (chunked prefill) paged attention with a causal
+ * mask ("vLLM source walkthrough: PagedAttention and Continuous Batching"
+ * §2.8: prefill rows and decode rows in one batch, long prompts in chunks;
+ * "vLLM PagedAttention: from memory fragmentation to slot mapping" §6: query
+ * start locations slice the packed tokens per request, positions set the
+ * causal boundary).
+ *
+ * Sequence i owns the packed query rows [query_start_loc[i],
+ * query_start_loc[i+1]): its last L_i positions (their K/V already written
+ * to the cache).  Row r is at position p = T_i - L_i + (r - query_start_loc[i])
+ * and attends to keys 0..p of its sequence:
+ *   out[r][h] = sum_{t <= p} softmax_t(scale * q[r][h].k_t) v_t,
+ * kv head floor(h / (Hq/Hkv)), keys read through the block table as in
+ * pa_decode.  A decode row is a sequence with L_i = 1.
+ *
+ * q, out           device [total_q][num_q_heads][head_dim], cache dtype.
+ * query_start_loc  device int32 [num_seqs + 1], non-decreasing, last = total_q.
+ * max_q_len        host upper bound of L_i (sizes the grid).
+ * Other arguments as pa_decode.  L_i > T_i is reported (PA_DEVERR_SEQ_LEN)
+ * and that sequence's rows are left untouched.  bf16 with head_dim 64/128,
+ * block_size 8 or a multiple of 16, and a group size dividing 64 runs on the
+ * TMA + tensor-core kernel; other valid shapes (head_dim <= 256) on a
+ * portable kernel.
+ */
+pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t total_q,
+                     int32_t max_q_len, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                     const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                     int32_t num_q_heads, float scale, void* out, const pa_cache_desc* cache,
+                     void* stream);
+
+/*
  * Which decode kernel these arguments select: 1 = the TMA + tensor-core
  * kernel (bf16, head_dim 64 or 128, block_size 8 or a multiple of 16 up to
  * 256, group size <= 16), 0 = the portable kernel

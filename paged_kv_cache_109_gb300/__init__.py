@@ -21,7 +21,7 @@ from ._build import LIB as LIBRARY_PATH
 from ._build import build
 from .block_pool import BlockPool, SharedTailWrite
 
-__all__ = ["write_kv", "write_kv_positions", "copy_blocks", "decode", "decode_workspace_bytes", "decode_partition_tokens",
+__all__ = ["write_kv", "write_kv_positions", "copy_blocks", "decode", "prefill", "decode_workspace_bytes", "decode_partition_tokens",
            "decode_path", "last_device_error", "PaError", "build", "BlockPool",
            "SharedTailWrite", "LIBRARY_PATH", "load_library", "CacheDesc"]
 
@@ -62,6 +62,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.pa_write_kv_positions.restype = ctypes.c_int
     lib.pa_copy_blocks.argtypes = [P, P, I32, P, P, I32, P, I32, DP, P]
     lib.pa_copy_blocks.restype = ctypes.c_int
+    lib.pa_prefill.argtypes = [P, P, I32, I32, P, P, P, I32, P, I32, I32, I32, ctypes.c_float,
+                               P, DP, P]
+    lib.pa_prefill.restype = ctypes.c_int
     lib.pa_decode_partition_tokens.argtypes = [I32, I32, I32, DP]
     lib.pa_decode_partition_tokens.restype = I32
     lib.pa_decode_workspace_bytes.argtypes = [I32, I32, I32, I32, DP]
@@ -243,3 +246,29 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int,
 def last_device_error() -> int:
     """PA_DEVERR_* bits raised since the last call (synchronises the device)."""
     return int(load_library().pa_last_device_error())
+
+
+def prefill(q, query_start_loc, k_cache, v_cache, block_tables, seq_lens, max_q_len: int,
+            max_seq_len: int, scale: float | None = None, out=None, stream=None):
+    """Causal multi-query attention over the paged cache: sequence i's packed
+    rows query_start_loc[i]..query_start_loc[i+1] are its last positions.
+    Returns out [total_q, Hq, D] in the cache dtype."""
+    _dev(q, query_start_loc, k_cache, v_cache, block_tables, seq_lens)
+    for t in (query_start_loc, block_tables, seq_lens):
+        if t.dtype != torch.int32:
+            raise ValueError("query_start_loc, block_tables and seq_lens must be int32")
+    desc = cache_desc(k_cache)
+    total, hq, d = q.shape
+    if query_start_loc.numel() != seq_lens.numel() + 1:
+        raise ValueError("query_start_loc must have num_seqs + 1 entries")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out)
+    st = load_library().pa_prefill(
+        _ptr(q), _ptr(query_start_loc), total, max_q_len, _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), seq_lens.numel(), max_seq_len,
+        hq, float(scale), _ptr(out), ctypes.byref(desc), _stream(stream))
+    _check(st, "pa_prefill")
+    return out

@@ -42,7 +42,8 @@ struct DecodeArgs {
 
 // Effective length from a raw seq_lens value: clamps (and reports) lengths
 // the table or the host bound cannot cover.
-__device__ __forceinline__ int32_t clamp_len(const DecodeArgs& a, int32_t t) {
+template <typename Args>
+__device__ __forceinline__ int32_t clamp_len(const Args& a, int32_t t) {
     const int64_t cap64 = (int64_t)a.max_blocks * a.block_size;
     const int32_t cap = (int32_t)min((int64_t)a.max_seq_len, cap64);
     if (t < 0 || t > cap) {

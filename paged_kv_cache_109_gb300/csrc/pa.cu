@@ -17,6 +17,8 @@
 #include "decode_config.cuh"
 #include "decode_tma_mma.cuh"
 #include "merge.cuh"
+#include "prefill_generic.cuh"
+#include "prefill_tma_mma.cuh"
 #include "write_kv.cuh"
 
 namespace pa {
@@ -382,6 +384,75 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
         if (merr != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
+}
+
+pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t total_q,
+                     int32_t max_q_len, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                     const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                     int32_t num_q_heads, float scale, void* out, const pa_cache_desc* cache,
+                     void* stream) {
+    const int32_t path = pa_decode_path(num_q_heads, cache);
+    if (path < 0 || num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_seq_len < 0 ||
+        max_blocks_per_seq < 0 || max_q_len > max_seq_len)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_q == 0) return PA_OK;
+    if (!q || !query_start_loc || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+        return PA_ERR_INVALID_ARG;
+    if ((int64_t)max_blocks_per_seq * cache->block_size < max_seq_len) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 65535 || cache->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    const int32_t group = num_q_heads / cache->num_kv_heads;
+    const int eb = elem_bytes(cache);
+    if (!aligned(q, eb) || !aligned(out, eb) || !aligned(query_start_loc, 4) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    PrefillArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.query_start = query_start_loc;
+    a.seq_lens = seq_lens;
+    a.block_tables = block_tables;
+    a.out = out;
+    a.num_seqs = num_seqs;
+    a.max_blocks = max_blocks_per_seq;
+    a.max_seq_len = max_seq_len;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = cache->num_kv_heads;
+    a.group = group;
+    a.num_blocks = cache->num_blocks;
+    a.block_size = cache->block_size;
+    a.head_dim = cache->head_dim;
+    a.tokens_per_tile = 64 % group == 0 ? 64 / group : 0;
+    a.scale_log2 = scale * kLog2e;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) &&
+                      aligned(k_cache, 16) && aligned(v_cache, 16);
+    cudaError_t err;
+    if (fast) {
+        CUtensorMap mk, mv;
+        if (!cached_map(&mk, k_cache, cache, 0) || !cached_map(&mv, v_cache, cache, 1))
+            return PA_ERR_CUDA;
+        const int32_t tiles = std::max(1, (max_q_len + a.tokens_per_tile - 1) / a.tokens_per_tile);
+        dim3 grid(tiles, cache->num_kv_heads, num_seqs);
+        if (cache->head_dim == 128) {
+            auto kern = prefill_tma_mma_kernel<128>;
+            if (!set_smem(kern, PrefillCfg<128>::smem_bytes())) return PA_ERR_UNSUPPORTED;
+            err = launch_pdl(kern, grid, dim3(128), PrefillCfg<128>::smem_bytes(), st, mk, mv, a);
+        } else {
+            auto kern = prefill_tma_mma_kernel<64>;
+            if (!set_smem(kern, PrefillCfg<64>::smem_bytes())) return PA_ERR_UNSUPPORTED;
+            err = launch_pdl(kern, grid, dim3(128), PrefillCfg<64>::smem_bytes(), st, mk, mv, a);
+        }
+    } else {
+        if (cache->head_dim > 32 * kGenericMaxDimPerLane) return PA_ERR_UNSUPPORTED;
+        dim3 grid(total_q, cache->num_kv_heads);
+        if (cache->dtype == PA_F32)
+            err = launch_pdl(prefill_generic_kernel<float>, grid, dim3(128), 0, st, a);
+        else
+            err = launch_pdl(prefill_generic_kernel<__nv_bfloat16>, grid, dim3(128), 0, st, a);
+    }
+    return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 const char* pa_status_str(pa_status s) {

@@ -71,6 +71,7 @@ class Step:
     seq_lens: torch.Tensor       # [N] int32, lengths after this step's writes
     seq_ids: torch.Tensor = None     # [n_tok] int32: sequence of each new token
     positions: torch.Tensor = None   # [n_tok] int32: its position in that sequence
+    query_start: torch.Tensor = None  # [N + 1] int32: query rows per sequence (prefill)
 
 
 @dataclass
@@ -291,6 +292,43 @@ def cb(num_seqs=256, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16
                     1.0 / math.sqrt(head_dim), kc, vc, steps, seed, _stats(pool, seqs))
 
 
+def prefill(num_seqs=8, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+            max_len0=4096, chunk=2048, num_blocks=65536, seed=7,
+            dtype=torch.bfloat16) -> Workload:
+    """Chunked prefill: every sequence has a seeded history T0 ~ U[1, max_len0]
+    and takes a chunk of `chunk` new tokens; the step writes the chunk's K/V,
+    then attends causally from each chunk token (q rows = the chunk)."""
+    rng = np.random.default_rng(seed)
+    lens0 = rng.integers(1, max_len0 + 1, size=num_seqs)
+    pool = BlockPool(num_blocks, block_size, rng.permutation(num_blocks))
+    seqs = list(range(num_seqs))
+    for s in seqs:
+        pool.add(s, int(lens0[s]))
+    kc, vc = _fill_history(pool, num_kv_heads, head_dim, dtype, seed)
+    slots, tok_seq, tok_pos, qs = [], [], [], [0]
+    for s in seqs:
+        start = pool.lengths[s]
+        pool.grow(s, chunk)
+        slots.extend(pool.slots(s, start, chunk))
+        tok_seq.extend([s] * chunk)
+        tok_pos.extend(range(start, start + chunk))
+        qs.append(qs[-1] + chunk)
+    n_tok = len(slots)
+    width = pool.blocks_for(max_len0 + chunk)
+    step = Step(q=normal((n_tok, num_q_heads, head_dim), seed, 10, dtype),
+                k_new=normal((n_tok, num_kv_heads, head_dim), seed, 11, dtype),
+                v_new=normal((n_tok, num_kv_heads, head_dim), seed, 12, dtype),
+                slot_mapping=torch.tensor(slots, dtype=torch.int64),
+                block_tables=torch.tensor(pool.table_rows(seqs, width), dtype=torch.int32),
+                seq_lens=torch.tensor([pool.lengths[s] for s in seqs], dtype=torch.int32),
+                seq_ids=torch.tensor(tok_seq, dtype=torch.int32),
+                positions=torch.tensor(tok_pos, dtype=torch.int32),
+                query_start=torch.tensor(qs, dtype=torch.int32))
+    return Workload("prefill", dtype, num_blocks, block_size, num_q_heads, num_kv_heads,
+                    head_dim, 1.0 / math.sqrt(head_dim), kc, vc, [step], seed,
+                    _stats(pool, seqs))
+
+
 @dataclass
 class CopyWorkload:
     """Whole-block copies inside one pool: num_pairs disjoint (src, dst) pairs
@@ -326,7 +364,7 @@ def copy_pairs(num_blocks=65536, num_pairs=8192, num_kv_heads=8, head_dim=128, b
     return CopyWorkload("copy", k, v, pairs, seed)
 
 
-BUILDERS = {"tiny": tiny, "mha": mha, "gqa": gqa, "long": long, "cb": cb}
+BUILDERS = {"tiny": tiny, "mha": mha, "gqa": gqa, "long": long, "cb": cb, "prefill": prefill}
 
 
 def make(name: str, **overrides) -> Workload:

@@ -1,0 +1,159 @@
+"""pa_prefill (causal multi-query paged attention) on the GPU against the
+oracle: bf16 within 3e-3 + 1e-2 |ref|, fp32 within 1e-5."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_109_gb300 as pa
+from paged_kv_cache_109_gb300 import workloads
+from tests._gpu import BF16_ATOL, BF16_RTOL, assert_close, tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def clear_device_error(cuda_device):
+    pa.last_device_error()
+    yield
+
+
+def case(hq, hkv, d, bs, ctx, qlens, dtype=torch.bfloat16, seed=0, extra_blocks=3):
+    """Sequences of total length ctx[i] whose last qlens[i] positions are queried."""
+    g = torch.Generator().manual_seed(seed)
+    need = [-(-t // bs) for t in ctx]
+    nb = sum(need) + extra_blocks
+    perm = torch.randperm(nb, generator=g).tolist()
+    width = max(need)
+    tables, pos = [], 0
+    for k in need:
+        tables.append(perm[pos:pos + k] + [-1] * (width - k))
+        pos += k
+    kc = torch.randn(nb, hkv, bs, d, generator=g).to(dtype)
+    vc = torch.randn(nb, hkv, bs, d, generator=g).to(dtype)
+    qs = [0]
+    for L in qlens:
+        qs.append(qs[-1] + L)
+    q = torch.randn(qs[-1], hq, d, generator=g).to(dtype)
+    return (q, torch.tensor(qs, dtype=torch.int32), kc, vc,
+            torch.tensor(tables, dtype=torch.int32), torch.tensor(ctx, dtype=torch.int32))
+
+
+def run(dev, q, qs, kc, vc, bt, sl, scale):
+    out = pa.prefill(q.to(dev), qs.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), sl.to(dev),
+                     int((qs[1:] - qs[:-1]).max()), int(sl.max()), scale)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+FAST = [
+    # Hq, Hkv, D, B, contexts, query lengths
+    (32, 8, 128, 16, (300, 17, 64, 1000), (300, 5, 64, 100)),     # G=4: prompt, chunks
+    (32, 32, 128, 16, (70, 129), (70, 33)),                       # G=1 (MHA)
+    (64, 8, 128, 32, (257, 40), (100, 40)),                       # G=8, B=32
+    (16, 1, 128, 16, (90,), (17,)),                               # G=16
+    (8, 4, 64, 64, (130, 64, 1), (130, 7, 1)),                    # G=2, D=64, B=64
+    (32, 8, 128, 8, (45, 200), (45, 31)),                         # B=8
+    (32, 8, 128, 16, (5, 3, 9), (1, 1, 1)),                       # decode rows only
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,ctx,qlens", FAST)
+def test_fast_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens):
+    q, qs, kc, vc, bt, sl = case(hq, hkv, d, bs, ctx, qlens, seed=hq + bs)
+    assert pa.decode_path(hq, kc) == 1
+    scale = 1 / math.sqrt(d)
+    out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
+    ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "prefill")
+    assert pa.last_device_error() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,ctx,qlens,dtype", [
+    (4, 2, 8, 4, (10, 7), (10, 3), torch.float32),               # the worked-example shape
+    (12, 4, 128, 16, (100, 33), (20, 33), torch.bfloat16),       # G=3: portable kernel
+    (6, 2, 96, 8, (50,), (9,), torch.bfloat16),                  # D=96
+    (32, 8, 128, 16, (300, 40), (64, 40), torch.float32),
+])
+def test_portable_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens, dtype):
+    q, qs, kc, vc, bt, sl = case(hq, hkv, d, bs, ctx, qlens, dtype=dtype, seed=d)
+    scale = 0.8 / math.sqrt(d)
+    out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
+    ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
+    atol, rtol = tolerance(dtype)
+    assert_close(out.double().numpy(), ref, atol, rtol, "portable prefill")
+
+
+def test_long_context_slides_the_table_window(cuda_device):
+    """A 20000-token context needs 1250 table entries: more than the kernel's
+    1024-entry window."""
+    q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (20000,), (70,), seed=3)
+    scale = 1 / math.sqrt(128)
+    out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
+    ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "long context")
+
+
+def test_decode_rows_agree_with_pa_decode(cuda_device):
+    q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (700, 30, 2000), (1, 1, 1), seed=4)
+    scale = 1 / math.sqrt(128)
+    out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
+    dec = pa.decode(q.to(cuda_device), kc.to(cuda_device), vc.to(cuda_device),
+                    bt.to(cuda_device), sl.to(cuda_device), int(sl.max()), scale).cpu()
+    assert_close(out.double().numpy(), dec.double().numpy(), 2 * BF16_ATOL, 2 * BF16_RTOL,
+                 "prefill vs decode")
+
+
+def test_chunks_agree_with_the_whole_prompt(cuda_device):
+    """Rows 60..99 of a 100-token prompt equal a 40-token chunk over the same
+    cache (the chunked-prefill invariant)."""
+    q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (100,), (100,), seed=5)
+    scale = 1 / math.sqrt(128)
+    whole = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
+    part = run(cuda_device, q[60:], torch.tensor([0, 40], dtype=torch.int32), kc, vc, bt, sl,
+               scale)
+    assert torch.equal(whole[60:], part) or \
+        np.abs(whole[60:].double().numpy() - part.double().numpy()).max() < 2 * BF16_ATOL
+
+
+def test_garbage_past_the_last_key_is_ignored(cuda_device):
+    q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (37, 90), (5, 90), seed=6)
+    scale = 1 / math.sqrt(128)
+    ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
+    for i, t in enumerate(sl.tolist()):
+        last = int(bt[i, (t - 1) // 16])
+        kc[last, :, t % 16:] = float("nan")
+        vc[last, :, t % 16:] = float("inf")
+    out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "nan tail")
+
+
+def test_query_longer_than_sequence_is_reported(cuda_device):
+    q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (40, 60), (10, 20), seed=7)
+    sl = sl.clone()
+    sl[0] = 5                                      # 10 query rows but only 5 positions
+    out = pa.prefill(q.to(cuda_device), qs.to(cuda_device), kc.to(cuda_device),
+                     vc.to(cuda_device), bt.to(cuda_device), sl.to(cuda_device), 20, 60, 0.1)
+    torch.cuda.synchronize()
+    assert pa.last_device_error() & pa.DEVERR_SEQ_LEN
+    ref = oracle.prefill(q[10:], torch.tensor([0, 20], dtype=torch.int32), kc, vc, bt[1:],
+                         sl[1:], 0.1)
+    assert_close(out[10:].double().cpu().numpy(), ref, BF16_ATOL, BF16_RTOL, "other sequence")
+
+
+def test_prefill_workload_reduced(cuda_device):
+    """The chunked-prefill workload at reduced size: write the chunk, attend."""
+    wl = workloads.prefill(num_seqs=3, max_len0=500, chunk=200, num_blocks=1024)
+    st = wl.steps[0]
+    kd, vd = wl.k_cache.to(cuda_device), wl.v_cache.to(cuda_device)
+    pa.write_kv(st.k_new.to(cuda_device), st.v_new.to(cuda_device),
+                st.slot_mapping.to(cuda_device), kd, vd)
+    out = pa.prefill(st.q.to(cuda_device), st.query_start.to(cuda_device), kd, vd,
+                     st.block_tables.to(cuda_device), st.seq_lens.to(cuda_device), 200,
+                     int(st.seq_lens.max()), wl.scale).cpu()
+    kh, vh = wl.k_cache.clone(), wl.v_cache.clone()
+    oracle.write_kv(st.k_new, st.v_new, st.slot_mapping, kh, vh)
+    ref = oracle.prefill(st.q, st.query_start, kh, vh, st.block_tables, st.seq_lens, wl.scale)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "prefill workload")
