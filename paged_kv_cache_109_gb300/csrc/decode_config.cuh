@@ -11,6 +11,9 @@
 
 #include "pa.h"
 
+#ifndef PA_PREFILL_MMA_SYNC
+#define PA_PREFILL_MMA_SYNC 0   // 1: warp-level mma.sync prefill instead of tcgen05
+#endif
 #ifndef PA_USE_PDL
 #define PA_USE_PDL 1   // launch with programmatic stream serialization
 #endif

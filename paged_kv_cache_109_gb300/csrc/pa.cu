@@ -18,6 +18,7 @@
 #include "decode_tma_mma.cuh"
 #include "merge.cuh"
 #include "prefill_generic.cuh"
+#include "prefill_tc.cuh"
 #include "prefill_tma_mma.cuh"
 #include "write_kv.cuh"
 
@@ -423,7 +424,11 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     a.num_blocks = cache->num_blocks;
     a.block_size = cache->block_size;
     a.head_dim = cache->head_dim;
-    a.tokens_per_tile = 64 % group == 0 ? 64 / group : 0;
+#if PA_PREFILL_MMA_SYNC
+    a.tokens_per_tile = 64 % group == 0 ? 64 / group : 0;     // 64-row mma.sync tiles
+#else
+    a.tokens_per_tile = 128 % group == 0 ? 128 / group : 0;   // 128-row tcgen05 tiles
+#endif
     a.scale_log2 = scale * kLog2e;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) &&
@@ -435,6 +440,7 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
             return PA_ERR_CUDA;
         const int32_t tiles = std::max(1, (max_q_len + a.tokens_per_tile - 1) / a.tokens_per_tile);
         dim3 grid(tiles, cache->num_kv_heads, num_seqs);
+#if PA_PREFILL_MMA_SYNC
         if (cache->head_dim == 128) {
             auto kern = prefill_tma_mma_kernel<128>;
             if (!set_smem(kern, PrefillCfg<128>::smem_bytes())) return PA_ERR_UNSUPPORTED;
@@ -444,6 +450,19 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
             if (!set_smem(kern, PrefillCfg<64>::smem_bytes())) return PA_ERR_UNSUPPORTED;
             err = launch_pdl(kern, grid, dim3(128), PrefillCfg<64>::smem_bytes(), st, mk, mv, a);
         }
+#else
+        if (cache->head_dim == 128) {
+            auto kern = prefill_tc_kernel<128>;
+            if (!set_smem(kern, PrefillTcCfg<128>::smem_bytes())) return PA_ERR_UNSUPPORTED;
+            err = launch_pdl(kern, grid, dim3(128), PrefillTcCfg<128>::smem_bytes(), st, mk, mv,
+                             a);
+        } else {
+            auto kern = prefill_tc_kernel<64>;
+            if (!set_smem(kern, PrefillTcCfg<64>::smem_bytes())) return PA_ERR_UNSUPPORTED;
+            err = launch_pdl(kern, grid, dim3(128), PrefillTcCfg<64>::smem_bytes(), st, mk, mv,
+                             a);
+        }
+#endif
     } else {
         if (cache->head_dim > 32 * kGenericMaxDimPerLane) return PA_ERR_UNSUPPORTED;
         dim3 grid(total_q, cache->num_kv_heads);
