@@ -446,7 +446,7 @@ def run_prefill(args, rank, world, device):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2),
         "prefill_tflops": round(tflops, 1),
-        "roofline": {"bound": "tensor", "kernel": "pa_prefill call (mma.sync bf16)",
+        "roofline": {"bound": "tensor", "kernel": "pa_prefill call (tcgen05 bf16)",
                      "achieved": round(tflops, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
                      "flops_per_call": flops, "prefill_ms_mean": round(statistics.mean(pre_ms), 4)},

@@ -40,18 +40,18 @@ struct PrefillTcCfg {
     static constexpr int kSlice = kKeys * 128;           // one block, one slice: 4 KiB
     static constexpr int kTile = kHalves * kSlice;       // K (or V) block
     static constexpr int kStageBytes = 2 * kTile;        // K + V
-    static constexpr int kStages = 3;
+    static constexpr int kStages = 4;
     static constexpr int kQSlice = kRows * 128;          // 16 KiB
     static constexpr int kQBytes = kHalves * kQSlice;
     static constexpr int kPBytes = kRows * kKeys * 2;    // 8 KiB, no-swizzle core matrices
     static constexpr int kWindow = 256;                  // block ids in shared memory
-    static constexpr uint32_t kTmemCols = 256;           // S: 32 columns, O: D columns
-    static constexpr uint32_t kOCol = 32;
+    static constexpr uint32_t kTmemCols = 256;           // S: 2 x 32 columns, O: D columns
+    static constexpr uint32_t kOCol = 64;
     static constexpr int kQOff = 0;
     static constexpr int kStageOff = kQBytes;
     static constexpr int kPOff = kStageOff + kStages * kStageBytes;
     static constexpr int kBarOff = kPOff + kPBytes;
-    static constexpr int kBars = kStages + 3;            // full[kStages], S, O, final drain
+    static constexpr int kBars = kStages + 4;            // full[kStages], S[2], O, final drain
     static constexpr int kSlotOff = kBarOff + 8 * kBars;
     static constexpr int kWinOff = kSlotOff + 16;
     static size_t smem_bytes() { return 1024 + kWinOff + 4 * kWindow; }
@@ -72,9 +72,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::kSlotOff);
     int32_t* win = reinterpret_cast<int32_t*>(sm + C::kWinOff);
-    const uint32_t bar_s = smem_u32(&bars[C::kStages]);
-    const uint32_t bar_o = smem_u32(&bars[C::kStages + 1]);
-    const uint32_t bar_fin = smem_u32(&bars[C::kStages + 2]);
+    const uint32_t bar_s0 = smem_u32(&bars[C::kStages]);      // S buffer 0, buffer 1 at +8
+    const uint32_t bar_o = smem_u32(&bars[C::kStages + 2]);
+    const uint32_t bar_fin = smem_u32(&bars[C::kStages + 3]);
 
     const int32_t tid = threadIdx.x, warp = tid >> 5;
     if (tid == 0) {
@@ -215,10 +215,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // thread 0: S = Q K^T for key block kb (its stage has landed)
     constexpr uint32_t kIdescS = umma_idesc_bf16(128, C::kKeys, 0);
     constexpr uint32_t kIdescO = umma_idesc_bf16(128, 64, 1);
-    auto issue_s = [&](int32_t kb) {
+    auto issue_s = [&](int32_t kb) {   // thread 0; S buffer kb & 1
         const int32_t st = kb % C::kStages;
+        const uint32_t bar = bar_s0 + 8 * (kb & 1);
         if (!s_stage_ok[st]) {
-            mbar_arrive(bar_s);
+            mbar_arrive(bar);
             return;
         }
         const uint32_t kbase = sm_u + C::kStageOff + st * C::kStageBytes;
@@ -228,37 +229,55 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 umma_sdesc(sm_u + C::kQOff + (ks >> 2) * C::kQSlice + (ks & 3) * 32, 16, 1024, 2);
             const uint64_t bd = umma_sdesc(kbase + (ks >> 2) * C::kSlice + (ks & 3) * 32, 16,
                                            1024, 2);
-            umma_bf16(s_tmem, ad, bd, kIdescS, ks > 0);
+            umma_bf16(s_tmem + (kb & 1) * C::kKeys, ad, bd, kIdescS, ks > 0);
         }
-        umma_commit(bar_s);
+        umma_commit(bar);
     };
 
     bool failed = false;
     bool o_init = false;                               // thread 0: O written at least once
+    bool t0_fail = false;                              // thread 0: a stage copy never landed
     if (tid == 0) {
         for (int32_t kb = 0; kb < min(nb, C::kStages); ++kb) issue(kb);
-        failed = !mbar_wait_bounded(smem_u32(&bars[0]), 0, kWaitLimitCycles);
-        if (!failed) {
+        if (!mbar_wait_bounded(smem_u32(&bars[0]), 0, kWaitLimitCycles)) {
+            t0_fail = true;
+            mbar_arrive(bar_s0);
+        } else {
             tc_fence_after();
             issue_s(0);
         }
     }
-    if (__syncthreads_or(failed)) failed = true;
 
-    float m = -INFINITY, l = 0.f;
-    bool t0_fail = false;                              // thread 0: a stage copy never landed
-    int32_t kb = 0;
-    for (; kb < nb && !failed; ++kb) {
+    // m_ref: the reference maximum P is taken against.  It moves only when a
+    // row's maximum exceeds it by more than 8 (base 2), so O is rescaled
+    // rarely; P stays <= 2^8 and O / l does not depend on the reference.
+    constexpr float kRescaleSlack = 8.f;
+    float m_ref = -INFINITY, l = 0.f;
+    for (int32_t kb = 0; kb < nb; ++kb) {
         const int32_t st = kb % C::kStages;
-        const bool s_ready = t0_fail ? false : mbar_wait_bounded(bar_s, kb & 1, kWaitLimitCycles);
+        const uint32_t bar_s = bar_s0 + 8 * (kb & 1);
+        const bool s_ready =
+            t0_fail ? false : mbar_wait_bounded(bar_s, (kb >> 1) & 1, kWaitLimitCycles);
         if (__syncthreads_or(!s_ready)) {
             failed = true;
             break;
         }
         tc_fence_after();
+        // start S of the next block now: it runs while this block's softmax does
+        if (tid == 0 && kb + 1 < nb) {
+            const int32_t st1 = (kb + 1) % C::kStages;
+            if (!mbar_wait_bounded(smem_u32(&bars[st1]), ((kb + 1) / C::kStages) & 1,
+                                   kWaitLimitCycles)) {
+                t0_fail = true;                // reported at the next S barrier
+                mbar_arrive(bar_s0 + 8 * ((kb + 1) & 1));
+            } else {
+                tc_fence_after();
+                issue_s(kb + 1);
+            }
+        }
         const bool ok = s_stage_ok[st];
         float sv[32];
-        if (ok) tmem_ld32(s_tmem + lane_base, sv);
+        if (ok) tmem_ld32(s_tmem + (kb & 1) * C::kKeys + lane_base, sv);
         float mx = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -266,16 +285,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             sv[j] = (ok && key <= pos) ? sv[j] * a.scale_log2 : -INFINITY;
             mx = fmaxf(mx, sv[j]);
         }
-        const float mn = fmaxf(m, mx);
-        const float alpha = mn == -INFINITY ? 1.f : exp2f(m - mn);
+        const bool raise = mx > m_ref + kRescaleSlack || (m_ref == -INFINITY && mx > -INFINITY);
+        const float m_new = raise ? mx : m_ref;
+        const float alpha = raise ? exp2f(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
         float rs = 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            sv[j] = mn == -INFINITY ? 0.f : exp2f(sv[j] - mn);
+            sv[j] = m_new == -INFINITY ? 0.f : exp2f(sv[j] - m_new);
             rs += sv[j];
         }
         l = l * alpha + rs;
-        m = mn;
+        m_ref = m_new;
         // the previous P V must be done before O is rescaled or P is rewritten
         if (kb > 0) {
             if (__syncthreads_or(!mbar_wait_bounded(bar_o, (kb - 1) & 1, kWaitLimitCycles))) {
@@ -283,7 +303,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 break;
             }
             tc_fence_after();
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     float ov[32];
@@ -338,8 +358,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 mbar_arrive(bar_o);
             }
         }
-        // refill the stage of block kb - 1 (its P V has completed), sliding
-        // the block-id window first when the refill needs it (uniform branch)
+        // refill the stage of block kb - 1 (its S and P V have completed),
+        // sliding the block-id window first when needed (uniform branch)
         const int32_t nxt = kb - 1 + C::kStages;
         if (kb >= 1 && nxt < nb) {
             if (last_blk(nxt) >= s_win0 + C::kWindow) {
@@ -348,16 +368,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 __syncthreads();
             }
             if (tid == 0) issue(nxt);
-        }
-        if (tid == 0 && kb + 1 < nb) {
-            const int32_t st1 = (kb + 1) % C::kStages;
-            if (!mbar_wait_bounded(smem_u32(&bars[st1]), ((kb + 1) / C::kStages) & 1,
-                                   kWaitLimitCycles)) {
-                t0_fail = true;               // reported at the next S barrier
-            } else {
-                tc_fence_after();
-                issue_s(kb + 1);
-            }
         }
     }
 
