@@ -14,6 +14,9 @@
 #ifndef PA_PREFILL_MMA_SYNC
 #define PA_PREFILL_MMA_SYNC 0   // 1: warp-level mma.sync prefill instead of tcgen05
 #endif
+#ifndef PA_PREFILL_KEYS
+#define PA_PREFILL_KEYS 128   // keys per block of the tcgen05 prefill (64 or 128)
+#endif
 #ifndef PA_USE_PDL
 #define PA_USE_PDL 1   // launch with programmatic stream serialization
 #endif

@@ -19,6 +19,7 @@
 #include "merge.cuh"
 #include "prefill_generic.cuh"
 #include "prefill_tc.cuh"
+#include "prefill_ws.cuh"
 #include "prefill_tma_mma.cuh"
 #include "write_kv.cuh"
 
@@ -429,16 +430,19 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
 #else
     a.tokens_per_tile = 128 % group == 0 ? 128 / group : 0;   // 128-row tcgen05 tiles
 #endif
+    constexpr int32_t kTilesPerCta = PA_PREFILL_MMA_SYNC ? 1 : 2;
     a.scale_log2 = scale * kLog2e;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the tensor-core kernel takes its row maximum before scaling: scale >= 0
     const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) &&
-                      aligned(k_cache, 16) && aligned(v_cache, 16);
+                      aligned(k_cache, 16) && aligned(v_cache, 16) && scale >= 0.f;
     cudaError_t err;
     if (fast) {
         CUtensorMap mk, mv;
         if (!cached_map(&mk, k_cache, cache, 0) || !cached_map(&mv, v_cache, cache, 1))
             return PA_ERR_CUDA;
-        const int32_t tiles = std::max(1, (max_q_len + a.tokens_per_tile - 1) / a.tokens_per_tile);
+        const int32_t per_cta = kTilesPerCta * a.tokens_per_tile;
+        const int32_t tiles = std::max(1, (max_q_len + per_cta - 1) / per_cta);
         dim3 grid(tiles, cache->num_kv_heads, num_seqs);
 #if PA_PREFILL_MMA_SYNC
         if (cache->head_dim == 128) {
@@ -452,15 +456,15 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
         }
 #else
         if (cache->head_dim == 128) {
-            auto kern = prefill_tc_kernel<128>;
-            if (!set_smem(kern, PrefillTcCfg<128>::smem_bytes())) return PA_ERR_UNSUPPORTED;
-            err = launch_pdl(kern, grid, dim3(128), PrefillTcCfg<128>::smem_bytes(), st, mk, mv,
-                             a);
+            using Cfg = PrefillWsCfg<128, PA_PREFILL_KEYS>;
+            auto kern = prefill_ws_kernel<128, PA_PREFILL_KEYS>;
+            if (!set_smem(kern, Cfg::smem_bytes())) return PA_ERR_UNSUPPORTED;
+            err = launch_pdl(kern, grid, dim3(Cfg::kThreads), Cfg::smem_bytes(), st, mk, mv, a);
         } else {
-            auto kern = prefill_tc_kernel<64>;
-            if (!set_smem(kern, PrefillTcCfg<64>::smem_bytes())) return PA_ERR_UNSUPPORTED;
-            err = launch_pdl(kern, grid, dim3(128), PrefillTcCfg<64>::smem_bytes(), st, mk, mv,
-                             a);
+            using Cfg = PrefillWsCfg<64, PA_PREFILL_KEYS>;
+            auto kern = prefill_ws_kernel<64, PA_PREFILL_KEYS>;
+            if (!set_smem(kern, Cfg::smem_bytes())) return PA_ERR_UNSUPPORTED;
+            err = launch_pdl(kern, grid, dim3(Cfg::kThreads), Cfg::smem_bytes(), st, mk, mv, a);
         }
 #endif
     } else {

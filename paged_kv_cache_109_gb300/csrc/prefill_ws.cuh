@@ -1,0 +1,402 @@
+// prefill_ws.cuh -- multi-query (chunked prefill) paged attention on the
+// 5th-generation tensor cores (tcgen05, tensor-memory accumulators), bf16,
+// with warp-specialised roles.
+//
+// Definition: sequence i's packed query rows are its last L_i positions; the
+// row at position p attends to keys 0..p of the sequence through its block
+// table ("vLLM source walkthrough: PagedAttention and Continuous Batching"
+// §2.8; "vLLM PagedAttention: from memory fragmentation to slot mapping" §6).
+//
+// One CTA per (pair of query tiles, kv head g, sequence i).  A tile is 128
+// MMA rows = (query token, query head of the group) pairs, head fastest, so
+// it holds 128/G tokens; the CTA's two tiles are consecutive.  Both tiles
+// share each key block, so K and V cross shared memory once per 256 rows.
+//
+//   warps 0-3  softmax of tile 0 (thread t owns tensor-memory lane t)
+//   warps 4-7  softmax of tile 1
+//   warp 8     producer: block-table lookups and TMA copies of K and V blocks
+//              (KEYS keys each) into a ring of shared-memory slots
+//   warp 9     MMA issue: S_t = Q_t K^T (M128 x N KEYS) and O_t += P_t V
+//              (M128 x N64 per 64 output columns), fp32 in tensor memory
+//
+// Per key block kb the MMA warp issues, for t = 0, 1: S_t(kb), then
+// O_t += P_t(kb-1) V(kb-1) as soon as softmax t has published P_t(kb-1).  So
+// S_t(kb) runs while the tensor core still has the previous block's P V to do,
+// and each softmax warpgroup overlaps the other's tensor-core work.
+//
+// Softmax per row and block: load S (tcgen05.ld), mask keys past the row's
+// position (diagonal blocks only), p = 2^(s c - m) with c = scale log2(e) and
+// a lazily moved reference maximum m (it moves only when the block maximum
+// exceeds it by more than 8, so O is rescaled rarely, p <= 2^8 and O / l does
+// not depend on m), accumulate l, write P (bf16, K-major core matrices) to
+// shared memory.  O is divided by l at the end.
+//
+// Synchronisation is by mbarriers only; every wait is bounded, and a timeout
+// raises PA_DEVERR_TIMEOUT and ends the role's work (the others then time
+// out too) without leaving copies or MMAs in flight past the CTA's end.
+#pragma once
+
+#include "prefill_tma_mma.cuh"
+
+namespace pa {
+
+template <int D, int KEYS>
+struct PrefillWsCfg {
+    static constexpr int kThreads = 320;
+    static constexpr int kSoftmaxWarps = 8;
+    static constexpr int kProducerWarp = 8;
+    static constexpr int kMmaWarp = 9;
+    static constexpr int kTiles = 2;
+    static constexpr int kRows = 128;                     // rows per tile = tensor-memory lanes
+    static constexpr int kKeys = KEYS;                    // N of S, K of P V
+    static constexpr int kHalves = D / 64;                // 64-column (128-byte) slices
+    static constexpr int kSlice = kKeys * 128;            // one block, one slice
+    static constexpr int kItem = kHalves * kSlice;        // K or V of one block
+    static constexpr int kQSlice = kRows * 128;
+    static constexpr int kQTile = kHalves * kQSlice;
+    static constexpr int kPTile = kRows * kKeys * 2;
+    static constexpr int kPGroup = kKeys / 8 * 128;       // P: stride of 8-row groups
+    static constexpr int kQOff = 0;
+    static constexpr int kSlotOff = kTiles * kQTile;
+    static constexpr int kSmemMax = 232448;               // dynamic shared memory per CTA
+    static constexpr int kSlots = (kSmemMax - 2048 - kSlotOff - kTiles * kPTile) / kItem;
+    static constexpr int kPOff = kSlotOff + kSlots * kItem;
+    static constexpr int kBarOff = kPOff + kTiles * kPTile;
+    static constexpr int kBars = 2 * kSlots + 7;          // K/V full, K/V empty, S, P, O, final
+    static constexpr int kTslotOff = kBarOff + 8 * kBars;
+    static size_t smem_bytes() { return 1024 + kTslotOff + 16; }
+    static constexpr uint32_t kTmemCols = 512;            // per tile: S at +0, O at +128
+    static constexpr uint32_t kTileCols = 256;
+    static constexpr uint32_t kOCol = 128;
+    static_assert(D == 64 || D == 128, "head_dim");
+    static_assert(KEYS == 64 || KEYS == 128, "key block");
+    static_assert(kSlots >= 3, "ring");
+};
+
+template <int D, int KEYS>
+__global__ void __launch_bounds__(320, 1)
+prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
+    using C = PrefillWsCfg<D, KEYS>;
+    extern __shared__ uint8_t sm_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sm_u = smem_u32(sm);
+    const uint32_t bar0 = sm_u + C::kBarOff;
+    auto kv_full = [&](int32_t s) { return bar0 + 8u * s; };
+    auto kv_empty = [&](int32_t s) { return bar0 + 8u * (C::kSlots + s); };
+    auto s_full = [&](int32_t t) { return bar0 + 8u * (2 * C::kSlots + t); };
+    auto p_full = [&](int32_t t) { return bar0 + 8u * (2 * C::kSlots + 2 + t); };
+    auto o_done = [&](int32_t t) { return bar0 + 8u * (2 * C::kSlots + 4 + t); };
+    const uint32_t bar_fin = bar0 + 8u * (2 * C::kSlots + 6);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::kTslotOff);
+
+    const int32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int32_t s = 0; s < C::kSlots; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        for (int32_t t = 0; t < C::kTiles; ++t) {
+            mbar_init(s_full(t), 1);
+            mbar_init(p_full(t), 4);                      // one arrival per softmax warp
+            mbar_init(o_done(t), 1);
+        }
+        mbar_init(bar_fin, 1);
+        mbar_fence_init();
+    }
+    if (warp == C::kProducerWarp && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+    }
+    griddep_wait();
+
+    const int32_t cta = gridDim.x - 1 - blockIdx.x;       // latest (longest) tiles first
+    const int32_t g = blockIdx.y, i = blockIdx.z;
+    const int32_t G = a.group, BS = a.block_size;
+    const int32_t q0 = a.query_start[i], L = a.query_start[i + 1] - q0;
+    const int32_t T = clamp_len(a, a.seq_lens[i]);
+    if (L > T) {
+        if (tid == 0 && cta == 0 && g == 0) raise_error(PA_DEVERR_SEQ_LEN);
+        return;
+    }
+    const int32_t tpt = C::kRows / G;                     // tokens per tile
+    const int32_t tok0 = cta * C::kTiles * tpt;
+    if (L <= 0 || tok0 >= L) return;
+    const int32_t ntok = min(C::kTiles * tpt, L - tok0);
+    const int32_t ntiles = ntok > tpt ? 2 : 1;
+    const int32_t pos0 = T - L + tok0;
+    const int32_t nkeys = pos0 + ntok;
+    const int32_t nb = (nkeys + C::kKeys - 1) / C::kKeys;
+
+    if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tslot), C::kTmemCols);
+
+    // softmax threads: row r of tile w
+    const int32_t w = warp >> 2, r = tid & (C::kRows - 1);
+    const int32_t tok = w * tpt + r / G, head = r - (r / G) * G;
+    const bool softmax = warp < C::kSoftmaxWarps && w < ntiles;
+    const bool row_ok = softmax && tok < ntok;
+    const int32_t pos = pos0 + min(tok, ntok - 1);
+    const int64_t row_elem = ((int64_t)(q0 + tok0 + tok) * a.num_q_heads + g * G + head) * D;
+    if (softmax) {
+        // Q row -> shared memory, 128-byte swizzle per 64-column slice
+        const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+#pragma unroll
+        for (int32_t c = 0; c < D / 8; ++c) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (row_ok) v = *reinterpret_cast<const uint4*>(q + row_elem + c * 8);
+            const int32_t h = c >> 3, cc = c & 7;
+            *reinterpret_cast<uint4*>(sm + C::kQOff + w * C::kQTile + h * C::kQSlice + r * 128 +
+                                      ((cc ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    // a bounded wait whose outcome is the same in every lane of the warp
+    auto warp_wait = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kWaitLimitCycles)) != 0;
+    };
+
+    if (warp == C::kProducerWarp) {
+        // ---- producer ------------------------------------------------------
+        const int32_t* table = a.block_tables + (int64_t)i * a.max_blocks;
+        const int32_t sub = BS >= 16 ? 16 : BS;           // rows per TMA box
+        const int32_t nsub = C::kKeys / sub;
+        const uint32_t box_bytes = (uint32_t)sub * 128u;
+        int32_t it = 0;                                   // ring items issued (K, V, K, V ...)
+        bool ok = true;
+        for (int32_t kb = 0; kb < nb && ok; ++kb) {
+            // lane j: the j-th box of the block (its paged block and row)
+            bool has = false;
+            int32_t y = 0, z = -1;
+            if (lane < nsub) {
+                const int32_t key0 = kb * C::kKeys + lane * sub;
+                has = key0 < nkeys;
+                if (has) {
+                    const int32_t blk = key0 / BS;
+                    const int32_t id = table[blk];
+                    y = key0 - blk * BS;
+                    if (id < 0 || id >= a.num_blocks)
+                        raise_error(PA_DEVERR_TABLE_ENTRY);   // z = -1: the box reads zeros
+                    else
+                        z = id * a.num_kv_heads + g;
+                }
+            }
+            const uint32_t nbox = __popc(__ballot_sync(0xffffffffu, has));
+            const uint32_t bytes = nbox * box_bytes * C::kHalves;
+            for (int32_t kv = 0; kv < 2; ++kv, ++it) {
+                const int32_t s = it % C::kSlots;
+                if (it >= C::kSlots && !warp_wait(kv_empty(s), ((it / C::kSlots) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(kv_full(s), bytes);
+                __syncwarp();
+                if (has) {
+                    const uint32_t dst = sm_u + C::kSlotOff + s * C::kItem + lane * box_bytes;
+                    const void* map = kv ? static_cast<const void*>(&tmap_v)
+                                         : static_cast<const void*>(&tmap_k);
+#pragma unroll
+                    for (int32_t h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(dst + h * C::kSlice, map, h * 64, y, z, kv_full(s));
+                }
+            }
+        }
+        // the last copy into each slot has landed before the CTA may end
+        for (int32_t j = max(0, it - C::kSlots); j < it; ++j)
+            mbar_wait_bounded(kv_full(j % C::kSlots), (j / C::kSlots) & 1, kWaitLimitCycles);
+        if (!ok && lane == 0) raise_error(PA_DEVERR_TIMEOUT);
+    } else if (warp == C::kMmaWarp) {
+        // ---- MMA issue -----------------------------------------------------
+        constexpr uint32_t kIdS = umma_idesc_bf16(128, C::kKeys, 0);
+        constexpr uint32_t kIdO = umma_idesc_bf16(128, 64, 1);
+        bool ok = true;
+        for (int32_t kb = 0; kb <= nb && ok; ++kb) {
+            const int32_t kit = 2 * kb, vit = 2 * kb - 1;  // K(kb), V(kb - 1)
+            const int32_t ks = kit % C::kSlots, vs = (vit + C::kSlots) % C::kSlots;
+            if (kb < nb) ok = warp_wait(kv_full(ks), (kit / C::kSlots) & 1);
+            if (ok && kb > 0) {
+                ok = warp_wait(kv_full(vs), (vit / C::kSlots) & 1);
+                const int32_t nvalid = nkeys - (kb - 1) * C::kKeys;
+                if (ok && kb == nb && nvalid < C::kKeys) {
+                    // V rows past the last key may hold anything (NaN): clear them
+                    uint8_t* vt = sm + C::kSlotOff + vs * C::kItem;
+                    const int32_t pieces = (C::kKeys - nvalid) * 8;
+                    for (int32_t x = lane; x < C::kHalves * pieces; x += 32) {
+                        const int32_t h = x / pieces, rr = x - h * pieces;
+                        *reinterpret_cast<uint4*>(vt + h * C::kSlice + nvalid * 128 + rr * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+            }
+            for (int32_t t = 0; t < ntiles && ok; ++t) {
+                if (kb > 0 && !warp_wait(p_full(t), (kb - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    if (kb < nb) {
+                        const uint32_t kbase = sm_u + C::kSlotOff + ks * C::kItem;
+                        const uint32_t qbase = sm_u + C::kQOff + t * C::kQTile;
+#pragma unroll
+                        for (int32_t k = 0; k < D / 16; ++k) {
+                            const uint64_t ad = umma_sdesc(
+                                qbase + (k >> 2) * C::kQSlice + (k & 3) * 32, 16, 1024, 2);
+                            const uint64_t bd = umma_sdesc(
+                                kbase + (k >> 2) * C::kSlice + (k & 3) * 32, 16, 1024, 2);
+                            umma_bf16(tmem + t * C::kTileCols, ad, bd, kIdS, k > 0);
+                        }
+                        umma_commit(s_full(t));
+                    }
+                    if (kb > 0) {
+                        const uint32_t vbase = sm_u + C::kSlotOff + vs * C::kItem;
+                        const uint32_t pbase = sm_u + C::kPOff + t * C::kPTile;
+#pragma unroll
+                        for (int32_t k = 0; k < C::kKeys / 16; ++k) {
+                            const uint64_t ad = umma_sdesc(pbase + k * 256, 128, C::kPGroup, 0);
+#pragma unroll
+                            for (int32_t h = 0; h < C::kHalves; ++h) {
+                                const uint64_t bd = umma_sdesc(
+                                    vbase + h * C::kSlice + k * 2048, 16, 1024, 2);
+                                umma_bf16(tmem + t * C::kTileCols + C::kOCol + h * 64, ad, bd,
+                                          kIdO, (kb > 1 || k > 0) ? 1u : 0u);
+                            }
+                        }
+                        umma_commit(o_done(t));
+                    }
+                }
+                __syncwarp();
+            }
+            if (ok && lane == 0) {
+                if (kb < nb) umma_commit(kv_empty(ks));
+                if (kb > 0) umma_commit(kv_empty(vs));
+            }
+            __syncwarp();
+        }
+        // every MMA issued has finished before tensor memory is released
+        if (lane == 0) umma_commit(bar_fin);
+        __syncwarp();
+        mbar_wait_bounded(bar_fin, 0, kWaitLimitCycles);
+        if (!ok && lane == 0) raise_error(PA_DEVERR_TIMEOUT);
+    } else if (softmax) {
+        // ---- softmax of tile w, row r --------------------------------------
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t s_tm = tmem + w * C::kTileCols + lane_base;
+        const uint32_t o_tm = s_tm + C::kOCol;
+        uint8_t* prow = sm + C::kPOff + w * C::kPTile + (r >> 3) * C::kPGroup + (r & 7) * 16;
+        const float c = a.scale_log2;                     // >= 0 on this path
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int32_t kb = 0; kb < nb; ++kb) {
+            if (!warp_wait(s_full(w), kb & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[C::kKeys / 32][32];
+#pragma unroll
+            for (int32_t q4 = 0; q4 < C::kKeys / 32; ++q4) tmem_ld32_async(s_tm + q4 * 32, sr[q4]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int32_t q4 = 0; q4 < C::kKeys / 32; ++q4) tmem_regs_ready(sr[q4]);
+            const int32_t key0 = kb * C::kKeys;
+            const bool full = key0 + C::kKeys - 1 <= pos;
+            float mraw = -INFINITY;
+            if (full) {
+#pragma unroll
+                for (int32_t j = 0; j < C::kKeys; ++j)
+                    mraw = fmaxf(mraw, __uint_as_float(sr[j >> 5][j & 31]));
+            } else {
+#pragma unroll
+                for (int32_t j = 0; j < C::kKeys; ++j)
+                    if (key0 + j <= pos) mraw = fmaxf(mraw, __uint_as_float(sr[j >> 5][j & 31]));
+            }
+            const float mx = mraw == -INFINITY ? -INFINITY : mraw * c;
+            const bool raise = mx > m_ref + 8.f;
+            const float m_new = raise ? mx : m_ref;
+            const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
+            const float nm = m_new == -INFINITY ? 0.f : -m_new;
+            float rs0 = 0.f, rs1 = 0.f;
+            uint32_t pk[C::kKeys / 2];
+#pragma unroll
+            for (int32_t j = 0; j < C::kKeys; j += 2) {
+                float p0 = ex2_approx(fmaf(__uint_as_float(sr[j >> 5][j & 31]), c, nm));
+                float p1 = ex2_approx(fmaf(__uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31]), c, nm));
+                if (!full) {
+                    p0 = key0 + j <= pos ? p0 : 0.f;
+                    p1 = key0 + j + 1 <= pos ? p1 : 0.f;
+                }
+                rs0 += p0;
+                rs1 += p1;
+                pk[j >> 1] = pack_bf16x2(p0, p1);
+            }
+            // the previous P V has finished: O may be rescaled, P rewritten
+            if (kb > 0) {
+                if (!warp_wait(o_done(w), (kb - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                    for (int32_t cc = 0; cc < D / 32; ++cc) {
+                        float ov[32];
+                        tmem_ld32(o_tm + cc * 32, ov);
+#pragma unroll
+                        for (int32_t j = 0; j < 32; ++j) ov[j] *= alpha;
+                        tmem_st32(o_tm + cc * 32, ov);
+                    }
+                }
+            }
+            // P row -> shared memory: K-major core matrices (8 rows x 16 bytes),
+            // key chunks 128 bytes apart, 8-row groups kPGroup bytes apart
+#pragma unroll
+            for (int32_t kc = 0; kc < C::kKeys / 8; ++kc)
+                *reinterpret_cast<uint4*>(prow + kc * 128) =
+                    make_uint4(pk[kc * 4], pk[kc * 4 + 1], pk[kc * 4 + 2], pk[kc * 4 + 3]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(w));
+            l = l * alpha + (rs0 + rs1);
+            m_ref = m_new;
+        }
+        if (ok) ok = warp_wait(o_done(w), (nb - 1) & 1);
+        if (ok) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+            for (int32_t cc = 0; cc < D / 32; ++cc) {
+                float ov[32];
+                tmem_ld32(o_tm + cc * 32, ov);
+                if (row_ok) {
+#pragma unroll
+                    for (int32_t q4 = 0; q4 < 4; ++q4) {
+                        uint4 v;
+                        v.x = pack_bf16x2(ov[q4 * 8 + 0] * inv, ov[q4 * 8 + 1] * inv);
+                        v.y = pack_bf16x2(ov[q4 * 8 + 2] * inv, ov[q4 * 8 + 3] * inv);
+                        v.z = pack_bf16x2(ov[q4 * 8 + 4] * inv, ov[q4 * 8 + 5] * inv);
+                        v.w = pack_bf16x2(ov[q4 * 8 + 6] * inv, ov[q4 * 8 + 7] * inv);
+                        *reinterpret_cast<uint4*>(out + row_elem + cc * 32 + q4 * 8) = v;
+                    }
+                }
+            }
+        } else if (lane == 0) {
+            raise_error(PA_DEVERR_TIMEOUT);
+        }
+    }
+    griddep_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+}  // namespace pa
