@@ -16,20 +16,24 @@
 //   warps 4-7  softmax of tile 1
 //   warp 8     producer: block-table lookups and TMA copies of K and V blocks
 //              (KEYS keys each) into a ring of shared-memory slots
-//   warp 9     MMA issue: S_t = Q_t K^T (M128 x N KEYS) and O_t += P_t V
-//              (M128 x N64 per 64 output columns), fp32 in tensor memory
+//   warp 9     MMA issue, fp32 accumulators in tensor memory:
+//                S_t  = Q_t K^T   M128 x N KEYS, A and B from shared memory
+//                O_t += P_t V     M128 x N D, A = P_t from tensor memory
 //
-// Per key block kb the MMA warp issues, for t = 0, 1: S_t(kb), then
-// O_t += P_t(kb-1) V(kb-1) as soon as softmax t has published P_t(kb-1).  So
-// S_t(kb) runs while the tensor core still has the previous block's P V to do,
-// and each softmax warpgroup overlaps the other's tensor-core work.
+// Tensor memory per tile: S_t (KEYS fp32 columns) and O_t (D columns).  The
+// softmax writes P_t (bf16 pairs) over the first KEYS/2 columns of S_t once
+// it has S_t in registers.  Per key block kb the MMA warp issues, for t = 0,
+// 1: O_t += P_t(kb-1) V(kb-1) as soon as softmax t publishes P_t(kb-1), then
+// S_t(kb) into the same columns (tcgen05 MMAs of one thread run in issue
+// order, so P_t is read before it is overwritten).  Each softmax warpgroup
+// overlaps the other tile's tensor-core work, and with P off shared memory
+// the K/V ring holds enough blocks to hide the copies' latency.
 //
 // Softmax per row and block: load S (tcgen05.ld), mask keys past the row's
 // position (diagonal blocks only), p = 2^(s c - m) with c = scale log2(e) and
 // a lazily moved reference maximum m (it moves only when the block maximum
 // exceeds it by more than 8, so O is rescaled rarely, p <= 2^8 and O / l does
-// not depend on m), accumulate l, write P (bf16, K-major core matrices) to
-// shared memory.  O is divided by l at the end.
+// not depend on m), accumulate l, store P.  O is divided by l at the end.
 //
 // Synchronisation is by mbarriers only; every wait is bounded, and a timeout
 // raises PA_DEVERR_TIMEOUT and ends the role's work (the others then time
@@ -54,23 +58,20 @@ struct PrefillWsCfg {
     static constexpr int kItem = kHalves * kSlice;        // K or V of one block
     static constexpr int kQSlice = kRows * 128;
     static constexpr int kQTile = kHalves * kQSlice;
-    static constexpr int kPTile = kRows * kKeys * 2;
-    static constexpr int kPGroup = kKeys / 8 * 128;       // P: stride of 8-row groups
     static constexpr int kQOff = 0;
     static constexpr int kSlotOff = kTiles * kQTile;
     static constexpr int kSmemMax = 232448;               // dynamic shared memory per CTA
-    static constexpr int kSlots = (kSmemMax - 2048 - kSlotOff - kTiles * kPTile) / kItem;
-    static constexpr int kPOff = kSlotOff + kSlots * kItem;
-    static constexpr int kBarOff = kPOff + kTiles * kPTile;
+    static constexpr int kSlots = (kSmemMax - 2048 - kSlotOff) / kItem;
+    static constexpr int kBarOff = kSlotOff + kSlots * kItem;
     static constexpr int kBars = 2 * kSlots + 7;          // K/V full, K/V empty, S, P, O, final
     static constexpr int kTslotOff = kBarOff + 8 * kBars;
     static size_t smem_bytes() { return 1024 + kTslotOff + 16; }
-    static constexpr uint32_t kTmemCols = 512;            // per tile: S at +0, O at +128
+    static constexpr uint32_t kTmemCols = 512;            // per tile: S (and P) at +0, O at +128
     static constexpr uint32_t kTileCols = 256;
     static constexpr uint32_t kOCol = 128;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(KEYS == 64 || KEYS == 128, "key block");
-    static_assert(kSlots >= 3, "ring");
+    static_assert(kSlots >= 4, "ring");
 };
 
 template <int D, int KEYS>
@@ -213,7 +214,7 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
     } else if (warp == C::kMmaWarp) {
         // ---- MMA issue -----------------------------------------------------
         constexpr uint32_t kIdS = umma_idesc_bf16(128, C::kKeys, 0);
-        constexpr uint32_t kIdO = umma_idesc_bf16(128, 64, 1);
+        constexpr uint32_t kIdO = umma_idesc_bf16(128, D, 1);
         bool ok = true;
         for (int32_t kb = 0; kb <= nb && ok; ++kb) {
             const int32_t kit = 2 * kb, vit = 2 * kb - 1;  // K(kb), V(kb - 1)
@@ -236,41 +237,39 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 __syncwarp();
             }
             for (int32_t t = 0; t < ntiles && ok; ++t) {
-                if (kb > 0 && !warp_wait(p_full(t), (kb - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    if (kb < nb) {
-                        const uint32_t kbase = sm_u + C::kSlotOff + ks * C::kItem;
-                        const uint32_t qbase = sm_u + C::kQOff + t * C::kQTile;
-#pragma unroll
-                        for (int32_t k = 0; k < D / 16; ++k) {
-                            const uint64_t ad = umma_sdesc(
-                                qbase + (k >> 2) * C::kQSlice + (k & 3) * 32, 16, 1024, 2);
-                            const uint64_t bd = umma_sdesc(
-                                kbase + (k >> 2) * C::kSlice + (k & 3) * 32, 16, 1024, 2);
-                            umma_bf16(tmem + t * C::kTileCols, ad, bd, kIdS, k > 0);
-                        }
-                        umma_commit(s_full(t));
+                const uint32_t s_t = tmem + t * C::kTileCols;
+                if (kb > 0) {
+                    // O_t += P_t(kb - 1) V(kb - 1); V: MN-major, 64-column atoms
+                    // kSlice bytes apart (LBO); P: 16 keys = 8 columns per step
+                    if (!warp_wait(p_full(t), (kb - 1) & 1)) {
+                        ok = false;
+                        break;
                     }
-                    if (kb > 0) {
+                    tc_fence_after();
+                    if (lane == 0) {
                         const uint32_t vbase = sm_u + C::kSlotOff + vs * C::kItem;
-                        const uint32_t pbase = sm_u + C::kPOff + t * C::kPTile;
 #pragma unroll
                         for (int32_t k = 0; k < C::kKeys / 16; ++k) {
-                            const uint64_t ad = umma_sdesc(pbase + k * 256, 128, C::kPGroup, 0);
-#pragma unroll
-                            for (int32_t h = 0; h < C::kHalves; ++h) {
-                                const uint64_t bd = umma_sdesc(
-                                    vbase + h * C::kSlice + k * 2048, 16, 1024, 2);
-                                umma_bf16(tmem + t * C::kTileCols + C::kOCol + h * 64, ad, bd,
-                                          kIdO, (kb > 1 || k > 0) ? 1u : 0u);
-                            }
+                            const uint64_t bd = umma_sdesc(vbase + k * 2048, C::kSlice, 1024, 2);
+                            umma_bf16_ts(s_t + C::kOCol, s_t + k * 8, bd, kIdO,
+                                         (kb > 1 || k > 0) ? 1u : 0u);
                         }
                         umma_commit(o_done(t));
                     }
+                }
+                if (kb < nb && lane == 0) {
+                    // S_t(kb) = Q_t K(kb)^T over the columns P_t(kb - 1) occupied
+                    const uint32_t kbase = sm_u + C::kSlotOff + ks * C::kItem;
+                    const uint32_t qbase = sm_u + C::kQOff + t * C::kQTile;
+#pragma unroll
+                    for (int32_t k = 0; k < D / 16; ++k) {
+                        const uint64_t ad =
+                            umma_sdesc(qbase + (k >> 2) * C::kQSlice + (k & 3) * 32, 16, 1024, 2);
+                        const uint64_t bd =
+                            umma_sdesc(kbase + (k >> 2) * C::kSlice + (k & 3) * 32, 16, 1024, 2);
+                        umma_bf16(s_t, ad, bd, kIdS, k > 0);
+                    }
+                    umma_commit(s_full(t));
                 }
                 __syncwarp();
             }
@@ -290,7 +289,6 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t s_tm = tmem + w * C::kTileCols + lane_base;
         const uint32_t o_tm = s_tm + C::kOCol;
-        uint8_t* prow = sm + C::kPOff + w * C::kPTile + (r >> 3) * C::kPGroup + (r & 7) * 16;
         const float c = a.scale_log2;                     // >= 0 on this path
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
@@ -308,36 +306,51 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             for (int32_t q4 = 0; q4 < C::kKeys / 32; ++q4) tmem_regs_ready(sr[q4]);
             const int32_t key0 = kb * C::kKeys;
             const bool full = key0 + C::kKeys - 1 <= pos;
-            float mraw = -INFINITY;
+            float mp[8];
+#pragma unroll
+            for (int32_t u = 0; u < 8; ++u) mp[u] = -INFINITY;
             if (full) {
 #pragma unroll
                 for (int32_t j = 0; j < C::kKeys; ++j)
-                    mraw = fmaxf(mraw, __uint_as_float(sr[j >> 5][j & 31]));
+                    mp[j & 7] = fmaxf(mp[j & 7], __uint_as_float(sr[j >> 5][j & 31]));
             } else {
 #pragma unroll
                 for (int32_t j = 0; j < C::kKeys; ++j)
-                    if (key0 + j <= pos) mraw = fmaxf(mraw, __uint_as_float(sr[j >> 5][j & 31]));
+                    if (key0 + j <= pos)
+                        mp[j & 7] = fmaxf(mp[j & 7], __uint_as_float(sr[j >> 5][j & 31]));
             }
+            const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                     fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
             const float mx = mraw == -INFINITY ? -INFINITY : mraw * c;
             const bool raise = mx > m_ref + 8.f;
             const float m_new = raise ? mx : m_ref;
             const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
             const float nm = m_new == -INFINITY ? 0.f : -m_new;
-            float rs0 = 0.f, rs1 = 0.f;
-            uint32_t pk[C::kKeys / 2];
+            float rs[4];
 #pragma unroll
-            for (int32_t j = 0; j < C::kKeys; j += 2) {
-                float p0 = ex2_approx(fmaf(__uint_as_float(sr[j >> 5][j & 31]), c, nm));
-                float p1 = ex2_approx(fmaf(__uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31]), c, nm));
-                if (!full) {
-                    p0 = key0 + j <= pos ? p0 : 0.f;
-                    p1 = key0 + j + 1 <= pos ? p1 : 0.f;
+            for (int32_t u = 0; u < 4; ++u) rs[u] = 0.f;
+            // P -> tensor memory over the first KEYS/2 columns of S_t (S_t is
+            // in registers, and P_t(kb - 1) V(kb - 1) ran before S_t(kb)), 64
+            // keys = 32 columns at a time
+#pragma unroll
+            for (int32_t q4 = 0; q4 < C::kKeys / 64; ++q4) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int32_t jj = 0; jj < 32; ++jj) {
+                    const int32_t j = q4 * 64 + 2 * jj;
+                    float p0 = ex2_approx(fmaf(__uint_as_float(sr[j >> 5][j & 31]), c, nm));
+                    float p1 =
+                        ex2_approx(fmaf(__uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31]), c, nm));
+                    if (!full) {
+                        p0 = key0 + j <= pos ? p0 : 0.f;
+                        p1 = key0 + j + 1 <= pos ? p1 : 0.f;
+                    }
+                    rs[jj & 3] += p0 + p1;
+                    pk[jj] = pack_bf16x2(p0, p1);
                 }
-                rs0 += p0;
-                rs1 += p1;
-                pk[j >> 1] = pack_bf16x2(p0, p1);
+                tmem_st32_async(s_tm + q4 * 32, pk);
             }
-            // the previous P V has finished: O may be rescaled, P rewritten
+            // O may be rescaled once the previous P V has finished
             if (kb > 0) {
                 if (!warp_wait(o_done(w), (kb - 1) & 1)) {
                     ok = false;
@@ -355,17 +368,11 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     }
                 }
             }
-            // P row -> shared memory: K-major core matrices (8 rows x 16 bytes),
-            // key chunks 128 bytes apart, 8-row groups kPGroup bytes apart
-#pragma unroll
-            for (int32_t kc = 0; kc < C::kKeys / 8; ++kc)
-                *reinterpret_cast<uint4*>(prow + kc * 128) =
-                    make_uint4(pk[kc * 4], pk[kc * 4 + 1], pk[kc * 4 + 2], pk[kc * 4 + 3]);
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(w));
-            l = l * alpha + (rs0 + rs1);
+            l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
             m_ref = m_new;
         }
         if (ok) ok = warp_wait(o_done(w), (nb - 1) & 1);
