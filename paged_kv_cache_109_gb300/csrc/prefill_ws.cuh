@@ -215,10 +215,22 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // ---- MMA issue -----------------------------------------------------
         constexpr uint32_t kIdS = umma_idesc_bf16(128, C::kKeys, 0);
         constexpr uint32_t kIdO = umma_idesc_bf16(128, D, 1);
+        // Descriptors of step 0; a step adds its byte offset / 16 to the start
+        // address field (addresses stay below 2^18, so the field never carries).
+        uint64_t qdesc[C::kTiles];
+#pragma unroll
+        for (int32_t t = 0; t < C::kTiles; ++t)
+            qdesc[t] = umma_sdesc(sm_u + C::kQOff + t * C::kQTile, 16, 1024, 2);
+        const bool leader = elect_one();
         bool ok = true;
         for (int32_t kb = 0; kb <= nb && ok; ++kb) {
             const int32_t kit = 2 * kb, vit = 2 * kb - 1;  // K(kb), V(kb - 1)
             const int32_t ks = kit % C::kSlots, vs = (vit + C::kSlots) % C::kSlots;
+            // K: K-major, 128-byte swizzle; V: MN-major, 64-column atoms kSlice
+            // bytes apart (LBO)
+            const uint64_t kdesc = umma_sdesc(sm_u + C::kSlotOff + ks * C::kItem, 16, 1024, 2);
+            const uint64_t vdesc =
+                umma_sdesc(sm_u + C::kSlotOff + vs * C::kItem, C::kSlice, 1024, 2);
             if (kb < nb) ok = warp_wait(kv_full(ks), (kit / C::kSlots) & 1);
             if (ok && kb > 0) {
                 ok = warp_wait(kv_full(vs), (vit / C::kSlots) & 1);
@@ -239,48 +251,39 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             for (int32_t t = 0; t < ntiles && ok; ++t) {
                 const uint32_t s_t = tmem + t * C::kTileCols;
                 if (kb > 0) {
-                    // O_t += P_t(kb - 1) V(kb - 1); V: MN-major, 64-column atoms
-                    // kSlice bytes apart (LBO); P: 16 keys = 8 columns per step
+                    // O_t += P_t(kb - 1) V(kb - 1); P: 16 keys = 8 columns per step
                     if (!warp_wait(p_full(t), (kb - 1) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t vbase = sm_u + C::kSlotOff + vs * C::kItem;
+                    if (leader) {
 #pragma unroll
-                        for (int32_t k = 0; k < C::kKeys / 16; ++k) {
-                            const uint64_t bd = umma_sdesc(vbase + k * 2048, C::kSlice, 1024, 2);
-                            umma_bf16_ts(s_t + C::kOCol, s_t + k * 8, bd, kIdO,
-                                         (kb > 1 || k > 0) ? 1u : 0u);
-                        }
+                        for (int32_t k = 0; k < C::kKeys / 16; ++k)
+                            umma_bf16_ts(s_t + C::kOCol, s_t + k * 8, vdesc + (uint64_t)(k * 128),
+                                         kIdO, (kb > 1 || k > 0) ? 1u : 0u);
                         umma_commit(o_done(t));
                     }
                 }
-                if (kb < nb && lane == 0) {
+                if (kb < nb && leader) {
                     // S_t(kb) = Q_t K(kb)^T over the columns P_t(kb - 1) occupied
-                    const uint32_t kbase = sm_u + C::kSlotOff + ks * C::kItem;
-                    const uint32_t qbase = sm_u + C::kQOff + t * C::kQTile;
 #pragma unroll
-                    for (int32_t k = 0; k < D / 16; ++k) {
-                        const uint64_t ad =
-                            umma_sdesc(qbase + (k >> 2) * C::kQSlice + (k & 3) * 32, 16, 1024, 2);
-                        const uint64_t bd =
-                            umma_sdesc(kbase + (k >> 2) * C::kSlice + (k & 3) * 32, 16, 1024, 2);
-                        umma_bf16(s_t, ad, bd, kIdS, k > 0);
-                    }
+                    for (int32_t k = 0; k < D / 16; ++k)
+                        umma_bf16(s_t, qdesc[t] + (uint64_t)((k >> 2) * (C::kQSlice >> 4) + (k & 3) * 2),
+                                  kdesc + (uint64_t)((k >> 2) * (C::kSlice >> 4) + (k & 3) * 2), kIdS,
+                                  k > 0 ? 1u : 0u);
                     umma_commit(s_full(t));
                 }
                 __syncwarp();
             }
-            if (ok && lane == 0) {
+            if (ok && leader) {
                 if (kb < nb) umma_commit(kv_empty(ks));
                 if (kb > 0) umma_commit(kv_empty(vs));
             }
             __syncwarp();
         }
         // every MMA issued has finished before tensor memory is released
-        if (lane == 0) umma_commit(bar_fin);
+        if (leader) umma_commit(bar_fin);
         __syncwarp();
         mbar_wait_bounded(bar_fin, 0, kWaitLimitCycles);
         if (!ok && lane == 0) raise_error(PA_DEVERR_TIMEOUT);
@@ -298,57 +301,70 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 break;
             }
             tc_fence_after();
-            uint32_t sr[C::kKeys / 32][32];
-#pragma unroll
-            for (int32_t q4 = 0; q4 < C::kKeys / 32; ++q4) tmem_ld32_async(s_tm + q4 * 32, sr[q4]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int32_t q4 = 0; q4 < C::kKeys / 32; ++q4) tmem_regs_ready(sr[q4]);
             const int32_t key0 = kb * C::kKeys;
             const bool full = key0 + C::kKeys - 1 <= pos;
-            float mp[8];
+            // pass 1, row maximum: S in 64-column halves, four max3 chains
+            float mp[4];
 #pragma unroll
-            for (int32_t u = 0; u < 8; ++u) mp[u] = -INFINITY;
-            if (full) {
+            for (int32_t u = 0; u < 4; ++u) mp[u] = -INFINITY;
 #pragma unroll
-                for (int32_t j = 0; j < C::kKeys; ++j)
-                    mp[j & 7] = fmaxf(mp[j & 7], __uint_as_float(sr[j >> 5][j & 31]));
-            } else {
+            for (int32_t hh = 0; hh < C::kKeys / 64; ++hh) {
+                uint32_t sr[2][32];
+                tmem_ld32_async(s_tm + hh * 64, sr[0]);
+                tmem_ld32_async(s_tm + hh * 64 + 32, sr[1]);
+                tmem_wait_ld();
+                tmem_regs_ready(sr[0]);
+                tmem_regs_ready(sr[1]);
 #pragma unroll
-                for (int32_t j = 0; j < C::kKeys; ++j)
-                    if (key0 + j <= pos)
-                        mp[j & 7] = fmaxf(mp[j & 7], __uint_as_float(sr[j >> 5][j & 31]));
+                for (int32_t j = 0; j < 64; j += 8)
+#pragma unroll
+                    for (int32_t u = 0; u < 4; ++u) {
+                        const int32_t j0 = j + 2 * u, j1 = j0 + 1;
+                        float v0 = __uint_as_float(sr[j0 >> 5][j0 & 31]);
+                        float v1 = __uint_as_float(sr[j1 >> 5][j1 & 31]);
+                        if (!full) {
+                            v0 = key0 + hh * 64 + j0 <= pos ? v0 : -INFINITY;
+                            v1 = key0 + hh * 64 + j1 <= pos ? v1 : -INFINITY;
+                        }
+                        mp[u] = fmax3(mp[u], v0, v1);
+                    }
             }
-            const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                     fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+            const float mraw = fmaxf(fmax3(mp[0], mp[1], mp[2]), mp[3]);
             const float mx = mraw == -INFINITY ? -INFINITY : mraw * c;
             const bool raise = mx > m_ref + 8.f;
             const float m_new = raise ? mx : m_ref;
             const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
             const float nm = m_new == -INFINITY ? 0.f : -m_new;
-            float rs[4];
+            // pass 2: p = 2^(s c - m) two at a time (packed fp32 FMA and add) for
+            // each 64-column half of S, P -> tensor memory over the first KEYS/2
+            // columns of S_t: half hh of P lands on columns that hold keys already
+            // read (and P_t(kb - 1) V(kb - 1) ran before S_t(kb))
+            const float2 c2 = make_float2(c, c), nm2 = make_float2(nm, nm);
+            float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int32_t u = 0; u < 4; ++u) rs[u] = 0.f;
-            // P -> tensor memory over the first KEYS/2 columns of S_t (S_t is
-            // in registers, and P_t(kb - 1) V(kb - 1) ran before S_t(kb)), 64
-            // keys = 32 columns at a time
-#pragma unroll
-            for (int32_t q4 = 0; q4 < C::kKeys / 64; ++q4) {
+            for (int32_t hh = 0; hh < C::kKeys / 64; ++hh) {
+                uint32_t sr[2][32];
+                tmem_ld32_async(s_tm + hh * 64, sr[0]);
+                tmem_ld32_async(s_tm + hh * 64 + 32, sr[1]);
+                tmem_wait_ld();
+                tmem_regs_ready(sr[0]);
+                tmem_regs_ready(sr[1]);
                 uint32_t pk[32];
 #pragma unroll
                 for (int32_t jj = 0; jj < 32; ++jj) {
-                    const int32_t j = q4 * 64 + 2 * jj;
-                    float p0 = ex2_approx(fmaf(__uint_as_float(sr[j >> 5][j & 31]), c, nm));
-                    float p1 =
-                        ex2_approx(fmaf(__uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31]), c, nm));
+                    const int32_t j = 2 * jj;
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[j >> 5][j & 31]),
+                                                            __uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31])),
+                                                c2, nm2);
+                    float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                     if (!full) {
-                        p0 = key0 + j <= pos ? p0 : 0.f;
-                        p1 = key0 + j + 1 <= pos ? p1 : 0.f;
+                        pp.x = key0 + hh * 64 + j <= pos ? pp.x : 0.f;
+                        pp.y = key0 + hh * 64 + j + 1 <= pos ? pp.y : 0.f;
                     }
-                    rs[jj & 3] += p0 + p1;
-                    pk[jj] = pack_bf16x2(p0, p1);
+                    rs[jj & 1] = __fadd2_rn(rs[jj & 1], pp);
+                    pk[jj] = pack_bf16x2(pp.x, pp.y);
                 }
-                tmem_st32_async(s_tm + q4 * 32, pk);
+                tmem_st32_async(s_tm + hh * 32, pk);
             }
             // O may be rescaled once the previous P V has finished
             if (kb > 0) {
@@ -372,7 +388,7 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(w));
-            l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+            l = l * alpha + ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y));
             m_ref = m_new;
         }
         if (ok) ok = warp_wait(o_done(w), (nb - 1) & 1);
