@@ -33,7 +33,10 @@
 // position (diagonal blocks only), p = 2^(s c - m) with c = scale log2(e) and
 // a lazily moved reference maximum m (it moves only when the block maximum
 // exceeds it by more than 8, so O is rescaled rarely, p <= 2^8 and O / l does
-// not depend on m), accumulate l, store P.  O is divided by l at the end.
+// not depend on m), accumulate l, store P.  Since m rarely moves, p is
+// computed against the current m in the same pass that finds the block
+// maximum, and recomputed only for blocks that raise it.  O is divided by l
+// at the end.
 //
 // Synchronisation is by mbarriers only; every wait is bounded, and a timeout
 // raises PA_DEVERR_TIMEOUT and ends the role's work (the others then time
@@ -303,69 +306,56 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tc_fence_after();
             const int32_t key0 = kb * C::kKeys;
             const bool full = key0 + C::kKeys - 1 <= pos;
-            // pass 1, row maximum: S in 64-column halves, four max3 chains
+            // One pass over S, 32 columns at a time: p = 2^(s c - m_ref) against
+            // the current reference (packed fp32 FMA and add) and the block
+            // maximum.  If some row's maximum exceeds its reference by more than
+            // 8, the warp recomputes p from S (still in tensor memory: P is stored
+            // only afterwards), each row against its own, possibly raised,
+            // reference; rows that keep theirs get the same p again.
+            const float2 c2 = make_float2(c, c);
             float mp[4];
+            float2 rs[2];
+            uint32_t pk[C::kKeys / 64][32];
+            auto one_pass = [&](float ref, bool want_max) {
+                const float2 nm2 = make_float2(-ref, -ref);
+                rs[0] = rs[1] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int32_t u = 0; u < 4; ++u) mp[u] = -INFINITY;
+                for (int32_t u = 0; u < 4; ++u) mp[u] = -INFINITY;
 #pragma unroll
-            for (int32_t hh = 0; hh < C::kKeys / 64; ++hh) {
-                uint32_t sr[2][32];
-                tmem_ld32_async(s_tm + hh * 64, sr[0]);
-                tmem_ld32_async(s_tm + hh * 64 + 32, sr[1]);
-                tmem_wait_ld();
-                tmem_regs_ready(sr[0]);
-                tmem_regs_ready(sr[1]);
+                for (int32_t q4 = 0; q4 < C::kKeys / 32; ++q4) {
+                    uint32_t sr[32];
+                    tmem_ld32_async(s_tm + q4 * 32, sr);
+                    tmem_wait_ld();
+                    tmem_regs_ready(sr);
 #pragma unroll
-                for (int32_t j = 0; j < 64; j += 8)
-#pragma unroll
-                    for (int32_t u = 0; u < 4; ++u) {
-                        const int32_t j0 = j + 2 * u, j1 = j0 + 1;
-                        float v0 = __uint_as_float(sr[j0 >> 5][j0 & 31]);
-                        float v1 = __uint_as_float(sr[j1 >> 5][j1 & 31]);
-                        if (!full) {
-                            v0 = key0 + hh * 64 + j0 <= pos ? v0 : -INFINITY;
-                            v1 = key0 + hh * 64 + j1 <= pos ? v1 : -INFINITY;
-                        }
-                        mp[u] = fmax3(mp[u], v0, v1);
+                    for (int32_t jj = 0; jj < 16; ++jj) {
+                        const int32_t j = 2 * jj;
+                        const float v0 = __uint_as_float(sr[j]);
+                        const float v1 = __uint_as_float(sr[j + 1]);
+                        const bool in0 = full || key0 + q4 * 32 + j <= pos;
+                        const bool in1 = full || key0 + q4 * 32 + j + 1 <= pos;
+                        if (want_max)
+                            mp[jj & 3] = fmax3(mp[jj & 3], in0 ? v0 : -INFINITY, in1 ? v1 : -INFINITY);
+                        const float2 x = __ffma2_rn(make_float2(v0, v1), c2, nm2);
+                        float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        pp.x = in0 ? pp.x : 0.f;
+                        pp.y = in1 ? pp.y : 0.f;
+                        rs[jj & 1] = __fadd2_rn(rs[jj & 1], pp);
+                        pk[q4 >> 1][(q4 & 1) * 16 + jj] = pack_bf16x2(pp.x, pp.y);
                     }
-            }
+                }
+            };
+            one_pass(m_ref == -INFINITY ? 0.f : m_ref, true);
             const float mraw = fmaxf(fmax3(mp[0], mp[1], mp[2]), mp[3]);
             const float mx = mraw == -INFINITY ? -INFINITY : mraw * c;
             const bool raise = mx > m_ref + 8.f;
             const float m_new = raise ? mx : m_ref;
             const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
-            const float nm = m_new == -INFINITY ? 0.f : -m_new;
-            // pass 2: p = 2^(s c - m) two at a time (packed fp32 FMA and add) for
-            // each 64-column half of S, P -> tensor memory over the first KEYS/2
-            // columns of S_t: half hh of P lands on columns that hold keys already
-            // read (and P_t(kb - 1) V(kb - 1) ran before S_t(kb))
-            const float2 c2 = make_float2(c, c), nm2 = make_float2(nm, nm);
-            float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            if (__any_sync(0xffffffffu, raise)) one_pass(m_new == -INFINITY ? 0.f : m_new, false);
+            // P -> tensor memory over the first KEYS/2 columns of S_t (all of S
+            // has been read; P_t(kb - 1) V(kb - 1) ran before S_t(kb))
 #pragma unroll
-            for (int32_t hh = 0; hh < C::kKeys / 64; ++hh) {
-                uint32_t sr[2][32];
-                tmem_ld32_async(s_tm + hh * 64, sr[0]);
-                tmem_ld32_async(s_tm + hh * 64 + 32, sr[1]);
-                tmem_wait_ld();
-                tmem_regs_ready(sr[0]);
-                tmem_regs_ready(sr[1]);
-                uint32_t pk[32];
-#pragma unroll
-                for (int32_t jj = 0; jj < 32; ++jj) {
-                    const int32_t j = 2 * jj;
-                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[j >> 5][j & 31]),
-                                                            __uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31])),
-                                                c2, nm2);
-                    float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    if (!full) {
-                        pp.x = key0 + hh * 64 + j <= pos ? pp.x : 0.f;
-                        pp.y = key0 + hh * 64 + j + 1 <= pos ? pp.y : 0.f;
-                    }
-                    rs[jj & 1] = __fadd2_rn(rs[jj & 1], pp);
-                    pk[jj] = pack_bf16x2(pp.x, pp.y);
-                }
-                tmem_st32_async(s_tm + hh * 32, pk);
-            }
+            for (int32_t hh = 0; hh < C::kKeys / 64; ++hh) tmem_st32_async(s_tm + hh * 32, pk[hh]);
             // O may be rescaled once the previous P V has finished
             if (kb > 0) {
                 if (!warp_wait(o_done(w), (kb - 1) & 1)) {
