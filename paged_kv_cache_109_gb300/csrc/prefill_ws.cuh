@@ -43,6 +43,8 @@
 // out too) without leaving copies or MMAs in flight past the CTA's end.
 #pragma once
 
+#include <type_traits>
+
 #include "prefill_tma_mma.cuh"
 
 namespace pa {
@@ -316,7 +318,10 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             float mp[4];
             float2 rs[2];
             uint32_t pk[C::kKeys / 64][32];
-            auto one_pass = [&](float ref, bool want_max) {
+            // kMasked: a diagonal block (keys past some row's position); the
+            // common case is compiled without the per-key selects
+            auto one_pass = [&](float ref, bool want_max, auto masked) {
+                constexpr bool kMasked = decltype(masked)::value;
                 const float2 nm2 = make_float2(-ref, -ref);
                 rs[0] = rs[1] = make_float2(0.f, 0.f);
 #pragma unroll
@@ -330,28 +335,43 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
                     for (int32_t jj = 0; jj < 16; ++jj) {
                         const int32_t j = 2 * jj;
-                        const float v0 = __uint_as_float(sr[j]);
-                        const float v1 = __uint_as_float(sr[j + 1]);
-                        const bool in0 = full || key0 + q4 * 32 + j <= pos;
-                        const bool in1 = full || key0 + q4 * 32 + j + 1 <= pos;
-                        if (want_max)
-                            mp[jj & 3] = fmax3(mp[jj & 3], in0 ? v0 : -INFINITY, in1 ? v1 : -INFINITY);
+                        float v0 = __uint_as_float(sr[j]);
+                        float v1 = __uint_as_float(sr[j + 1]);
+                        bool in0 = true, in1 = true;
+                        if constexpr (kMasked) {
+                            in0 = key0 + q4 * 32 + j <= pos;
+                            in1 = key0 + q4 * 32 + j + 1 <= pos;
+                            v0 = in0 ? v0 : -INFINITY;       // 2^-inf = 0 below (c >= 0)
+                            v1 = in1 ? v1 : -INFINITY;
+                        }
+                        if (want_max) mp[jj & 3] = fmax3(mp[jj & 3], v0, v1);
                         const float2 x = __ffma2_rn(make_float2(v0, v1), c2, nm2);
                         float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        pp.x = in0 ? pp.x : 0.f;
-                        pp.y = in1 ? pp.y : 0.f;
+                        if constexpr (kMasked) {
+                            pp.x = in0 ? pp.x : 0.f;         // c = 0: -inf * 0 is NaN
+                            pp.y = in1 ? pp.y : 0.f;
+                        }
                         rs[jj & 1] = __fadd2_rn(rs[jj & 1], pp);
                         pk[q4 >> 1][(q4 & 1) * 16 + jj] = pack_bf16x2(pp.x, pp.y);
                     }
                 }
             };
-            one_pass(m_ref == -INFINITY ? 0.f : m_ref, true);
+            // the version is chosen per warp (the tcgen05 loads inside are
+            // warp-collective): unmasked only when every row sees the whole block
+            const bool warp_full = __all_sync(0xffffffffu, full) != 0;
+            auto run_pass = [&](float ref, bool want_max) {
+                if (warp_full)
+                    one_pass(ref, want_max, std::false_type{});
+                else
+                    one_pass(ref, want_max, std::true_type{});
+            };
+            run_pass(m_ref == -INFINITY ? 0.f : m_ref, true);
             const float mraw = fmaxf(fmax3(mp[0], mp[1], mp[2]), mp[3]);
             const float mx = mraw == -INFINITY ? -INFINITY : mraw * c;
             const bool raise = mx > m_ref + 8.f;
             const float m_new = raise ? mx : m_ref;
             const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
-            if (__any_sync(0xffffffffu, raise)) one_pass(m_new == -INFINITY ? 0.f : m_new, false);
+            if (__any_sync(0xffffffffu, raise)) run_pass(m_new == -INFINITY ? 0.f : m_new, false);
             // P -> tensor memory over the first KEYS/2 columns of S_t (all of S
             // has been read; P_t(kb - 1) V(kb - 1) ran before S_t(kb))
 #pragma unroll
