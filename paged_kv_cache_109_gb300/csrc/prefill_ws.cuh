@@ -308,74 +308,92 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tc_fence_after();
             const int32_t key0 = kb * C::kKeys;
             const bool full = key0 + C::kKeys - 1 <= pos;
-            // One pass over S, 32 columns at a time: p = 2^(s c - m_ref) against
-            // the current reference (packed fp32 FMA and add) and the block
-            // maximum.  If some row's maximum exceeds its reference by more than
-            // 8, the warp recomputes p from S (still in tensor memory: P is stored
-            // only afterwards), each row against its own, possibly raised,
-            // reference; rows that keep theirs get the same p again.
+            // Each 64-key half of S: load it, take its maximum, move this row's
+            // reference m_ref if that maximum exceeds it by more than 8, then
+            // p = 2^(s c - m_ref) (packed fp32 FMA and add) and P -> tensor
+            // memory over the first KEYS/2 columns of S_t (half hh of P lands on
+            // columns of keys already read; P_t(kb - 1) V(kb - 1) ran before
+            // S_t(kb)).  A reference raised in a later half rescales the halves
+            // of P already stored (their values only shrink).
             const float2 c2 = make_float2(c, c);
-            float mp[4];
-            float2 rs[2];
-            uint32_t pk[C::kKeys / 64][32];
-            // kMasked: a diagonal block (keys past some row's position); the
-            // common case is compiled without the per-key selects
-            auto one_pass = [&](float ref, bool want_max, auto masked) {
+            float alpha = 1.f;                            // this block's rescale of O
+            auto half = [&](int32_t hh, auto masked) {
                 constexpr bool kMasked = decltype(masked)::value;
-                const float2 nm2 = make_float2(-ref, -ref);
-                rs[0] = rs[1] = make_float2(0.f, 0.f);
+                uint32_t sr[2][32];
+                tmem_ld32_async(s_tm + hh * 64, sr[0]);
+                tmem_ld32_async(s_tm + hh * 64 + 32, sr[1]);
+                tmem_wait_ld();
+                tmem_regs_ready(sr[0]);
+                tmem_regs_ready(sr[1]);
+                if constexpr (kMasked) {
+#pragma unroll
+                    for (int32_t j = 0; j < 64; ++j)
+                        if (key0 + hh * 64 + j > pos) sr[j >> 5][j & 31] = __float_as_uint(-INFINITY);
+                }
+                float mp[4];
 #pragma unroll
                 for (int32_t u = 0; u < 4; ++u) mp[u] = -INFINITY;
 #pragma unroll
-                for (int32_t q4 = 0; q4 < C::kKeys / 32; ++q4) {
-                    uint32_t sr[32];
-                    tmem_ld32_async(s_tm + q4 * 32, sr);
-                    tmem_wait_ld();
-                    tmem_regs_ready(sr);
+                for (int32_t jj = 0; jj < 32; ++jj)
+                    mp[jj & 3] = fmax3(mp[jj & 3], __uint_as_float(sr[(2 * jj) >> 5][(2 * jj) & 31]),
+                                       __uint_as_float(sr[(2 * jj + 1) >> 5][(2 * jj + 1) & 31]));
+                const float mraw = fmaxf(fmax3(mp[0], mp[1], mp[2]), mp[3]);
+                const float mx = mraw == -INFINITY ? -INFINITY : mraw * c;
+                const bool up = mx > m_ref + 8.f;
+                const float a = up ? ex2_approx(m_ref - mx) : 1.f;   // 0 when m_ref = -inf
+                if (up) m_ref = mx;
+                alpha *= a;
+                l *= a;
+                if (hh > 0 && __any_sync(0xffffffffu, up)) {
+                    // rescale the P already stored (bf16 pairs) by this row's factor
+                    tmem_wait_st();
 #pragma unroll
-                    for (int32_t jj = 0; jj < 16; ++jj) {
-                        const int32_t j = 2 * jj;
-                        float v0 = __uint_as_float(sr[j]);
-                        float v1 = __uint_as_float(sr[j + 1]);
-                        bool in0 = true, in1 = true;
-                        if constexpr (kMasked) {
-                            in0 = key0 + q4 * 32 + j <= pos;
-                            in1 = key0 + q4 * 32 + j + 1 <= pos;
-                            v0 = in0 ? v0 : -INFINITY;       // 2^-inf = 0 below (c >= 0)
-                            v1 = in1 ? v1 : -INFINITY;
+                    for (int32_t h0 = 0; h0 < hh; ++h0) {
+                        uint32_t pr[32];
+                        tmem_ld32_async(s_tm + h0 * 32, pr);
+                        tmem_wait_ld();
+                        tmem_regs_ready(pr);
+#pragma unroll
+                        for (int32_t j = 0; j < 32; ++j) {
+                            const float2 f = __bfloat1622float2(
+                                *reinterpret_cast<const __nv_bfloat162*>(&pr[j]));
+                            pr[j] = pack_bf16x2(f.x * a, f.y * a);
                         }
-                        if (want_max) mp[jj & 3] = fmax3(mp[jj & 3], v0, v1);
-                        const float2 x = __ffma2_rn(make_float2(v0, v1), c2, nm2);
-                        float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        if constexpr (kMasked) {
-                            pp.x = in0 ? pp.x : 0.f;         // c = 0: -inf * 0 is NaN
-                            pp.y = in1 ? pp.y : 0.f;
-                        }
-                        rs[jj & 1] = __fadd2_rn(rs[jj & 1], pp);
-                        pk[q4 >> 1][(q4 & 1) * 16 + jj] = pack_bf16x2(pp.x, pp.y);
+                        tmem_st32_async(s_tm + h0 * 32, pr);
                     }
                 }
+                const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+                const float2 nm2 = make_float2(-ref, -ref);
+                float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                uint32_t pk[32];
+#pragma unroll
+                for (int32_t jj = 0; jj < 32; ++jj) {
+                    const int32_t j = 2 * jj;
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[j >> 5][j & 31]),
+                                                            __uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31])),
+                                                c2, nm2);
+                    float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    if constexpr (kMasked) {                 // c = 0: -inf * 0 is NaN
+                        pp.x = key0 + hh * 64 + j <= pos ? pp.x : 0.f;
+                        pp.y = key0 + hh * 64 + j + 1 <= pos ? pp.y : 0.f;
+                    }
+                    rs[jj & 1] = __fadd2_rn(rs[jj & 1], pp);
+                    pk[jj] = pack_bf16x2(pp.x, pp.y);
+                }
+                tmem_st32_async(s_tm + hh * 32, pk);
+                l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
             };
-            // the version is chosen per warp (the tcgen05 loads inside are
+            // the version is chosen per warp (the tcgen05 accesses inside are
             // warp-collective): unmasked only when every row sees the whole block
             const bool warp_full = __all_sync(0xffffffffu, full) != 0;
-            auto run_pass = [&](float ref, bool want_max) {
-                if (warp_full)
-                    one_pass(ref, want_max, std::false_type{});
-                else
-                    one_pass(ref, want_max, std::true_type{});
-            };
-            run_pass(m_ref == -INFINITY ? 0.f : m_ref, true);
-            const float mraw = fmaxf(fmax3(mp[0], mp[1], mp[2]), mp[3]);
-            const float mx = mraw == -INFINITY ? -INFINITY : mraw * c;
-            const bool raise = mx > m_ref + 8.f;
-            const float m_new = raise ? mx : m_ref;
-            const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
-            if (__any_sync(0xffffffffu, raise)) run_pass(m_new == -INFINITY ? 0.f : m_new, false);
-            // P -> tensor memory over the first KEYS/2 columns of S_t (all of S
-            // has been read; P_t(kb - 1) V(kb - 1) ran before S_t(kb))
 #pragma unroll
-            for (int32_t hh = 0; hh < C::kKeys / 64; ++hh) tmem_st32_async(s_tm + hh * 32, pk[hh]);
+            for (int32_t hh = 0; hh < C::kKeys / 64; ++hh) {
+                if (warp_full)
+                    half(hh, std::false_type{});
+                else
+                    half(hh, std::true_type{});
+            }
+            const bool raise = alpha != 1.f;
             // O may be rescaled once the previous P V has finished
             if (kb > 0) {
                 if (!warp_wait(o_done(w), (kb - 1) & 1)) {
@@ -398,8 +416,6 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(w));
-            l = l * alpha + ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y));
-            m_ref = m_new;
         }
         if (ok) ok = warp_wait(o_done(w), (nb - 1) & 1);
         if (ok) {
