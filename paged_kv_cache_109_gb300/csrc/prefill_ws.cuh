@@ -169,48 +169,70 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     if (warp == C::kProducerWarp) {
         // ---- producer ------------------------------------------------------
+        // Ring items in the order the MMA warp consumes them: K(0), then per
+        // block kb: K(kb + 1), V(kb); so K runs a block ahead of V.  Lane j
+        // copies the j-th box of a block; its block-table entry is read two
+        // blocks ahead of use, so the lookup latency overlaps the waits.
         const int32_t* table = a.block_tables + (int64_t)i * a.max_blocks;
         const int32_t sub = BS >= 16 ? 16 : BS;           // rows per TMA box
         const int32_t nsub = C::kKeys / sub;
         const uint32_t box_bytes = (uint32_t)sub * 128u;
-        int32_t it = 0;                                   // ring items issued (K, V, K, V ...)
+        auto lookup = [&](int32_t kb) {                    // raw table entry of lane's box
+            const int32_t key0 = kb * C::kKeys + lane * sub;
+            return (kb < nb && lane < nsub && key0 < nkeys) ? table[key0 / BS] : 0;
+        };
+        struct Box {
+            bool has;
+            int32_t y, z;
+            uint32_t bytes;
+        };
+        auto decode = [&](int32_t kb, int32_t id) {
+            Box bx{false, 0, -1, 0u};
+            const int32_t key0 = kb * C::kKeys + lane * sub;
+            bx.has = lane < nsub && key0 < nkeys;
+            if (bx.has) {
+                bx.y = key0 - (key0 / BS) * BS;
+                if (id < 0 || id >= a.num_blocks)
+                    raise_error(PA_DEVERR_TABLE_ENTRY);       // z = -1: the box reads zeros
+                else
+                    bx.z = id * a.num_kv_heads + g;
+            }
+            bx.bytes = __popc(__ballot_sync(0xffffffffu, bx.has)) * box_bytes * C::kHalves;
+            return bx;
+        };
+        int32_t it = 0;                                   // ring items issued
         bool ok = true;
-        for (int32_t kb = 0; kb < nb && ok; ++kb) {
-            // lane j: the j-th box of the block (its paged block and row)
-            bool has = false;
-            int32_t y = 0, z = -1;
-            if (lane < nsub) {
-                const int32_t key0 = kb * C::kKeys + lane * sub;
-                has = key0 < nkeys;
-                if (has) {
-                    const int32_t blk = key0 / BS;
-                    const int32_t id = table[blk];
-                    y = key0 - blk * BS;
-                    if (id < 0 || id >= a.num_blocks)
-                        raise_error(PA_DEVERR_TABLE_ENTRY);   // z = -1: the box reads zeros
-                    else
-                        z = id * a.num_kv_heads + g;
-                }
+        auto issue = [&](const Box& bx, bool is_v) {
+            const int32_t s = it % C::kSlots;
+            if (it >= C::kSlots && !warp_wait(kv_empty(s), ((it / C::kSlots) - 1) & 1)) {
+                ok = false;
+                return;
             }
-            const uint32_t nbox = __popc(__ballot_sync(0xffffffffu, has));
-            const uint32_t bytes = nbox * box_bytes * C::kHalves;
-            for (int32_t kv = 0; kv < 2; ++kv, ++it) {
-                const int32_t s = it % C::kSlots;
-                if (it >= C::kSlots && !warp_wait(kv_empty(s), ((it / C::kSlots) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) mbar_arrive_expect_tx(kv_full(s), bytes);
-                __syncwarp();
-                if (has) {
-                    const uint32_t dst = sm_u + C::kSlotOff + s * C::kItem + lane * box_bytes;
-                    const void* map = kv ? static_cast<const void*>(&tmap_v)
-                                         : static_cast<const void*>(&tmap_k);
+            if (lane == 0) mbar_arrive_expect_tx(kv_full(s), bx.bytes);
+            __syncwarp();
+            if (bx.has) {
+                const uint32_t dst = sm_u + C::kSlotOff + s * C::kItem + lane * box_bytes;
+                const void* map =
+                    is_v ? static_cast<const void*>(&tmap_v) : static_cast<const void*>(&tmap_k);
 #pragma unroll
-                    for (int32_t h = 0; h < C::kHalves; ++h)
-                        tma_load_3d(dst + h * C::kSlice, map, h * 64, y, z, kv_full(s));
-                }
+                for (int32_t h = 0; h < C::kHalves; ++h)
+                    tma_load_3d(dst + h * C::kSlice, map, h * 64, bx.y, bx.z, kv_full(s));
             }
+            ++it;
+        };
+        Box cur = decode(0, lookup(0));
+        int32_t raw_next = lookup(1);
+        issue(cur, false);                                // K(0)
+        for (int32_t kb = 0; kb < nb && ok; ++kb) {
+            const int32_t raw_after = lookup(kb + 2);
+            Box nxt{};
+            if (kb + 1 < nb) {
+                nxt = decode(kb + 1, raw_next);
+                issue(nxt, false);                        // K(kb + 1)
+            }
+            if (ok) issue(cur, true);                     // V(kb)
+            cur = nxt;
+            raw_next = raw_after;
         }
         // the last copy into each slot has landed before the CTA may end
         for (int32_t j = max(0, it - C::kSlots); j < it; ++j)
@@ -229,7 +251,10 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const bool leader = elect_one();
         bool ok = true;
         for (int32_t kb = 0; kb <= nb && ok; ++kb) {
-            const int32_t kit = 2 * kb, vit = 2 * kb - 1;  // K(kb), V(kb - 1)
+            // ring items: K(0) = 0, K(kb) = 2 kb - 1; V(kb) = 2 kb + 2, or 2 kb + 1
+            // for the last block (no K(kb + 1) before it)
+            const int32_t kit = kb == 0 ? 0 : 2 * kb - 1;
+            const int32_t vit = kb == 0 ? -1 : (kb < nb ? 2 * kb : 2 * kb - 1);   // V(kb - 1)
             const int32_t ks = kit % C::kSlots, vs = (vit + C::kSlots) % C::kSlots;
             // K: K-major, 128-byte swizzle; V: MN-major, 64-column atoms kSlice
             // bytes apart (LBO)
