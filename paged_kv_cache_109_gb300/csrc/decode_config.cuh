@@ -17,6 +17,9 @@
 #ifndef PA_PREFILL_KEYS
 #define PA_PREFILL_KEYS 128   // keys per block of the tcgen05 prefill (64 or 128)
 #endif
+#ifndef PA_PREFILL_PRODUCERS
+#define PA_PREFILL_PRODUCERS 2   // warps issuing the prefill's K/V copies
+#endif
 #ifndef PA_USE_PDL
 #define PA_USE_PDL 1   // launch with programmatic stream serialization
 #endif

@@ -51,9 +51,10 @@ namespace pa {
 
 template <int D, int KEYS>
 struct PrefillWsCfg {
-    static constexpr int kThreads = 320;
+    static constexpr int kProducers = PA_PREFILL_PRODUCERS;   // copy-issuing warps
+    static constexpr int kThreads = 32 * (9 + kProducers);
     static constexpr int kSoftmaxWarps = 8;
-    static constexpr int kProducerWarp = 8;
+    static constexpr int kProducerWarp = 8;               // and warps 10, 11, ...
     static constexpr int kMmaWarp = 9;
     static constexpr int kTiles = 2;
     static constexpr int kRows = 128;                     // rows per tile = tensor-memory lanes
@@ -80,7 +81,7 @@ struct PrefillWsCfg {
 };
 
 template <int D, int KEYS>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(PrefillWsCfg<D, KEYS>::kThreads, 1)
 prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
     using C = PrefillWsCfg<D, KEYS>;
@@ -167,8 +168,11 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
         return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kWaitLimitCycles)) != 0;
     };
 
-    if (warp == C::kProducerWarp) {
-        // ---- producer ------------------------------------------------------
+    if (warp == C::kProducerWarp || warp > C::kMmaWarp) {
+        // ---- producers -----------------------------------------------------
+        // kProducers warps share the ring round-robin (item j is issued by
+        // producer j % kProducers), so several warps' copies are in flight.
+        const int32_t parity = warp == C::kProducerWarp ? 0 : warp - C::kMmaWarp;
         // Ring items in the order the MMA warp consumes them: K(0), then per
         // block kb: K(kb + 1), V(kb); so K runs a block ahead of V.  Lane j
         // copies the j-th box of a block; its block-table entry is read two
@@ -203,6 +207,10 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
         int32_t it = 0;                                   // ring items issued
         bool ok = true;
         auto issue = [&](const Box& bx, bool is_v) {
+            if (it % C::kProducers != parity) {
+                ++it;
+                return;
+            }
             const int32_t s = it % C::kSlots;
             if (it >= C::kSlots && !warp_wait(kv_empty(s), ((it / C::kSlots) - 1) & 1)) {
                 ok = false;
@@ -236,7 +244,8 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         // the last copy into each slot has landed before the CTA may end
         for (int32_t j = max(0, it - C::kSlots); j < it; ++j)
-            mbar_wait_bounded(kv_full(j % C::kSlots), (j / C::kSlots) & 1, kWaitLimitCycles);
+            if (j % C::kProducers == parity)
+                mbar_wait_bounded(kv_full(j % C::kSlots), (j / C::kSlots) & 1, kWaitLimitCycles);
         if (!ok && lane == 0) raise_error(PA_DEVERR_TIMEOUT);
     } else if (warp == C::kMmaWarp) {
         // ---- MMA issue -----------------------------------------------------
