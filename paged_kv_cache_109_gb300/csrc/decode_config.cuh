@@ -11,15 +11,6 @@
 
 #include "pa.h"
 
-#ifndef PA_PREFILL_MMA_SYNC
-#define PA_PREFILL_MMA_SYNC 0   // 1: warp-level mma.sync prefill instead of tcgen05
-#endif
-#ifndef PA_PREFILL_KEYS
-#define PA_PREFILL_KEYS 128   // keys per block of the tcgen05 prefill (64 or 128)
-#endif
-#ifndef PA_PREFILL_PRODUCERS
-#define PA_PREFILL_PRODUCERS 2   // warps issuing the prefill's K/V copies
-#endif
 #ifndef PA_USE_PDL
 #define PA_USE_PDL 1   // launch with programmatic stream serialization
 #endif

@@ -18,9 +18,7 @@
 #include "decode_tma_mma.cuh"
 #include "merge.cuh"
 #include "prefill_generic.cuh"
-#include "prefill_tc.cuh"
 #include "prefill_ws.cuh"
-#include "prefill_tma_mma.cuh"
 #include "write_kv.cuh"
 
 namespace pa {
@@ -425,12 +423,8 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     a.num_blocks = cache->num_blocks;
     a.block_size = cache->block_size;
     a.head_dim = cache->head_dim;
-#if PA_PREFILL_MMA_SYNC
-    a.tokens_per_tile = 64 % group == 0 ? 64 / group : 0;     // 64-row mma.sync tiles
-#else
     a.tokens_per_tile = 128 % group == 0 ? 128 / group : 0;   // 128-row tcgen05 tiles
-#endif
-    constexpr int32_t kTilesPerCta = PA_PREFILL_MMA_SYNC ? 1 : 2;
+    constexpr int32_t kTilesPerCta = 2;
     a.scale_log2 = scale * kLog2e;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the tensor-core kernel takes its row maximum before scaling: scale >= 0
@@ -444,17 +438,6 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
         const int32_t per_cta = kTilesPerCta * a.tokens_per_tile;
         const int32_t tiles = std::max(1, (max_q_len + per_cta - 1) / per_cta);
         dim3 grid(tiles, cache->num_kv_heads, num_seqs);
-#if PA_PREFILL_MMA_SYNC
-        if (cache->head_dim == 128) {
-            auto kern = prefill_tma_mma_kernel<128>;
-            if (!set_smem(kern, PrefillCfg<128>::smem_bytes())) return PA_ERR_UNSUPPORTED;
-            err = launch_pdl(kern, grid, dim3(128), PrefillCfg<128>::smem_bytes(), st, mk, mv, a);
-        } else {
-            auto kern = prefill_tma_mma_kernel<64>;
-            if (!set_smem(kern, PrefillCfg<64>::smem_bytes())) return PA_ERR_UNSUPPORTED;
-            err = launch_pdl(kern, grid, dim3(128), PrefillCfg<64>::smem_bytes(), st, mk, mv, a);
-        }
-#else
         if (cache->head_dim == 128) {
             using Cfg = PrefillWsCfg<128, PA_PREFILL_KEYS>;
             auto kern = prefill_ws_kernel<128, PA_PREFILL_KEYS>;
@@ -466,7 +449,6 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
             if (!set_smem(kern, Cfg::smem_bytes())) return PA_ERR_UNSUPPORTED;
             err = launch_pdl(kern, grid, dim3(Cfg::kThreads), Cfg::smem_bytes(), st, mk, mv, a);
         }
-#endif
     } else {
         if (cache->head_dim > 32 * kGenericMaxDimPerLane) return PA_ERR_UNSUPPORTED;
         dim3 grid(total_q, cache->num_kv_heads);

@@ -8,7 +8,7 @@
 // online softmax (the same definition as the TMA kernel and the oracle).
 #pragma once
 
-#include "prefill_tma_mma.cuh"
+#include "prefill_args.cuh"
 
 namespace pa {
 

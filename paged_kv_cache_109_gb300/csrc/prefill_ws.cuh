@@ -45,7 +45,7 @@
 
 #include <type_traits>
 
-#include "prefill_tma_mma.cuh"
+#include "prefill_args.cuh"
 
 namespace pa {
 

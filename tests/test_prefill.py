@@ -157,3 +157,26 @@ def test_prefill_workload_reduced(cuda_device):
     oracle.write_kv(st.k_new, st.v_new, st.slot_mapping, kh, vh)
     ref = oracle.prefill(st.q, st.query_start, kh, vh, st.block_tables, st.seq_lens, wl.scale)
     assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "prefill workload")
+
+
+def test_negative_scale_takes_the_portable_kernel(cuda_device):
+    """The tensor-core kernel needs scale >= 0; a negative scale is still
+    computed exactly by the portable kernel."""
+    q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (150, 60), (40, 60), seed=8)
+    out = run(cuda_device, q, qs, kc, vc, bt, sl, -0.05)
+    ref = oracle.prefill(q, qs, kc, vc, bt, sl, -0.05)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "negative scale")
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (4, 2, 8)])
+def test_bad_table_entry_is_reported(cuda_device, hq, hkv, d):
+    """An out-of-range block id in one sequence's table raises the error bit;
+    the other sequence's rows are unaffected (fast and portable kernels)."""
+    q, qs, kc, vc, bt, sl = case(hq, hkv, d, 16, (300, 200), (100, 50), seed=9)
+    ref = oracle.prefill(q[100:], torch.tensor([0, 50], dtype=torch.int32), kc, vc, bt[1:],
+                         sl[1:], 1 / math.sqrt(d))
+    bad = bt.clone()
+    bad[0, 3] = kc.shape[0] + 5
+    out = run(cuda_device, q, qs, kc, vc, bad, sl, 1 / math.sqrt(d))
+    assert pa.last_device_error() & pa.DEVERR_TABLE_ENTRY
+    assert_close(out[100:].double().numpy(), ref, BF16_ATOL, BF16_RTOL, "other sequence")
