@@ -36,6 +36,7 @@ METRIC = "paged decode KV GB/s and % of GB300 HBM peak; decode tokens/s per laye
 L2_BYTES = 129 * 1024 * 1024
 DEC_SAMPLE = 8          # decode calls bracketed by events: every 8th step
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0     # GB300 HBM3e nominal, reported beside the measured denominator
 WORKLOAD_TEXT = {
     "mha": "MHA decode bf16: 32 seqs, Hq=Hkv=32, D=128, B=16, T~U[128,2048], 8192-block "
            "shuffled pool; step = write 1 new token per seq + decode",
@@ -193,30 +194,71 @@ def measured_peak() -> tuple[float, str]:
 
 # ---- CPU oracle (reference arm and cpu_baseline) ----------------------------------
 
-def time_oracle(wl, budget_s: float, max_reps: int = 50) -> dict:
+def time_oracle(wl, budget_s: float, max_reps: int = 50, gpu_outs=None,
+                one_core_s: float = 0.0) -> dict:
     """The oracle, as it stands, on the host cores: full steps (write + decode
-    of every (sequence, head)) repeated until ~budget_s seconds."""
+    of every (sequence, head)) repeated until ~budget_s seconds.  With
+    ``gpu_outs`` (the GPU's output of each step), each step's oracle output is
+    also compared with the GPU's (outside the timed span): the largest
+    absolute error and the largest ratio to the bf16 bound 3e-3 + 1e-2 |ref|."""
     import oracle
     threads = oracle.max_threads()
     kc, vc = wl.k_cache.clone(), wl.v_cache.clone()
-    done_bytes, reps, t0 = 0, 0, time.perf_counter()
-    elapsed = 0.0
+    done_bytes, reps, elapsed = 0, 0, 0.0
+    err_abs, err_ratio, checked = 0.0, 0.0, set()
     while reps < max_reps:
         k = reps % len(wl.steps)
         st = wl.steps[k]
+        t0 = time.perf_counter()
         oracle.write_kv(st.k_new, st.v_new, st.slot_mapping, kc, vc)
-        oracle.decode(st.q, kc, vc, st.block_tables, st.seq_lens, wl.scale)
+        ref = oracle.decode(st.q, kc, vc, st.block_tables, st.seq_lens, wl.scale)
+        elapsed += time.perf_counter() - t0
         b = step_bytes(wl, k, split_traffic=False)
         done_bytes += b["decode"] + b["write"]
         reps += 1
-        elapsed = time.perf_counter() - t0
+        if gpu_outs is not None and k not in checked:
+            got = gpu_outs[k].double().cpu().numpy()
+            diff = abs(got - ref)
+            err_abs = max(err_abs, float(diff.max()))
+            err_ratio = max(err_ratio, float((diff / (3e-3 + 1e-2 * abs(ref))).max()))
+            checked.add(k)
         if elapsed >= budget_s:
             break
-    return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": threads,
-            "kind": "oracle", "seconds": round(elapsed, 3), "steps": reps,
-            "sample": f"{reps} full step(s) of the {wl.name} workload (write + decode of "
-                      f"all sequences and heads), fp64 C oracle with OpenMP, "
-                      f"{elapsed:.1f} s"}
+    out = {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": threads,
+           "kind": "oracle", "seconds": round(elapsed, 3), "steps": reps,
+           "sample": f"{reps} full step(s) of the {wl.name} workload (write + decode of "
+                     f"all sequences and heads), fp64 C oracle with OpenMP, "
+                     f"{elapsed:.1f} s"}
+    # one step on one core takes about (all-core step time) x threads
+    step_1core_est = elapsed / max(reps, 1) * threads
+    if one_core_s > 0 and threads > 1 and step_1core_est > 2 * one_core_s:
+        out["value_1_core"] = None
+        out["note_1_core"] = f"skipped: one step would take about {step_1core_est:.0f} s on one core"
+    elif one_core_s > 0 and threads > 1:
+        # the same steps on one core, for a shorter sample
+        oracle.set_threads(1)
+        try:
+            kc1, vc1 = wl.k_cache.clone(), wl.v_cache.clone()
+            b1, r1, e1 = 0, 0, 0.0
+            while r1 < max_reps and e1 < one_core_s:
+                k = r1 % len(wl.steps)
+                st = wl.steps[k]
+                t0 = time.perf_counter()
+                oracle.write_kv(st.k_new, st.v_new, st.slot_mapping, kc1, vc1)
+                oracle.decode(st.q, kc1, vc1, st.block_tables, st.seq_lens, wl.scale)
+                e1 += time.perf_counter() - t0
+                b = step_bytes(wl, k, split_traffic=False)
+                b1 += b["decode"] + b["write"]
+                r1 += 1
+            out["value_1_core"] = b1 / e1 / 1e9
+            out["steps_1_core"] = r1
+        finally:
+            oracle.set_threads(threads)
+    if gpu_outs is not None:
+        out["max_abs_err_vs_gpu"] = err_abs
+        out["max_err_over_bf16_bound"] = round(err_ratio, 4)
+        out["steps_compared"] = len(checked)
+    return out
 
 
 def time_oracle_copy(args) -> dict:
@@ -330,8 +372,11 @@ def run_ours(args, rank, world, device):
     launches = sum(launches_per_step[it % nsteps_wl] for it in range(K))
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = time_oracle(wl, args.cpu_seconds)
+        cpu = time_oracle(wl, args.cpu_seconds, max_reps=100000, gpu_outs=outs,
+                          one_core_s=min(5.0, args.cpu_seconds / 2))
     b0 = bytes_[0]
+    q10, _, _, _, _, _, _, _, q90 = statistics.quantiles(dec_ms, n=10) if len(dec_ms) > 1 \
+        else [dec_ms[0]] * 9
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
@@ -349,6 +394,7 @@ def run_ours(args, rank, world, device):
                          f"per step vs {L2_BYTES / 2**20:.0f} MiB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "decode_tokens_per_s_per_layer": round(world * seqs / (total_ms / 1e3), 1),
         "bytes_per_step": {"unique_kv": b0["unique_kv"], "logical_kv": b0["logical_kv"],
                            "decode": b0["decode"], "write": b0["write"]},
@@ -358,6 +404,7 @@ def run_ours(args, rank, world, device):
                      "frac": round(dec_achieved / peak, 4),
                      "traffic": None if overrides(args) else measured_traffic(args.workload),
                      "decode_ms_median": round(statistics.median(dec_ms), 5),
+                     "decode_ms_p10": round(q10, 5), "decode_ms_p90": round(q90, 5),
                      "timed_launches": len(dec_ms),
                      "how": f"events around the pa_decode call on every {DEC_SAMPLE}th timed "
                             "step (launch on the caller's stream)"},
@@ -542,6 +589,7 @@ def run_copy(args, rank, world, device):
                    "l2": f"inputs larger than L2: {step_bytes_ / 2 / 2**20:.0f} MiB read per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "bytes_per_step": step_bytes_,
         "roofline": roof,
         "e2e": {"value": round(step_bytes_ / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",

@@ -47,7 +47,7 @@ __device__ __forceinline__ int32_t clamp_len(const Args& a, int32_t t) {
     const int64_t cap64 = (int64_t)a.max_blocks * a.block_size;
     const int32_t cap = (int32_t)min((int64_t)a.max_seq_len, cap64);
     if (t < 0 || t > cap) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(PA_DEVERR_SEQ_LEN);
+        if (threadIdx.x == 0) raise_error(PA_DEVERR_SEQ_LEN);
         t = t < 0 ? 0 : cap;
     }
     return t;
