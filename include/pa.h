@@ -29,6 +29,15 @@
  * lengths, q, out, workspace).  The library allocates no device memory and
  * keeps no per-call state; it caches one TMA descriptor pair per host thread.
  *
+ * Memory: caches and workspaces must be device (or managed) memory.  The
+ * per-call arguments marked "device or pinned" below -- queries, new K/V,
+ * slots, tables, lengths, query starts and outputs -- may instead be
+ * page-locked host memory: the kernels then read or write it directly over
+ * the host link (NVLink-C2C on Grace-Blackwell), with no staging copy.
+ * Pageable host memory, or a cache or workspace outside device memory, is
+ * refused with PA_ERR_INVALID_ARG (PA_ERR_WORKSPACE for the workspace)
+ * before anything is launched.
+ *
  * Errors: argument problems found on the host return a status and launch
  * nothing.  Problems only visible on the device (a needed block-table entry
  * outside [0, num_blocks), a sequence longer than its table or than
@@ -76,8 +85,8 @@ typedef struct {
 /*
  * pa_write_kv -- cache write through slot_mapping.
  *
- * k, v          device, [num_tokens][num_kv_heads][head_dim], cache dtype.
- * slot_mapping  device int64 [num_tokens]; token j goes to slot s =
+ * k, v          device or pinned, [num_tokens][num_kv_heads][head_dim], cache dtype.
+ * slot_mapping  device or pinned int64 [num_tokens]; token j goes to slot s =
  *               slot_mapping[j]: block s / B, row s % B, for every kv head.
  *               s < 0 means "skip this token".  Slots must be distinct within
  *               one call (two writers of one slot race).
@@ -97,12 +106,12 @@ pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
  * positions and the device block table give the slot mapping; §3: slot =
  * table[pos / B] * B + pos % B).
  *
- * seq_ids, positions  device int32 [num_tokens]; token j belongs to sequence
+ * seq_ids, positions  device or pinned int32 [num_tokens]; token j belongs to sequence
  *               seq_ids[j] at position positions[j].  A negative id or
  *               position means "skip"; an id >= num_seqs, a position past the
  *               table, or a table entry outside [0, num_blocks) is skipped and
  *               reported (PA_DEVERR_TABLE_ENTRY).
- * block_tables  device int32 [num_seqs][max_blocks_per_seq].
+ * block_tables  device or pinned int32 [num_seqs][max_blocks_per_seq].
  * Other arguments as pa_write_kv.
  */
 pa_status pa_write_kv_positions(const void* k, const void* v, const int32_t* seq_ids,
@@ -163,17 +172,17 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  * table[i][t / B] * B + t % B, and T_i = seq_lens[i].  T_i == 0 gives a zero
  * row.
  *
- * q              device [num_seqs][num_q_heads][head_dim], cache dtype.
- * block_tables   device int32 [num_seqs][max_blocks_per_seq]; entries at or
+ * q              device or pinned [num_seqs][num_q_heads][head_dim], cache dtype.
+ * block_tables   device or pinned int32 [num_seqs][max_blocks_per_seq]; entries at or
  *                beyond ceil(T_i / B) are never read (pad with -1).
- * seq_lens       device int32 [num_seqs].
+ * seq_lens       device or pinned int32 [num_seqs].
  * max_seq_len    host upper bound of seq_lens (sizes the grid; no device
  *                read-back).  Must satisfy max_seq_len <= max_blocks_per_seq*B.
  * scale          softmax scale (1/sqrt(head_dim) for standard attention).
  * partition_tokens  split-K partition (multiple of B), or 0 for automatic.
  *                Sequences longer than one partition are computed per
  *                partition and merged with a log-sum-exp reduction.
- * out            device [num_seqs][num_q_heads][head_dim], cache dtype,
+ * out            device or pinned [num_seqs][num_q_heads][head_dim], cache dtype,
  *                round-to-nearest-even from fp32.
  * workspace      device, >= pa_decode_workspace_bytes(...) bytes, 256-byte
  *                aligned; may be NULL when that size is 0.
@@ -202,14 +211,14 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * kv head floor(h / (Hq/Hkv)), keys read through the block table as in
  * pa_decode.  A decode row is a sequence with L_i = 1.
  *
- * q, out           device [total_q][num_q_heads][head_dim], cache dtype.
- * query_start_loc  device int32 [num_seqs + 1], non-decreasing, last = total_q.
+ * q, out           device or pinned [total_q][num_q_heads][head_dim], cache dtype.
+ * query_start_loc  device or pinned int32 [num_seqs + 1], non-decreasing, last = total_q.
  * max_q_len        host upper bound of L_i (sizes the grid).
  * Other arguments as pa_decode.  L_i > T_i is reported (PA_DEVERR_SEQ_LEN)
  * and that sequence's rows are left untouched.  bf16 with head_dim 64/128,
- * block_size 8 or a multiple of 16, and a group size dividing 128 runs on the
- * TMA + tcgen05 kernel (tensor-memory accumulators); other valid shapes
- * (head_dim <= 256) on a portable kernel.
+ * block_size 8 or a multiple of 16, a group size dividing 128 and scale >= 0
+ * runs on the TMA + tcgen05 kernel (tensor-memory accumulators); other valid
+ * shapes (head_dim <= 256) and scales on a portable kernel.
  */
 pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t total_q,
                      int32_t max_q_len, const void* k_cache, const void* v_cache,

@@ -116,6 +116,14 @@ def _dev(*ts: torch.Tensor) -> None:
             raise ValueError("tensors must be contiguous")
 
 
+def _dev_or_pinned(*ts: torch.Tensor) -> None:
+    for t in ts:
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError("tensors must be on a CUDA device or in page-locked host memory")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -130,8 +138,11 @@ def _check(status: int, where: str) -> None:
 # ---- public calls -------------------------------------------------------------
 
 def write_kv(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
-    """Scatter k, v [n_tok, Hkv, D] into the caches at slot_mapping [n_tok] (int64)."""
-    _dev(k, v, slot_mapping, k_cache, v_cache)
+    """Scatter k, v [n_tok, Hkv, D] into the caches at slot_mapping [n_tok] (int64).
+    k, v and slot_mapping may be page-locked host tensors: the kernel reads them
+    over the host link."""
+    _dev(k_cache, v_cache)
+    _dev_or_pinned(k, v, slot_mapping)
     if slot_mapping.dtype != torch.int64:
         raise ValueError("slot_mapping must be int64")
     if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
@@ -150,8 +161,10 @@ def write_kv(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
 def write_kv_positions(k, v, seq_ids, positions, block_tables, k_cache, v_cache,
                        stream=None) -> None:
     """Scatter k, v [n_tok, Hkv, D] to the slots of (seq_ids[j], positions[j])
-    through block_tables [N, max_blocks]; slots are computed on the device."""
-    _dev(k, v, seq_ids, positions, block_tables, k_cache, v_cache)
+    through block_tables [N, max_blocks]; slots are computed on the device.
+    Everything but the caches may be page-locked host memory."""
+    _dev(k_cache, v_cache)
+    _dev_or_pinned(k, v, seq_ids, positions, block_tables)
     for t in (seq_ids, positions, block_tables):
         if t.dtype != torch.int32:
             raise ValueError("seq_ids, positions and block_tables must be int32")
@@ -167,14 +180,6 @@ def write_kv_positions(k, v, seq_ids, positions, block_tables, k_cache, v_cache,
         block_tables.shape[0], block_tables.shape[1], _ptr(k_cache), _ptr(v_cache),
         ctypes.byref(desc), _stream(stream))
     _check(st, "pa_write_kv_positions")
-
-
-def _dev_or_pinned(*ts: torch.Tensor) -> None:
-    for t in ts:
-        if not (t.is_cuda or t.is_pinned()):
-            raise ValueError("tensors must be on a CUDA device or in page-locked host memory")
-        if not t.is_contiguous():
-            raise ValueError("tensors must be contiguous")
 
 
 def copy_blocks(src_k, src_v, dst_k, dst_v, pairs, stream=None) -> None:
@@ -219,9 +224,12 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int,
 
     ``max_seq_len`` is a host-side upper bound of ``seq_lens`` (no device
     read-back).  ``workspace`` (uint8, device) is allocated if not given and
-    split-K needs one.
+    split-K needs one.  q, block_tables, seq_lens and out may be page-locked
+    host tensors, read and written by the kernels over the host link; a
+    missing ``out`` is allocated on the caches' device.
     """
-    _dev(q, k_cache, v_cache, block_tables, seq_lens)
+    _dev(k_cache, v_cache)
+    _dev_or_pinned(q, block_tables, seq_lens)
     if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise ValueError("block_tables and seq_lens must be int32")
     desc = cache_desc(k_cache)
@@ -229,11 +237,13 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int,
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
-        out = torch.empty_like(q)
-    _dev(out)
+        out = torch.empty_like(q, device=k_cache.device)
+    _dev_or_pinned(out)
     need = decode_workspace_bytes(n, hq, max_seq_len, desc, partition_tokens)
     if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=k_cache.device)
+    if workspace is not None:
+        _dev(workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load_library().pa_decode(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
@@ -252,8 +262,11 @@ def prefill(q, query_start_loc, k_cache, v_cache, block_tables, seq_lens, max_q_
             max_seq_len: int, scale: float | None = None, out=None, stream=None):
     """Causal multi-query attention over the paged cache: sequence i's packed
     rows query_start_loc[i]..query_start_loc[i+1] are its last positions.
-    Returns out [total_q, Hq, D] in the cache dtype."""
-    _dev(q, query_start_loc, k_cache, v_cache, block_tables, seq_lens)
+    Returns out [total_q, Hq, D] in the cache dtype.  Everything but the
+    caches may be page-locked host memory (read and written over the host
+    link); a missing ``out`` is allocated on the caches' device."""
+    _dev(k_cache, v_cache)
+    _dev_or_pinned(q, query_start_loc, block_tables, seq_lens)
     for t in (query_start_loc, block_tables, seq_lens):
         if t.dtype != torch.int32:
             raise ValueError("query_start_loc, block_tables and seq_lens must be int32")
@@ -264,8 +277,8 @@ def prefill(q, query_start_loc, k_cache, v_cache, block_tables, seq_lens, max_q_
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
-        out = torch.empty_like(q)
-    _dev(out)
+        out = torch.empty_like(q, device=k_cache.device)
+    _dev_or_pinned(out)
     st = load_library().pa_prefill(
         _ptr(q), _ptr(query_start_loc), total, max_q_len, _ptr(k_cache), _ptr(v_cache),
         _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), seq_lens.numel(), max_seq_len,

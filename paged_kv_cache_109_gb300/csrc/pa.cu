@@ -159,6 +159,31 @@ const void* device_view(const void* p) {
     }
 }
 
+// Step arguments (queries, new K/V, slots, tables, lengths, outputs) may be
+// device memory or page-locked host memory; the kernels then read or write
+// the host memory directly over the host link (NVLink-C2C on Grace-Blackwell),
+// with no staging copy.  Replaces p by the address kernels use; false for
+// pageable host memory, which a kernel must never touch.
+template <typename T>
+bool map_step_arg(T*& p) {
+    if (!p) return true;
+    const void* view = device_view(p);
+    if (!view) return false;
+    p = static_cast<T*>(const_cast<void*>(view));
+    return true;
+}
+
+// Caches and workspaces: device (or managed) memory only.
+bool device_memory(const void* p) {
+    if (!p) return false;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
 // Launch the cache-write kernel with the widest vector the row size and the
 // pointers' alignment allow.
 template <typename SlotFn>
@@ -166,6 +191,9 @@ pa_status launch_write(const void* k, const void* v, SlotFn slot_of, int32_t num
                        void* k_cache, void* v_cache, const pa_cache_desc* cache,
                        cudaStream_t st) {
     if (!k || !v || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+    if (!map_step_arg(k) || !map_step_arg(v) || !device_memory(k_cache) ||
+        !device_memory(v_cache))
+        return PA_ERR_INVALID_ARG;
     const int32_t row = cache->head_dim * elem_bytes(cache);
     int vec = 16;
     while (vec > 2 && (row % vec || !aligned(k, vec) || !aligned(v, vec) ||
@@ -209,7 +237,8 @@ pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
                       const pa_cache_desc* cache, void* stream) {
     if (!desc_ok(cache) || num_tokens < 0) return PA_ERR_INVALID_ARG;
     if (num_tokens == 0) return PA_OK;
-    if (!slot_mapping || !aligned(slot_mapping, 8)) return PA_ERR_INVALID_ARG;
+    if (!slot_mapping || !aligned(slot_mapping, 8) || !map_step_arg(slot_mapping))
+        return PA_ERR_INVALID_ARG;
     return launch_write(k, v, SlotFromMapping{slot_mapping}, num_tokens, k_cache, v_cache, cache,
                         static_cast<cudaStream_t>(stream));
 }
@@ -224,6 +253,8 @@ pa_status pa_write_kv_positions(const void* k, const void* v, const int32_t* seq
     if (num_tokens == 0) return PA_OK;
     if (!seq_ids || !positions || !block_tables || !aligned(seq_ids, 4) ||
         !aligned(positions, 4) || !aligned(block_tables, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!map_step_arg(seq_ids) || !map_step_arg(positions) || !map_step_arg(block_tables))
         return PA_ERR_INVALID_ARG;
     SlotFromPosition fn{seq_ids, positions, block_tables, num_seqs, max_blocks_per_seq,
                         cache->block_size, cache->num_blocks};
@@ -324,10 +355,14 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     if (!aligned(q, elem_bytes(cache)) || !aligned(out, elem_bytes(cache)) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PA_ERR_INVALID_ARG;
+    if (!map_step_arg(q) || !map_step_arg(block_tables) || !map_step_arg(seq_lens) ||
+        !map_step_arg(out) || !device_memory(k_cache) || !device_memory(v_cache))
+        return PA_ERR_INVALID_ARG;
     const int32_t max_parts = num_parts(max_seq_len, part);
     if (max_parts > 65535) return PA_ERR_UNSUPPORTED;
     const size_t need = workspace_bytes(num_seqs, num_q_heads, max_seq_len, part, cache);
-    if (need > 0 && (!workspace || workspace_bytes_given < need || !aligned(workspace, 256)))
+    if (need > 0 && (!workspace || workspace_bytes_given < need || !aligned(workspace, 256) ||
+                     !device_memory(workspace)))
         return PA_ERR_WORKSPACE;
 
     DecodeArgs a;
@@ -405,6 +440,10 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     const int eb = elem_bytes(cache);
     if (!aligned(q, eb) || !aligned(out, eb) || !aligned(query_start_loc, 4) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!map_step_arg(q) || !map_step_arg(query_start_loc) || !map_step_arg(block_tables) ||
+        !map_step_arg(seq_lens) || !map_step_arg(out) || !device_memory(k_cache) ||
+        !device_memory(v_cache))
         return PA_ERR_INVALID_ARG;
     PrefillArgs a;
     a.q = q;

@@ -347,3 +347,54 @@ def test_continuous_batching_full_size_sampled(cuda_device):
             assert_close(got[pairs[:, 0], pairs[:, 1]], ref[pairs[:, 0], pairs[:, 1]],
                          BF16_ATOL, BF16_RTOL, f"cb step {k}")
     assert pa.last_device_error() == 0
+
+
+def test_pinned_host_step_arguments(cuda_device):
+    """q, tables, lengths and out in page-locked host memory (read and written
+    by the kernel over the host link) give the same bits as device tensors."""
+    hq, hkv, d, bs = 32, 8, 128, 16
+    g = torch.Generator().manual_seed(21)
+    lens = [700, 33, 1500, 1]
+    need = [-(-t // bs) for t in lens]
+    nb = sum(need) + 4
+    perm = torch.randperm(nb, generator=g).tolist()
+    width, pos, rows = max(need), 0, []
+    for k in need:
+        rows.append(perm[pos:pos + k] + [-1] * (width - k))
+        pos += k
+    bt = torch.tensor(rows, dtype=torch.int32)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    kc = torch.randn(nb, hkv, bs, d, generator=g).to(torch.bfloat16).to(cuda_device)
+    vc = torch.randn(nb, hkv, bs, d, generator=g).to(torch.bfloat16).to(cuda_device)
+    q = torch.randn(len(lens), hq, d, generator=g).to(torch.bfloat16)
+    scale = 1 / math.sqrt(d)
+    ref = pa.decode(q.to(cuda_device), kc, vc, bt.to(cuda_device), sl.to(cuda_device), 1500,
+                    scale, partition_tokens=256).cpu()
+    out_h = torch.empty_like(q).pin_memory()
+    pa.decode(q.pin_memory(), kc, vc, bt.pin_memory(), sl.pin_memory(), 1500, scale,
+              out=out_h, partition_tokens=256)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, ref)
+    assert pa.last_device_error() == 0
+
+
+def test_pageable_or_host_cache_arguments_are_refused(cuda_device):
+    import ctypes
+    kc, vc, bt, sl, q = (t.to(cuda_device) for t in (
+        torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16), torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16),
+        torch.zeros(1, 4, dtype=torch.int32), torch.ones(1, dtype=torch.int32),
+        torch.zeros(1, 4, 64, dtype=torch.bfloat16)))
+    lib = pa.load_library()
+    desc = pa.cache_desc(kc)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream().cuda_stream
+    pageable_q = torch.zeros(1, 4, 64, dtype=torch.bfloat16)
+    st = lib.pa_decode(pageable_q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), 4,
+                       sl.data_ptr(), 1, 16, 4, ctypes.c_float(0.1), 0, out.data_ptr(), None, 0,
+                       ctypes.byref(desc), stream)
+    assert st == pa.PA_ERR_INVALID_ARG
+    pinned_cache = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16).pin_memory()
+    st = lib.pa_decode(q.data_ptr(), pinned_cache.data_ptr(), vc.data_ptr(), bt.data_ptr(), 4,
+                       sl.data_ptr(), 1, 16, 4, ctypes.c_float(0.1), 0, out.data_ptr(), None, 0,
+                       ctypes.byref(desc), stream)
+    assert st == pa.PA_ERR_INVALID_ARG

@@ -180,3 +180,17 @@ def test_bad_table_entry_is_reported(cuda_device, hq, hkv, d):
     out = run(cuda_device, q, qs, kc, vc, bad, sl, 1 / math.sqrt(d))
     assert pa.last_device_error() & pa.DEVERR_TABLE_ENTRY
     assert_close(out[100:].double().numpy(), ref, BF16_ATOL, BF16_RTOL, "other sequence")
+
+
+def test_prefill_from_pinned_host_arguments(cuda_device):
+    """q, query starts, tables, lengths and out in page-locked host memory give
+    the same bits as device tensors."""
+    q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (300, 90), (120, 90), seed=10)
+    scale = 1 / math.sqrt(128)
+    ref = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
+    kd, vd = kc.to(cuda_device), vc.to(cuda_device)
+    out_h = torch.empty_like(q).pin_memory()
+    pa.prefill(q.pin_memory(), qs.pin_memory(), kd, vd, bt.pin_memory(), sl.pin_memory(), 120,
+               300, scale, out=out_h)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, ref)

@@ -92,3 +92,31 @@ def test_write_continuous_batching_full_step(cuda_device):
     assert torch.equal(d.k_cache, hk)
     del hk
     assert torch.equal(d.v_cache, h.v_cache.to(cuda_device))
+
+
+@pytest.mark.parametrize("positions", [False, True])
+def test_write_from_pinned_host_arguments(cuda_device, positions):
+    """New K/V, slots (or ids, positions and tables) in page-locked host memory,
+    read by the kernel over the host link: the caches match the oracle bit for bit."""
+    nb, hkv, bs, d = 64, 8, 16, 128
+    g = torch.Generator().manual_seed(31)
+    n_tok = 40
+    tables = torch.randperm(nb, generator=g)[:60].view(6, 10).int()
+    seq_ids = torch.randint(0, 6, (n_tok,), generator=g, dtype=torch.int32)
+    pos = torch.randperm(10 * bs, generator=g)[:n_tok].to(torch.int32)
+    slots = torch.from_numpy(oracle.slots_from_positions(seq_ids, pos, tables, bs))
+    k = torch.randn(n_tok, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(n_tok, hkv, d, generator=g).to(torch.bfloat16)
+    kc = torch.randn(nb, hkv, bs, d, generator=g).to(torch.bfloat16)
+    vc = torch.randn(nb, hkv, bs, d, generator=g).to(torch.bfloat16)
+    kh, vh = kc.clone(), vc.clone()
+    oracle.write_kv(k, v, slots, kh, vh)
+    kd, vd = kc.to(cuda_device), vc.to(cuda_device)
+    if positions:
+        pa.write_kv_positions(k.pin_memory(), v.pin_memory(), seq_ids.pin_memory(),
+                              pos.pin_memory(), tables.pin_memory(), kd, vd)
+    else:
+        pa.write_kv(k.pin_memory(), v.pin_memory(), slots.pin_memory(), kd, vd)
+    torch.cuda.synchronize()
+    assert torch.equal(kd.cpu(), kh) and torch.equal(vd.cpu(), vh)
+    assert pa.last_device_error() == 0
