@@ -398,3 +398,40 @@ def test_pageable_or_host_cache_arguments_are_refused(cuda_device):
                        sl.data_ptr(), 1, 16, 4, ctypes.c_float(0.1), 0, out.data_ptr(), None, 0,
                        ctypes.byref(desc), stream)
     assert st == pa.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("part", [256, 64])
+def test_repeated_calls_on_one_workspace(cuda_device, part):
+    """Split-K into 16 and 63 partitions: repeated calls on one workspace give
+    the same bits, and the merged output matches the oracle."""
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (3000, 1, 777, 4000, 2048), seed=11)
+    n, hq, maxlen = 5, 32, 4000
+    need = pa.decode_workspace_bytes(n, hq, maxlen, kc, part)
+    ws = torch.empty(need, dtype=torch.uint8, device=cuda_device)
+    args = (q.to(cuda_device), kc.to(cuda_device), vc.to(cuda_device), bt.to(cuda_device),
+            sl.to(cuda_device), maxlen, 1 / math.sqrt(128))
+    first = pa.decode(*args, workspace=ws, partition_tokens=part).clone()
+    for _ in range(3):
+        again = pa.decode(*args, workspace=ws, partition_tokens=part)
+        assert torch.equal(again, first)
+    ref = oracle.decode(q, kc, vc, bt, sl, 1 / math.sqrt(128))
+    assert_close(first.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, "merged")
+    assert pa.last_device_error() == 0
+
+
+def test_stale_workspace_contents_do_not_matter(cuda_device):
+    """The workspace needs no initialisation: one full of 0xFF, then the same
+    buffer reused by a call of another shape, both give correct outputs."""
+    q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (3000, 2048, 900), seed=12)
+    need = pa.decode_workspace_bytes(3, 32, 3000, kc, 256)
+    ws = torch.full((need * 2,), 0xFF, dtype=torch.uint8, device=cuda_device)
+    scale = 1 / math.sqrt(128)
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    out = pa.decode(q.to(cuda_device), kc.to(cuda_device), vc.to(cuda_device), bt.to(cuda_device),
+                    sl.to(cuda_device), 3000, scale, workspace=ws, partition_tokens=256)
+    assert_close(out.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, "0xFF workspace")
+    out2 = pa.decode(q[:2].to(cuda_device), kc.to(cuda_device), vc.to(cuda_device),
+                     bt[:2].to(cuda_device), sl[:2].to(cuda_device), 3000, scale, workspace=ws,
+                     partition_tokens=512)
+    assert_close(out2.cpu().double().numpy(), ref[:2], BF16_ATOL, BF16_RTOL, "reused workspace")
+    assert pa.last_device_error() == 0
