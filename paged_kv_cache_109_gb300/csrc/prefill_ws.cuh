@@ -21,22 +21,22 @@
 //                O_t += P_t V     M128 x N D, A = P_t from tensor memory
 //
 // Tensor memory per tile: S_t (KEYS fp32 columns) and O_t (D columns).  The
-// softmax writes P_t (bf16 pairs) over the first KEYS/2 columns of S_t once
-// it has S_t in registers.  Per key block kb the MMA warp issues, for t = 0,
-// 1: O_t += P_t(kb-1) V(kb-1) as soon as softmax t publishes P_t(kb-1), then
-// S_t(kb) into the same columns (tcgen05 MMAs of one thread run in issue
-// order, so P_t is read before it is overwritten).  Each softmax warpgroup
-// overlaps the other tile's tensor-core work, and with P off shared memory
-// the K/V ring holds enough blocks to hide the copies' latency.
+// softmax writes P_t (bf16 pairs) over the first KEYS/2 columns of S_t, one
+// 64-key half at a time, and publishes each half.  Per key block kb the MMA
+// warp issues, for t = 0, 1: O_t += P_t(kb-1) V(kb-1) for keys 0-63 as soon
+// as that half is published (while the softmax computes keys 64-127), then
+// for keys 64-127, then S_t(kb) into the same columns (tcgen05 MMAs of one
+// thread run in issue order, so P_t is read before it is overwritten).  Each
+// softmax warpgroup overlaps the other tile's tensor-core work, and with P
+// off shared memory the K/V ring holds enough blocks to hide the copies'
+// latency.
 //
-// Softmax per row and block: load S (tcgen05.ld), mask keys past the row's
-// position (diagonal blocks only), p = 2^(s c - m) with c = scale log2(e) and
-// a lazily moved reference maximum m (it moves only when the block maximum
-// exceeds it by more than 8, so O is rescaled rarely, p <= 2^8 and O / l does
-// not depend on m), accumulate l, store P.  Since m rarely moves, p is
-// computed against the current m in the same pass that finds the block
-// maximum, and recomputed only for blocks that raise it.  O is divided by l
-// at the end.
+// Softmax per row and 64-key half: load S (tcgen05.ld), mask keys past the
+// row's position (diagonal blocks only), take the half's maximum, p = 2^(s c
+// - m) with c = scale log2(e) and a lazily moved reference maximum m (it
+// moves only when the maximum exceeds it by more than 8, so O is rescaled
+// rarely, p <= 2^8 and O / l does not depend on m), accumulate l, store P.
+// O is divided by l at the end.
 //
 // Synchronisation is by mbarriers only; every wait is bounded, and a timeout
 // raises PA_DEVERR_TIMEOUT and ends the role's work (the others then time
@@ -69,14 +69,15 @@ struct PrefillWsCfg {
     static constexpr int kSmemMax = 232448;               // dynamic shared memory per CTA
     static constexpr int kSlots = (kSmemMax - 2048 - kSlotOff) / kItem;
     static constexpr int kBarOff = kSlotOff + kSlots * kItem;
-    static constexpr int kBars = 2 * kSlots + 7;          // K/V full, K/V empty, S, P, O, final
+    // K/V full, K/V empty; per tile S full, P half 0, P full, O half 0, O done; final
+    static constexpr int kBars = 2 * kSlots + 11;
     static constexpr int kTslotOff = kBarOff + 8 * kBars;
     static size_t smem_bytes() { return 1024 + kTslotOff + 16; }
     static constexpr uint32_t kTmemCols = 512;            // per tile: S (and P) at +0, O at +128
     static constexpr uint32_t kTileCols = 256;
     static constexpr uint32_t kOCol = 128;
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(KEYS == 64 || KEYS == 128, "key block");
+    static_assert(KEYS == 128, "key block: two 64-key halves");
     static_assert(kSlots >= 4, "ring");
 };
 
@@ -95,7 +96,9 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
     auto s_full = [&](int32_t t) { return bar0 + 8u * (2 * C::kSlots + t); };
     auto p_full = [&](int32_t t) { return bar0 + 8u * (2 * C::kSlots + 2 + t); };
     auto o_done = [&](int32_t t) { return bar0 + 8u * (2 * C::kSlots + 4 + t); };
-    const uint32_t bar_fin = bar0 + 8u * (2 * C::kSlots + 6);
+    auto p_half = [&](int32_t t) { return bar0 + 8u * (2 * C::kSlots + 6 + t); };
+    auto o_half = [&](int32_t t) { return bar0 + 8u * (2 * C::kSlots + 8 + t); };
+    const uint32_t bar_fin = bar0 + 8u * (2 * C::kSlots + 10);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::kTslotOff);
 
     const int32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -108,6 +111,8 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             mbar_init(s_full(t), 1);
             mbar_init(p_full(t), 4);                      // one arrival per softmax warp
             mbar_init(o_done(t), 1);
+            mbar_init(p_half(t), 4);
+            mbar_init(o_half(t), 1);
         }
         mbar_init(bar_fin, 1);
         mbar_fence_init();
@@ -290,19 +295,27 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             for (int32_t t = 0; t < ntiles && ok; ++t) {
                 const uint32_t s_t = tmem + t * C::kTileCols;
                 if (kb > 0) {
-                    // O_t += P_t(kb - 1) V(kb - 1); P: 16 keys = 8 columns per step
-                    if (!warp_wait(p_full(t), (kb - 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (leader) {
+                    // O_t += P_t(kb - 1) V(kb - 1) in two halves: keys 0-63 as soon
+                    // as softmax t publishes them, keys 64-127 after; P: 16 keys
+                    // = 8 columns per step
 #pragma unroll
-                        for (int32_t k = 0; k < C::kKeys / 16; ++k)
-                            umma_bf16_ts(s_t + C::kOCol, s_t + k * 8, vdesc + (uint64_t)(k * 128),
-                                         kIdO, (kb > 1 || k > 0) ? 1u : 0u);
-                        umma_commit(o_done(t));
+                    for (int32_t hf = 0; hf < 2; ++hf) {
+                        if (!warp_wait(hf ? p_full(t) : p_half(t), (kb - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (leader) {
+#pragma unroll
+                            for (int32_t k = hf * 4; k < hf * 4 + 4; ++k)
+                                umma_bf16_ts(s_t + C::kOCol, s_t + k * 8,
+                                             vdesc + (uint64_t)(k * 128), kIdO,
+                                             (kb > 1 || k > 0) ? 1u : 0u);
+                            umma_commit(hf ? o_done(t) : o_half(t));
+                        }
+                        __syncwarp();
                     }
+                    if (!ok) break;
                 }
                 if (kb < nb && leader) {
                     // S_t(kb) = Q_t K(kb)^T over the columns P_t(kb - 1) occupied
@@ -343,15 +356,15 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int32_t key0 = kb * C::kKeys;
             const bool full = key0 + C::kKeys - 1 <= pos;
             // Each 64-key half of S: load it, take its maximum, move this row's
-            // reference m_ref if that maximum exceeds it by more than 8, then
-            // p = 2^(s c - m_ref) (packed fp32 FMA and add) and P -> tensor
-            // memory over the first KEYS/2 columns of S_t (half hh of P lands on
-            // columns of keys already read; P_t(kb - 1) V(kb - 1) ran before
-            // S_t(kb)).  A reference raised in a later half rescales the halves
-            // of P already stored (their values only shrink).
+            // reference m_ref if that maximum exceeds it by more than 8, p =
+            // 2^(s c - m_ref) (packed fp32 FMA and add), P -> tensor memory over
+            // the first 64 columns of S_t (half hh of P lands on columns of keys
+            // already read; P_t(kb - 1) V(kb - 1) ran before S_t(kb)), rescale O
+            // if the reference moved (once the P V it holds has finished), and
+            // publish the half: the MMA warp starts O += P V on keys 0-63 while
+            // keys 64-127 are still being computed.
             const float2 c2 = make_float2(c, c);
-            float alpha = 1.f;                            // this block's rescale of O
-            auto half = [&](int32_t hh, auto masked) {
+            auto half = [&](int32_t hh, auto masked) -> bool {
                 constexpr bool kMasked = decltype(masked)::value;
                 uint32_t sr[2][32];
                 tmem_ld32_async(s_tm + hh * 64, sr[0]);
@@ -376,26 +389,7 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const bool up = mx > m_ref + 8.f;
                 const float a = up ? ex2_approx(m_ref - mx) : 1.f;   // 0 when m_ref = -inf
                 if (up) m_ref = mx;
-                alpha *= a;
                 l *= a;
-                if (hh > 0 && __any_sync(0xffffffffu, up)) {
-                    // rescale the P already stored (bf16 pairs) by this row's factor
-                    tmem_wait_st();
-#pragma unroll
-                    for (int32_t h0 = 0; h0 < hh; ++h0) {
-                        uint32_t pr[32];
-                        tmem_ld32_async(s_tm + h0 * 32, pr);
-                        tmem_wait_ld();
-                        tmem_regs_ready(pr);
-#pragma unroll
-                        for (int32_t j = 0; j < 32; ++j) {
-                            const float2 f = __bfloat1622float2(
-                                *reinterpret_cast<const __nv_bfloat162*>(&pr[j]));
-                            pr[j] = pack_bf16x2(f.x * a, f.y * a);
-                        }
-                        tmem_st32_async(s_tm + h0 * 32, pr);
-                    }
-                }
                 const float ref = m_ref == -INFINITY ? 0.f : m_ref;
                 const float2 nm2 = make_float2(-ref, -ref);
                 float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -416,40 +410,36 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 tmem_st32_async(s_tm + hh * 32, pk);
                 l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
-            };
-            // the version is chosen per warp (the tcgen05 accesses inside are
-            // warp-collective): unmasked only when every row sees the whole block
-            const bool warp_full = __all_sync(0xffffffffu, full) != 0;
-#pragma unroll
-            for (int32_t hh = 0; hh < C::kKeys / 64; ++hh) {
-                if (warp_full)
-                    half(hh, std::false_type{});
-                else
-                    half(hh, std::true_type{});
-            }
-            const bool raise = alpha != 1.f;
-            // O may be rescaled once the previous P V has finished
-            if (kb > 0) {
-                if (!warp_wait(o_done(w), (kb - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, raise)) {
+                // O holds the P V of every earlier half: rescale it once that
+                // has finished, before this half is published (nothing to
+                // rescale before the first half)
+                if ((kb > 0 || hh > 0) && __any_sync(0xffffffffu, up)) {
+                    const bool waited = hh == 0 ? warp_wait(o_done(w), (kb - 1) & 1)
+                                                : warp_wait(o_half(w), kb & 1);
+                    if (!waited) return false;
+                    tc_fence_after();
 #pragma unroll
                     for (int32_t cc = 0; cc < D / 32; ++cc) {
                         float ov[32];
                         tmem_ld32(o_tm + cc * 32, ov);
 #pragma unroll
-                        for (int32_t j = 0; j < 32; ++j) ov[j] *= alpha;
+                        for (int32_t j = 0; j < 32; ++j) ov[j] *= a;
                         tmem_st32(o_tm + cc * 32, ov);
                     }
                 }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(w));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hh == 0 ? p_half(w) : p_full(w));
+                return true;
+            };
+            // the version is chosen per warp (the tcgen05 accesses inside are
+            // warp-collective): unmasked only when every row sees the whole block
+            const bool warp_full = __all_sync(0xffffffffu, full) != 0;
+#pragma unroll
+            for (int32_t hh = 0; hh < 2 && ok; ++hh)
+                ok = warp_full ? half(hh, std::false_type{}) : half(hh, std::true_type{});
+            if (!ok) break;
         }
         if (ok) ok = warp_wait(o_done(w), (nb - 1) & 1);
         if (ok) {
