@@ -364,81 +364,92 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // publish the half: the MMA warp starts O += P V on keys 0-63 while
             // keys 64-127 are still being computed.
             const float2 c2 = make_float2(c, c);
-            auto half = [&](int32_t hh, auto masked) -> bool {
+            auto block = [&](auto masked) -> bool {
                 constexpr bool kMasked = decltype(masked)::value;
                 uint32_t sr[2][32];
-                tmem_ld32_async(s_tm + hh * 64, sr[0]);
-                tmem_ld32_async(s_tm + hh * 64 + 32, sr[1]);
+                tmem_ld32_async(s_tm, sr[0]);
+                tmem_ld32_async(s_tm + 32, sr[1]);
                 tmem_wait_ld();
                 tmem_regs_ready(sr[0]);
                 tmem_regs_ready(sr[1]);
-                if constexpr (kMasked) {
 #pragma unroll
-                    for (int32_t j = 0; j < 64; ++j)
-                        if (key0 + hh * 64 + j > pos) sr[j >> 5][j & 31] = __float_as_uint(-INFINITY);
-                }
-                float mp[4];
+                for (int32_t hh = 0; hh < 2; ++hh) {
+                    if constexpr (kMasked) {
 #pragma unroll
-                for (int32_t u = 0; u < 4; ++u) mp[u] = -INFINITY;
-#pragma unroll
-                for (int32_t jj = 0; jj < 32; ++jj)
-                    mp[jj & 3] = fmax3(mp[jj & 3], __uint_as_float(sr[(2 * jj) >> 5][(2 * jj) & 31]),
-                                       __uint_as_float(sr[(2 * jj + 1) >> 5][(2 * jj + 1) & 31]));
-                const float mraw = fmaxf(fmax3(mp[0], mp[1], mp[2]), mp[3]);
-                const float mx = mraw == -INFINITY ? -INFINITY : mraw * c;
-                const bool up = mx > m_ref + 8.f;
-                const float a = up ? ex2_approx(m_ref - mx) : 1.f;   // 0 when m_ref = -inf
-                if (up) m_ref = mx;
-                l *= a;
-                const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-                const float2 nm2 = make_float2(-ref, -ref);
-                float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                uint32_t pk[32];
-#pragma unroll
-                for (int32_t jj = 0; jj < 32; ++jj) {
-                    const int32_t j = 2 * jj;
-                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[j >> 5][j & 31]),
-                                                            __uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31])),
-                                                c2, nm2);
-                    float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    if constexpr (kMasked) {                 // c = 0: -inf * 0 is NaN
-                        pp.x = key0 + hh * 64 + j <= pos ? pp.x : 0.f;
-                        pp.y = key0 + hh * 64 + j + 1 <= pos ? pp.y : 0.f;
+                        for (int32_t j = 0; j < 64; ++j)
+                            if (key0 + hh * 64 + j > pos) sr[j >> 5][j & 31] = __float_as_uint(-INFINITY);
                     }
-                    rs[jj & 1] = __fadd2_rn(rs[jj & 1], pp);
-                    pk[jj] = pack_bf16x2(pp.x, pp.y);
-                }
-                tmem_st32_async(s_tm + hh * 32, pk);
-                l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
-                // O holds the P V of every earlier half: rescale it once that
-                // has finished, before this half is published (nothing to
-                // rescale before the first half)
-                if ((kb > 0 || hh > 0) && __any_sync(0xffffffffu, up)) {
-                    const bool waited = hh == 0 ? warp_wait(o_done(w), (kb - 1) & 1)
-                                                : warp_wait(o_half(w), kb & 1);
-                    if (!waited) return false;
-                    tc_fence_after();
+                    float mp[4];
 #pragma unroll
-                    for (int32_t cc = 0; cc < D / 32; ++cc) {
-                        float ov[32];
-                        tmem_ld32(o_tm + cc * 32, ov);
+                    for (int32_t u = 0; u < 4; ++u) mp[u] = -INFINITY;
 #pragma unroll
-                        for (int32_t j = 0; j < 32; ++j) ov[j] *= a;
-                        tmem_st32(o_tm + cc * 32, ov);
+                    for (int32_t jj = 0; jj < 32; ++jj)
+                        mp[jj & 3] = fmax3(mp[jj & 3], __uint_as_float(sr[(2 * jj) >> 5][(2 * jj) & 31]),
+                                           __uint_as_float(sr[(2 * jj + 1) >> 5][(2 * jj + 1) & 31]));
+                    const float mraw = fmaxf(fmax3(mp[0], mp[1], mp[2]), mp[3]);
+                    const float mx = mraw == -INFINITY ? -INFINITY : mraw * c;
+                    const bool up = mx > m_ref + 8.f;
+                    const float a = up ? ex2_approx(m_ref - mx) : 1.f;   // 0 when m_ref = -inf
+                    if (up) m_ref = mx;
+                    l *= a;
+                    const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+                    const float2 nm2 = make_float2(-ref, -ref);
+                    float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int32_t jj = 0; jj < 32; ++jj) {
+                        const int32_t j = 2 * jj;
+                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[j >> 5][j & 31]),
+                                                                __uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31])),
+                                                    c2, nm2);
+                        float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        if constexpr (kMasked) {             // c = 0: -inf * 0 is NaN
+                            pp.x = key0 + hh * 64 + j <= pos ? pp.x : 0.f;
+                            pp.y = key0 + hh * 64 + j + 1 <= pos ? pp.y : 0.f;
+                        }
+                        rs[jj & 1] = __fadd2_rn(rs[jj & 1], pp);
+                        pk[jj] = pack_bf16x2(pp.x, pp.y);
+                    }
+                    tmem_st32_async(s_tm + hh * 32, pk);
+                    l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
+                    // the second half's scores load while this half is published
+                    if (hh == 0) {
+                        tmem_ld32_async(s_tm + 64, sr[0]);
+                        tmem_ld32_async(s_tm + 96, sr[1]);
+                    }
+                    // O holds the P V of every earlier half: rescale it once that
+                    // has finished, before this half is published (nothing to
+                    // rescale before the first half)
+                    if ((kb > 0 || hh > 0) && __any_sync(0xffffffffu, up)) {
+                        const bool waited = hh == 0 ? warp_wait(o_done(w), (kb - 1) & 1)
+                                                    : warp_wait(o_half(w), kb & 1);
+                        if (!waited) return false;
+                        tc_fence_after();
+#pragma unroll
+                        for (int32_t cc = 0; cc < D / 32; ++cc) {
+                            float ov[32];
+                            tmem_ld32(o_tm + cc * 32, ov);
+#pragma unroll
+                            for (int32_t j = 0; j < 32; ++j) ov[j] *= a;
+                            tmem_st32(o_tm + cc * 32, ov);
+                        }
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(hh == 0 ? p_half(w) : p_full(w));
+                    if (hh == 0) {
+                        tmem_wait_ld();
+                        tmem_regs_ready(sr[0]);
+                        tmem_regs_ready(sr[1]);
                     }
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(hh == 0 ? p_half(w) : p_full(w));
                 return true;
             };
             // the version is chosen per warp (the tcgen05 accesses inside are
             // warp-collective): unmasked only when every row sees the whole block
             const bool warp_full = __all_sync(0xffffffffu, full) != 0;
-#pragma unroll
-            for (int32_t hh = 0; hh < 2 && ok; ++hh)
-                ok = warp_full ? half(hh, std::false_type{}) : half(hh, std::true_type{});
+            ok = warp_full ? block(std::false_type{}) : block(std::true_type{});
             if (!ok) break;
         }
         if (ok) ok = warp_wait(o_done(w), (nb - 1) & 1);
