@@ -194,3 +194,39 @@ def test_prefill_from_pinned_host_arguments(cuda_device):
                300, scale, out=out_h)
     torch.cuda.synchronize()
     assert torch.equal(out_h, ref)
+
+
+@pytest.mark.slow
+def test_prefill_workload_full_size_sampled(cuda_device):
+    """The chunked-prefill workload at full size (8 x 2048-token chunks over
+    histories up to 4096 tokens), in the configuration the bench times:
+    48 sampled (row, head) outputs against the oracle.  Each sampled row r of
+    sequence i at position p is the single-query attention of q[r] over the
+    keys 0..p, computed by the oracle as a sequence of length p + 1."""
+    wl = workloads.prefill()
+    st = wl.steps[0]
+    kd, vd = wl.k_cache.to(cuda_device), wl.v_cache.to(cuda_device)
+    pa.write_kv(st.k_new.to(cuda_device), st.v_new.to(cuda_device),
+                st.slot_mapping.to(cuda_device), kd, vd)
+    qs = st.query_start
+    max_q = int((qs[1:] - qs[:-1]).max())
+    out = pa.prefill(st.q.to(cuda_device), qs.to(cuda_device), kd, vd,
+                     st.block_tables.to(cuda_device), st.seq_lens.to(cuda_device), max_q,
+                     int(st.seq_lens.max()), wl.scale).cpu()
+    assert pa.last_device_error() == 0
+    assert torch.isfinite(out.float()).all()
+    del kd, vd
+    oracle.write_kv(st.k_new, st.v_new, st.slot_mapping, wl.k_cache, wl.v_cache)
+    rng = np.random.default_rng(13)
+    rows = rng.integers(0, int(qs[-1]), size=48)
+    heads = rng.integers(0, wl.num_q_heads, size=48)
+    seq = np.searchsorted(qs.numpy(), rows, side="right") - 1
+    T, L = st.seq_lens.numpy()[seq], (qs[1:] - qs[:-1]).numpy()[seq]
+    pos = T - L + (rows - qs.numpy()[seq])
+    q1 = st.q[torch.from_numpy(rows)]
+    bt1 = st.block_tables[torch.from_numpy(seq)]
+    sl1 = torch.from_numpy((pos + 1).astype(np.int32))
+    pairs = np.stack([np.arange(48), heads], axis=1)
+    ref = oracle.decode(q1, wl.k_cache, wl.v_cache, bt1, sl1, wl.scale, pairs=pairs)
+    got = out[torch.from_numpy(rows), torch.from_numpy(heads)].double().numpy()
+    assert_close(got, ref[np.arange(48), heads], BF16_ATOL, BF16_RTOL, "prefill full size")
