@@ -389,7 +389,8 @@ def run_ours(args, rank, world, device):
                    "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
                    "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                    "block_size": wl.block_size, "max_seq_len": max(maxlens),
-                   "partition_tokens": b0["partition"],
+                   "partition_tokens": b0["partition"], "seed": wl.seed,
+                   "block_utilization": wl.stats.get("block_utilization"),
                    "l2": f"inputs larger than L2: {b0['unique_kv'] / 2**20:.0f} MiB of K/V "
                          f"per step vs {L2_BYTES / 2**20:.0f} MiB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
