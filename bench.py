@@ -192,6 +192,27 @@ def measured_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# ---- ranks (one process per GPU; replicas) -----------------------------------
+
+def rank_barrier() -> None:
+    """All ranks meet here (no-op for a single process)."""
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks (the slowest rank's timed region); x with
+    one process.  ``device`` holds the reduction buffer: the GPU under NCCL,
+    the CPU under gloo."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    if torch.distributed.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---- CPU oracle (reference arm and cpu_baseline) ----------------------------------
 
 def time_oracle(wl, budget_s: float, max_reps: int = 50, gpu_outs=None,
@@ -329,8 +350,7 @@ def run_ours(args, rank, world, device):
     sampled = list(range(0, K, DEC_SAMPLE))
     dec_ev = {it: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for it in sampled}
-    if world > 1:
-        torch.distributed.barrier()
+    rank_barrier()
     torch.cuda.synchronize(device)
     with ClockSampler(device.index or 0) as clocks:
         start = torch.cuda.Event(enable_timing=True)
@@ -340,13 +360,8 @@ def run_ours(args, rank, world, device):
             step(it % nsteps_wl, dec_ev.get(it))
         end.record(stream)
         torch.cuda.synchronize(device)
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    rank_barrier()
+    total_ms = max_over_ranks(start.elapsed_time(end), device)
     dec_ms = [dec_ev[it][0].elapsed_time(dec_ev[it][1]) for it in sampled]
     step_bytes_sum = sum(bytes_[it % nsteps_wl]["decode"] + bytes_[it % nsteps_wl]["write"]
                          for it in range(K))
@@ -360,7 +375,7 @@ def run_ours(args, rank, world, device):
         raise RuntimeError(f"device error flag {err} raised in the timed region")
 
     # end to end: host buffers, H2D of the step inputs and D2H of the output
-    e2e = run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_)
+    e2e = run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, world)
 
     launches_per_step = []
     for k in range(nsteps_wl):
@@ -459,6 +474,8 @@ def run_prefill(args, rank, world, device):
     sampled = list(range(0, K, DEC_SAMPLE))
     evs = {it: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for it in sampled}
+    rank_barrier()
+    torch.cuda.synchronize(device)
     with ClockSampler(device.index or 0) as clocks:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
@@ -466,7 +483,8 @@ def run_prefill(args, rank, world, device):
             step(evs.get(it))
         end.record(stream)
         torch.cuda.synchronize(device)
-    total_ms = start.elapsed_time(end)
+    rank_barrier()
+    total_ms = max_over_ranks(start.elapsed_time(end), device)
     if pa.last_device_error() != 0:
         raise RuntimeError("device error flag raised in the timed region")
     pre_ms = [evs[it][0].elapsed_time(evs[it][1]) for it in sampled]
@@ -543,6 +561,8 @@ def run_copy(args, rank, world, device):
     sampled = list(range(0, K, DEC_SAMPLE))
     evs = {it: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for it in sampled}
+    rank_barrier()
+    torch.cuda.synchronize(device)
     with ClockSampler(device.index or 0) as clocks:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
@@ -550,7 +570,8 @@ def run_copy(args, rank, world, device):
             step(evs.get(it))
         end.record(stream)
         torch.cuda.synchronize(device)
-    total_ms = start.elapsed_time(end)
+    rank_barrier()
+    total_ms = max_over_ranks(start.elapsed_time(end), device)
     if pa.last_device_error() != 0:
         raise RuntimeError("device error flag raised in the timed region")
     call_ms = [evs[it][0].elapsed_time(evs[it][1]) for it in sampled]
@@ -571,6 +592,8 @@ def run_copy(args, rank, world, device):
     probe = torch.empty(calls[0][2][0].shape, dtype=calls[0][2].dtype).pin_memory()
     s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     K2 = max(1, min(K, 200))
+    torch.cuda.synchronize(device)
+    rank_barrier()
     s2.record(stream)
     for _ in range(K2):
         for c, hp, dp in zip(calls, host_pairs, dev_pairs):
@@ -579,7 +602,8 @@ def run_copy(args, rank, world, device):
         probe.copy_(calls[-1][2][0], non_blocking=True)
     e2.record(stream)
     torch.cuda.synchronize(device)
-    e2e_ms = s2.elapsed_time(e2) / K2
+    rank_barrier()
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2), device) / K2
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
@@ -593,7 +617,7 @@ def run_copy(args, rank, world, device):
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "bytes_per_step": step_bytes_,
         "roofline": roof,
-        "e2e": {"value": round(step_bytes_ / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(world * step_bytes_ / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": sum(h.numel() * 8 for h in host_pairs),
                 "d2h_bytes_per_step": probe.numel() * probe.element_size(), "steps": K2},
         "gpu_launches": K * len(calls),
@@ -619,7 +643,7 @@ def _packed(tensors: dict, pinned: bool, device=None):
     return buf, views
 
 
-def run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_):
+def run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, world=1):
     """Same step through the public API from pinned host buffers: the step's
     inputs (q, new K/V, slots, tables, lengths), packed in one page-locked
     buffer, cross in one H2D copy; write + decode; the output returns in one
@@ -649,14 +673,16 @@ def run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_):
     for w in range(3):
         one(w % n)
     torch.cuda.synchronize(device)
+    rank_barrier()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
     for it in range(K):
         one(it % n)
     e.record(stream)
     torch.cuda.synchronize(device)
-    ms = s.elapsed_time(e)
-    total = sum(bytes_[it % n]["decode"] + bytes_[it % n]["write"] for it in range(K))
+    rank_barrier()
+    ms = max_over_ranks(s.elapsed_time(e), device)
+    total = world * sum(bytes_[it % n]["decode"] + bytes_[it % n]["write"] for it in range(K))
     h2d = sum(t.numel() * t.element_size() for t in host[0][1].values())
     d2h = outs_h[0].numel() * outs_h[0].element_size()
     return {"value": round(total / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
