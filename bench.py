@@ -568,7 +568,9 @@ def run_copy(args, rank, world, device):
     pa.load_library()
     stream = torch.cuda.current_stream(device)
     if args.workload == "copy":
-        wl = workloads.copy_pairs()
+        # --num-blocks: a smaller pool (profiling), a quarter of it copied per call
+        wl = (workloads.copy_pairs(num_blocks=args.num_blocks, num_pairs=args.num_blocks // 4)
+              if args.num_blocks else workloads.copy_pairs())
         kc, vc = wl.k_cache.to(device), wl.v_cache.to(device)
         pairs = wl.pairs.to(device)
         calls = [(kc, vc, kc, vc, pairs)]
