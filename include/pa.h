@@ -264,6 +264,23 @@ pa_status pa_decode_no_alloc(const void* q, const void* k_cache, const void* v_c
                              int32_t num_q_heads, float scale, int32_t partition_tokens,
                              void* out, const pa_cache_desc* cache, void* stream);
 
+/*
+ * pa_check_wait_timeout -- checks the bounded wait that every kernel here
+ * uses between its roles (copy issue, MMA issue, softmax).  One CTA of
+ * max(32, expected) threads initialises an mbarrier that needs `expected`
+ * arrivals, makes `arrivals` of them, and waits for the phase with a bound of
+ * `limit_cycles` SM clocks.
+ * - arrivals == expected: the phase completes and nothing is raised.
+ * - arrivals < expected: nothing completes the phase; the wait gives up after
+ *   the bound, PA_DEVERR_TIMEOUT is raised and the kernel returns.  Nothing
+ *   faults and the context stays usable.
+ * Read the outcome with pa_last_device_error().  Needs 1 <= expected <= 1024,
+ * 0 <= arrivals <= expected and 1000 <= limit_cycles <= 2^31, else
+ * PA_ERR_INVALID_ARG.  Asynchronous on `stream`.
+ */
+pa_status pa_check_wait_timeout(int32_t expected, int32_t arrivals, int64_t limit_cycles,
+                                void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* pa_status_str(pa_status status);
 

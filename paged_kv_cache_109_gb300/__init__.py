@@ -78,6 +78,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.pa_status_str.restype = ctypes.c_char_p
     lib.pa_last_device_error.argtypes = []
     lib.pa_last_device_error.restype = I32
+    lib.pa_check_wait_timeout.argtypes = [I32, I32, ctypes.c_int64, P]
+    lib.pa_check_wait_timeout.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -256,6 +258,15 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int,
 def last_device_error() -> int:
     """PA_DEVERR_* bits raised since the last call (synchronises the device)."""
     return int(load_library().pa_last_device_error())
+
+
+def check_wait_timeout(expected: int, arrivals: int, limit_cycles: int, stream=None) -> None:
+    """Runs the bounded-wait check: an mbarrier needing `expected` arrivals
+    gets `arrivals`, and one CTA waits for it for at most `limit_cycles`
+    clocks (PA_DEVERR_TIMEOUT when it gives up; read last_device_error())."""
+    st = load_library().pa_check_wait_timeout(expected, arrivals, limit_cycles,
+                                              _stream(stream))
+    _check(st, "pa_check_wait_timeout")
 
 
 def prefill(q, query_start_loc, k_cache, v_cache, block_tables, seq_lens, max_q_len: int,

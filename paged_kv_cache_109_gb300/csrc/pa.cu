@@ -19,6 +19,7 @@
 #include "merge.cuh"
 #include "prefill_generic.cuh"
 #include "prefill_ws.cuh"
+#include "wait_check.cuh"
 #include "write_kv.cuh"
 
 namespace pa {
@@ -508,6 +509,17 @@ const char* pa_status_str(pa_status s) {
         case PA_ERR_CUDA: return "CUDA error";
         default: return "unknown status";
     }
+}
+
+pa_status pa_check_wait_timeout(int32_t expected, int32_t arrivals, int64_t limit_cycles,
+                                void* stream) {
+    if (expected < 1 || expected > 1024 || arrivals < 0 || arrivals > expected ||
+        limit_cycles < 1000 || limit_cycles > (1LL << 31))
+        return PA_ERR_INVALID_ARG;
+    const int32_t threads = ((std::max(32, expected) + 31) / 32) * 32;
+    pa::wait_check_kernel<<<1, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+        expected, arrivals, (long long)limit_cycles);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int32_t pa_last_device_error(void) {

@@ -107,3 +107,10 @@ def test_binding_refuses_host_tensors():
     x = torch.zeros(2, 8, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         pa.write_kv(x, x, torch.zeros(2, dtype=torch.int64), torch.zeros(4, 8, 16, 128), x)
+
+
+def test_wait_check_refuses_bad_arguments_without_a_gpu(lib):
+    """Argument checks run before any launch, so they need no device."""
+    for args in [(0, 0, 2_000_000), (1025, 0, 2_000_000), (4, 5, 2_000_000),
+                 (4, -1, 2_000_000), (4, 4, 10), (4, 4, 1 << 40)]:
+        assert lib.pa_check_wait_timeout(*args, None) == pa.PA_ERR_INVALID_ARG
