@@ -45,6 +45,17 @@
  * bound) never fault: the kernel skips the offending access, sets a bit in a
  * device error word and carries on; read it with pa_last_device_error().
  * No C++ exception crosses this interface.
+ *
+ * Debugging: with PA_DEBUG=1 in the environment (read at every call), each
+ * call first synchronises its stream, copies its index arrays to the host and
+ * checks them as a whole.  Duplicate slots, two copies into one block (or,
+ * inside one pool, onto a source), entries or slots outside the pool, lengths
+ * past their bounds and query rows out of order are then refused with
+ * PA_ERR_INVALID_ARG before launch (the first violation is printed to
+ * stderr).  This is slow and is not for use under stream capture.
+ *
+ * Tracing: each call is an NVTX range of its own name (pa_write_kv,
+ * pa_decode, ...) around its checks and launches.
  */
 #ifndef PA_H
 #define PA_H

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstring>
@@ -13,6 +14,7 @@
 #include <utility>
 
 #include "common.cuh"
+#include "debug_checks.h"
 #include "decode_generic.cuh"
 #include "decode_config.cuh"
 #include "decode_tma_mma.cuh"
@@ -226,6 +228,15 @@ pa_status launch_write(const void* k, const void* v, SlotFn slot_of, int32_t num
     return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// An NVTX range over one library call (host side: argument checks and
+// launches), so profilers can attribute the kernels to the call that made them.
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange&) = delete;
+    CallRange& operator=(const CallRange&) = delete;
+};
+
 }  // namespace
 }  // namespace pa
 
@@ -236,12 +247,19 @@ extern "C" {
 pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
                       int32_t num_tokens, void* k_cache, void* v_cache,
                       const pa_cache_desc* cache, void* stream) {
+    const CallRange range("pa_write_kv");
     if (!desc_ok(cache) || num_tokens < 0) return PA_ERR_INVALID_ARG;
     if (num_tokens == 0) return PA_OK;
     if (!slot_mapping || !aligned(slot_mapping, 8) || !map_step_arg(slot_mapping))
         return PA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (debug::enabled()) {
+        const pa_status r = debug::check_slots(
+            slot_mapping, num_tokens, (int64_t)cache->num_blocks * cache->block_size, st);
+        if (r != PA_OK) return r;
+    }
     return launch_write(k, v, SlotFromMapping{slot_mapping}, num_tokens, k_cache, v_cache, cache,
-                        static_cast<cudaStream_t>(stream));
+                        st);
 }
 
 pa_status pa_write_kv_positions(const void* k, const void* v, const int32_t* seq_ids,
@@ -249,6 +267,7 @@ pa_status pa_write_kv_positions(const void* k, const void* v, const int32_t* seq
                                 const int32_t* block_tables, int32_t num_seqs,
                                 int32_t max_blocks_per_seq, void* k_cache, void* v_cache,
                                 const pa_cache_desc* cache, void* stream) {
+    const CallRange range("pa_write_kv_positions");
     if (!desc_ok(cache) || num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq < 0)
         return PA_ERR_INVALID_ARG;
     if (num_tokens == 0) return PA_OK;
@@ -257,16 +276,22 @@ pa_status pa_write_kv_positions(const void* k, const void* v, const int32_t* seq
         return PA_ERR_INVALID_ARG;
     if (!map_step_arg(seq_ids) || !map_step_arg(positions) || !map_step_arg(block_tables))
         return PA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (debug::enabled()) {
+        const pa_status r = debug::check_positions(seq_ids, positions, num_tokens, block_tables,
+                                                   num_seqs, max_blocks_per_seq, cache, st);
+        if (r != PA_OK) return r;
+    }
     SlotFromPosition fn{seq_ids, positions, block_tables, num_seqs, max_blocks_per_seq,
                         cache->block_size, cache->num_blocks};
-    return launch_write(k, v, fn, num_tokens, k_cache, v_cache, cache,
-                        static_cast<cudaStream_t>(stream));
+    return launch_write(k, v, fn, num_tokens, k_cache, v_cache, cache, st);
 }
 
 pa_status pa_copy_blocks(const void* src_k, const void* src_v, int32_t src_num_blocks,
                          void* dst_k, void* dst_v, int32_t dst_num_blocks,
                          const int64_t* block_pairs, int32_t num_pairs,
                          const pa_cache_desc* cache, void* stream) {
+    const CallRange range("pa_copy_blocks");
     if (!desc_ok(cache) || num_pairs < 0 || src_num_blocks < 0 || dst_num_blocks < 0)
         return PA_ERR_INVALID_ARG;
     if (num_pairs == 0) return PA_OK;
@@ -285,12 +310,17 @@ pa_status pa_copy_blocks(const void* src_k, const void* src_v, int32_t src_num_b
     if (block_bytes % vec || !aligned(sk, vec) || !aligned(sv, vec) || !aligned(dk, vec) ||
         !aligned(dv, vec))
         return PA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (debug::enabled()) {
+        const pa_status r = debug::check_pairs(pairs, num_pairs, src_num_blocks, dst_num_blocks,
+                                               sk == dk, st);
+        if (r != PA_OK) return r;
+    }
     const int64_t total = (int64_t)num_pairs * 2 * (block_bytes / vec);
     const int threads = 256;
     const int64_t sms = std::max(1, device_sm_count());
     const unsigned blocks = (unsigned)std::max<int64_t>(
         1, std::min<int64_t>((total + threads - 1) / threads, sms * 16));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto go = [&](auto kern) {
         return launch_pdl(kern, dim3(blocks), dim3(threads), 0, st,
                           static_cast<const uint8_t*>(sk), static_cast<const uint8_t*>(sv),
@@ -334,6 +364,7 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     int32_t num_q_heads, float scale, int32_t partition_tokens, void* out,
                     void* workspace, size_t workspace_bytes_given, const pa_cache_desc* cache,
                     void* stream) {
+    const CallRange range("pa_decode");
     const int32_t path = pa_decode_path(num_q_heads, cache);
     if (path < 0 || num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq < 0 ||
         partition_tokens < 0)
@@ -365,6 +396,12 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     if (need > 0 && (!workspace || workspace_bytes_given < need || !aligned(workspace, 256) ||
                      !device_memory(workspace)))
         return PA_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (debug::enabled()) {
+        const pa_status r = debug::check_tables(block_tables, max_blocks_per_seq, seq_lens,
+                                                num_seqs, max_seq_len, nullptr, 0, cache, st);
+        if (r != PA_OK) return r;
+    }
 
     DecodeArgs a;
     a.q = q;
@@ -391,7 +428,6 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     a.max_parts = max_parts;
     a.scale_log2 = scale * kLog2e;
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     dim3 grid(max_parts, cache->num_kv_heads, num_seqs);
     cudaError_t err;
     if (fast) {
@@ -428,6 +464,7 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
                      const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
                      int32_t num_q_heads, float scale, void* out, const pa_cache_desc* cache,
                      void* stream) {
+    const CallRange range("pa_prefill");
     const int32_t path = pa_decode_path(num_q_heads, cache);
     if (path < 0 || num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_seq_len < 0 ||
         max_blocks_per_seq < 0 || max_q_len > max_seq_len)
@@ -446,6 +483,13 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
         !map_step_arg(seq_lens) || !map_step_arg(out) || !device_memory(k_cache) ||
         !device_memory(v_cache))
         return PA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (debug::enabled()) {
+        const pa_status r = debug::check_tables(block_tables, max_blocks_per_seq, seq_lens,
+                                                num_seqs, max_seq_len, query_start_loc, total_q,
+                                                cache, st);
+        if (r != PA_OK) return r;
+    }
     PrefillArgs a;
     a.q = q;
     a.k_cache = k_cache;
@@ -466,7 +510,6 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     a.tokens_per_tile = 128 % group == 0 ? 128 / group : 0;   // 128-row tcgen05 tiles
     constexpr int32_t kTilesPerCta = 2;
     a.scale_log2 = scale * kLog2e;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the tensor-core kernel takes its row maximum before scaling: scale >= 0
     const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) &&
                       aligned(k_cache, 16) && aligned(v_cache, 16) && scale >= 0.f;
