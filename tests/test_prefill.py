@@ -57,6 +57,9 @@ FAST = [
     (8, 4, 64, 64, (130, 64, 1), (130, 7, 1)),                    # G=2, D=64, B=64
     (32, 8, 128, 8, (45, 200), (45, 31)),                         # B=8
     (32, 8, 128, 16, (5, 3, 9), (1, 1, 1)),                       # decode rows only
+    (32, 8, 128, 256, (600, 300, 40), (333, 0, 40)),              # B=256; a sequence with no rows
+    (32, 8, 128, 48, (200, 97), (150, 60)),                       # B=48: three boxes per block
+    (16, 1, 64, 16, (77, 300), (77, 129)),                        # G=16, D=64
 ]
 
 
