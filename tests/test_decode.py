@@ -95,6 +95,8 @@ FAST_CASES = [
     (64, 8, 128, 64, (64, 65, 777)),                               # G=8, B=64
     (32, 8, 128, 8, (1, 7, 8, 9, 15, 16, 17, 300)),                # B=8: 2 blocks/chunk
     (16, 16, 64, 8, (3, 24, 25, 130)),                             # B=8, D=64, MHA
+    (32, 8, 128, 256, (1, 255, 256, 257, 2000)),                   # B=256: 16 chunks/block
+    (32, 2, 64, 32, (1, 95, 96, 97, 800)),                         # G=16, D=64, B=32
 ]
 
 
