@@ -56,6 +56,12 @@
  *
  * Tracing: each call is an NVTX range of its own name (pa_write_kv,
  * pa_decode, ...) around its checks and launches.
+ *
+ * CUDA graphs: the launching calls can be captured on a stream and replayed.
+ * A replay reads whatever the captured buffers hold at that time.  The grid
+ * is fixed at capture from the host bounds (max_seq_len, max_q_len, token
+ * and pair counts), so only the buffers' contents may change between
+ * replays, with lengths staying within those bounds.
  */
 #ifndef PA_H
 #define PA_H
