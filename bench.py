@@ -162,23 +162,33 @@ KERNEL_SOURCES = ("decode_tma_mma.cuh", "ptx.cuh", "merge.cuh", "decode_generic.
                   "common.cuh", "decode_config.cuh")
 
 
-def kernel_source_hash() -> str:
+# sources of the kernels whose traffic is recorded for the prefill and copy lines
+PREFILL_SOURCES = ("prefill_ws.cuh", "prefill_args.cuh", "ptx.cuh", "common.cuh",
+                   "decode_generic.cuh")
+COPY_SOURCES = ("write_kv.cuh", "common.cuh", "ptx.cuh")
+
+
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "paged_kv_cache_109_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def measured_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, or None
-    when there is none for this workload or the kernel sources changed since."""
+    """DRAM bytes per launch of the line's dominant kernel from the committed
+    ncu summary, or None when there is none for this workload or that
+    kernel's sources (the record's list, else the decode kernel's) changed."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(workload)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
+    if not rec:
+        return None
+    sources = tuple(rec.get("kernel_sources", KERNEL_SOURCES))
+    if rec.get("kernel_source_hash") != kernel_source_hash(sources):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -552,7 +562,8 @@ def run_prefill(args, rank, world, device):
         "prefill_tflops": round(tflops, 1),
         "roofline": {"bound": "tensor", "kernel": "pa_prefill call (tcgen05 bf16)",
                      "achieved": round(tflops, 1), "peak": peak, "peak_kind": peak_kind,
-                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                     "traffic": None if overrides(args) else measured_traffic("prefill"),
                      "flops_per_call": flops, "prefill_ms_mean": round(statistics.mean(pre_ms), 4)},
         "e2e": e2e,
         "gpu_launches": 2 * K,
@@ -621,7 +632,8 @@ def run_copy(args, rank, world, device):
     if args.workload == "copy":
         roof = {"bound": "hbm", "kernel": "pa_copy_blocks call", "achieved": round(achieved, 2),
                 "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind} (a copy, like this kernel)",
-                "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None}
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": None if args.num_blocks else measured_traffic("copy")}
     else:
         roof = {"bound": "host link", "kernel": "pa_copy_blocks calls (out + in)",
                 "achieved": round(achieved, 2), "peak": None, "unit": "GB/s", "frac": None,

@@ -92,7 +92,7 @@ class Workload:
 
     @property
     def num_seqs(self) -> int:
-        return int(self.steps[0].q.shape[0])
+        return int(self.steps[0].seq_lens.numel())   # q has one row per query token
 
     @property
     def max_seq_len(self) -> int:
