@@ -334,17 +334,32 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             for (int nd = 0; nd < C::kDTiles; ++nd) {
                 acc[nd][0] *= al0;
                 acc[nd][1] *= al0;
-                if (G16) {
-                    acc[nd][2] *= al1;
-                    acc[nd][3] *= al1;
-                }
+                acc[nd][2] *= G16 ? al1 : al0;     // G <= 8: the lo products of rows 0-7
+                acc[nd][3] *= G16 ? al1 : al0;
             }
-            // acc += P . V (P reused from the S registers as the A operand)
-            uint32_t pf[4];
-            pf[0] = pack_bf16x2(s[0][0], s[0][1]);
-            pf[1] = G16 ? pack_bf16x2(s[0][2], s[0][3]) : 0u;
-            pf[2] = pack_bf16x2(s[1][0], s[1][1]);
-            pf[3] = G16 ? pack_bf16x2(s[1][2], s[1][3]) : 0u;
+            // acc += P . V (P reused from the S registers as the A operand).
+            // P = hi + lo, both bf16: hi is P rounded, lo the rounding error
+            // rounded again, so P V keeps about 16 significant bits of each
+            // weight instead of 8.  With G <= 8 the MMA's rows 8-15 are free
+            // and carry the lo parts of rows 0-7 (their products land in this
+            // thread's accumulators 2-3 and are added to 0-1 at the end); with
+            // G > 8 the lo parts take a second product (cheap: this kernel
+            // waits on HBM, not on the tensor pipe).
+            uint32_t pf[4], pl[4];
+            auto split = [](float x, float y, uint32_t& hi, uint32_t& lo) {
+                hi = pack_bf16x2(x, y);
+                lo = pack_bf16x2(x - __uint_as_float(hi << 16),
+                                 y - __uint_as_float(hi & 0xffff0000u));
+            };
+            split(s[0][0], s[0][1], pf[0], pl[0]);
+            split(s[1][0], s[1][1], pf[2], pl[2]);
+            if (G16) {
+                split(s[0][2], s[0][3], pf[1], pl[1]);
+                split(s[1][2], s[1][3], pf[3], pl[3]);
+            } else {
+                pf[1] = pl[0];
+                pf[3] = pl[2];
+            }
             {
                 const int tok = (lm & 1) * 8 + lr;
 #pragma unroll
@@ -356,6 +371,10 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     ldsm_x4_trans(addr, b0, b1, b2, b3);
                     mma_bf16_16816(acc[2 * dp], pf, b0, b1);
                     mma_bf16_16816(acc[2 * dp + 1], pf, b2, b3);
+                    if (G16) {
+                        mma_bf16_16816(acc[2 * dp], pl, b0, b1);
+                        mma_bf16_16816(acc[2 * dp + 1], pl, b2, b3);
+                    }
                 }
             }
         }
@@ -376,6 +395,13 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
 
+    if (!G16) {
+#pragma unroll
+        for (int nd = 0; nd < C::kDTiles; ++nd) {
+            acc[nd][0] += acc[nd][2];
+            acc[nd][1] += acc[nd][3];
+        }
+    }
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     if (G16) {

@@ -9,7 +9,8 @@ import torch
 import oracle
 import paged_kv_cache_109_gb300 as pa
 from paged_kv_cache_109_gb300 import workloads
-from tests._gpu import BF16_ATOL, BF16_RTOL, assert_close, tolerance
+from tests._gpu import (BF16_ATOL, BF16_RTOL, P_ROUND, assert_close, prefill_weight_rounding,
+                        tolerance)
 
 pytestmark = pytest.mark.gpu
 
@@ -70,7 +71,8 @@ def test_fast_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens):
     scale = 1 / math.sqrt(d)
     out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
     ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
-    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "prefill")
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "prefill",
+                 prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale))
     assert pa.last_device_error() == 0
 
 
@@ -96,7 +98,8 @@ def test_long_context_slides_the_table_window(cuda_device):
     scale = 1 / math.sqrt(128)
     out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
     ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
-    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "long context")
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "long context",
+                 prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale))
 
 
 def test_decode_rows_agree_with_pa_decode(cuda_device):
@@ -125,12 +128,13 @@ def test_garbage_past_the_last_key_is_ignored(cuda_device):
     q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (37, 90), (5, 90), seed=6)
     scale = 1 / math.sqrt(128)
     ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
+    extra = prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale)
     for i, t in enumerate(sl.tolist()):
         last = int(bt[i, (t - 1) // 16])
         kc[last, :, t % 16:] = float("nan")
         vc[last, :, t % 16:] = float("inf")
     out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
-    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "nan tail")
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "nan tail", extra)
 
 
 def test_query_longer_than_sequence_is_reported(cuda_device):
@@ -141,9 +145,9 @@ def test_query_longer_than_sequence_is_reported(cuda_device):
                      vc.to(cuda_device), bt.to(cuda_device), sl.to(cuda_device), 20, 60, 0.1)
     torch.cuda.synchronize()
     assert pa.last_device_error() & pa.DEVERR_SEQ_LEN
-    ref = oracle.prefill(q[10:], torch.tensor([0, 20], dtype=torch.int32), kc, vc, bt[1:],
-                         sl[1:], 0.1)
-    assert_close(out[10:].double().cpu().numpy(), ref, BF16_ATOL, BF16_RTOL, "other sequence")
+    rest = (q[10:], torch.tensor([0, 20], dtype=torch.int32), kc, vc, bt[1:], sl[1:], 0.1)
+    assert_close(out[10:].double().cpu().numpy(), oracle.prefill(*rest), BF16_ATOL, BF16_RTOL,
+                 "other sequence", prefill_weight_rounding(*rest))
 
 
 def test_prefill_workload_reduced(cuda_device):
@@ -158,8 +162,9 @@ def test_prefill_workload_reduced(cuda_device):
                      int(st.seq_lens.max()), wl.scale).cpu()
     kh, vh = wl.k_cache.clone(), wl.v_cache.clone()
     oracle.write_kv(st.k_new, st.v_new, st.slot_mapping, kh, vh)
-    ref = oracle.prefill(st.q, st.query_start, kh, vh, st.block_tables, st.seq_lens, wl.scale)
-    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "prefill workload")
+    args = (st.q, st.query_start, kh, vh, st.block_tables, st.seq_lens, wl.scale)
+    assert_close(out.double().numpy(), oracle.prefill(*args), BF16_ATOL, BF16_RTOL,
+                 "prefill workload", prefill_weight_rounding(*args))
 
 
 def test_negative_scale_takes_the_portable_kernel(cuda_device):
@@ -176,13 +181,15 @@ def test_bad_table_entry_is_reported(cuda_device, hq, hkv, d):
     """An out-of-range block id in one sequence's table raises the error bit;
     the other sequence's rows are unaffected (fast and portable kernels)."""
     q, qs, kc, vc, bt, sl = case(hq, hkv, d, 16, (300, 200), (100, 50), seed=9)
-    ref = oracle.prefill(q[100:], torch.tensor([0, 50], dtype=torch.int32), kc, vc, bt[1:],
-                         sl[1:], 1 / math.sqrt(d))
+    rest = (q[100:], torch.tensor([0, 50], dtype=torch.int32), kc, vc, bt[1:], sl[1:],
+            1 / math.sqrt(d))
+    ref = oracle.prefill(*rest)
     bad = bt.clone()
     bad[0, 3] = kc.shape[0] + 5
     out = run(cuda_device, q, qs, kc, vc, bad, sl, 1 / math.sqrt(d))
     assert pa.last_device_error() & pa.DEVERR_TABLE_ENTRY
-    assert_close(out[100:].double().numpy(), ref, BF16_ATOL, BF16_RTOL, "other sequence")
+    assert_close(out[100:].double().numpy(), ref, BF16_ATOL, BF16_RTOL, "other sequence",
+                 prefill_weight_rounding(*rest))
 
 
 def test_prefill_from_pinned_host_arguments(cuda_device):
@@ -231,5 +238,7 @@ def test_prefill_workload_full_size_sampled(cuda_device):
     sl1 = torch.from_numpy((pos + 1).astype(np.int32))
     pairs = np.stack([np.arange(48), heads], axis=1)
     ref = oracle.decode(q1, wl.k_cache, wl.v_cache, bt1, sl1, wl.scale, pairs=pairs)
+    wv = oracle.decode(q1, wl.k_cache, wl.v_cache.abs(), bt1, sl1, wl.scale, pairs=pairs)
     got = out[torch.from_numpy(rows), torch.from_numpy(heads)].double().numpy()
-    assert_close(got, ref[np.arange(48), heads], BF16_ATOL, BF16_RTOL, "prefill full size")
+    assert_close(got, ref[np.arange(48), heads], BF16_ATOL, BF16_RTOL, "prefill full size",
+                 P_ROUND * wv[np.arange(48), heads])
