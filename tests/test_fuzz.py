@@ -85,7 +85,8 @@ def test_fuzz_prefill(cuda_device, seed):
     rng = np.random.default_rng(2000 + seed)
     hkv, g, d, bs, lens = _case(rng, prefill=True)
     hq = hkv * g
-    kc, vc, bt, gen = _pool(rng, hkv, d, bs, lens, torch.bfloat16)
+    dtype = torch.float32 if rng.random() < 0.15 else torch.bfloat16
+    kc, vc, bt, gen = _pool(rng, hkv, d, bs, lens, dtype)
     # each sequence queries its last L_i positions (0 <= L_i <= T_i)
     qlens = [int(rng.integers(0, t + 1)) if rng.random() < 0.8 else t for t in lens]
     qs = torch.tensor(np.concatenate([[0], np.cumsum(qlens)]), dtype=torch.int32)
@@ -93,7 +94,7 @@ def test_fuzz_prefill(cuda_device, seed):
     if total == 0:
         qlens[0], total = 1, 1
         qs = torch.tensor(np.concatenate([[0], np.cumsum(qlens)]), dtype=torch.int32)
-    q = torch.randn(total, hq, d, generator=gen).to(torch.bfloat16)
+    q = torch.randn(total, hq, d, generator=gen).to(dtype)
     sl = torch.tensor(lens, dtype=torch.int32)
     scale = float(rng.uniform(0.5, 1.5)) / math.sqrt(d)
     dev = cuda_device
@@ -101,8 +102,76 @@ def test_fuzz_prefill(cuda_device, seed):
                      max(qlens), max(lens), scale)
     torch.cuda.synchronize()
     ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
-    what = f"hq={hq} hkv={hkv} d={d} B={bs} lens={lens} rows={qlens}"
-    # the tensor-core kernel (128 rows a tile: G divides 128) multiplies bf16 P
-    extra = prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale) if 128 % g == 0 else None
-    assert_close(out.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, what, extra)
+    what = f"hq={hq} hkv={hkv} d={d} B={bs} lens={lens} rows={qlens} {dtype}"
+    if dtype == torch.float32:                     # the portable kernel, fp32 throughout
+        assert_close(out.cpu().double().numpy(), ref, F32_ATOL, 0.0, what)
+    else:
+        # the tensor-core kernel (128 rows a tile: G divides 128) multiplies bf16 P
+        extra = prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale) if 128 % g == 0 else None
+        assert_close(out.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, what, extra)
+    assert pa.last_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fuzz_write_from_positions(cuda_device, seed):
+    """Slots computed on the device from (sequence, position): bit-exact
+    against the oracle, with skipped tokens (id or position -1)."""
+    rng = np.random.default_rng(3000 + seed)
+    hkv, _, d, bs, lens = _case(rng, prefill=True)
+    dtype = torch.float32 if rng.random() < 0.2 else torch.bfloat16
+    kc, vc, bt, gen = _pool(rng, hkv, d, bs, lens, dtype)
+    # distinct (sequence, position) pairs inside the lengths, a few skipped
+    cand = [(i, p) for i, t in enumerate(lens) for p in range(t)]
+    pick = rng.choice(len(cand), size=min(len(cand), int(rng.integers(1, 300))), replace=False)
+    sid = np.array([cand[j][0] for j in pick], dtype=np.int32)
+    pos = np.array([cand[j][1] for j in pick], dtype=np.int32)
+    skip = rng.random(len(pick)) < 0.1
+    sid[skip & (rng.random(len(pick)) < 0.5)] = -1
+    pos[skip & (sid >= 0)] = -1
+    k = torch.randn(len(pick), hkv, d, generator=gen).to(dtype)
+    v = torch.randn(len(pick), hkv, d, generator=gen).to(dtype)
+    dev = cuda_device
+    kd, vd = kc.to(dev), vc.to(dev)
+    pa.write_kv_positions(k.to(dev), v.to(dev), torch.from_numpy(sid).to(dev),
+                          torch.from_numpy(pos).to(dev), bt.to(dev), kd, vd)
+    slots = oracle.slots_from_positions(sid, pos, bt, bs)
+    assert oracle.write_kv(k, v, torch.from_numpy(slots), kc, vc) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(kd.cpu(), kc) and torch.equal(vd.cpu(), vc)
+    assert pa.last_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fuzz_copy_blocks(cuda_device, seed):
+    """Whole-block copies inside one pool and through page-locked host memory:
+    bit-exact against the oracle."""
+    rng = np.random.default_rng(4000 + seed)
+    hkv = int(rng.choice([1, 2, 8]))
+    d = int(rng.choice([64, 128]))
+    bs = int(rng.choice(BLOCK_SIZES))
+    nb = int(rng.integers(8, 200))
+    dtype = torch.float32 if rng.random() < 0.2 else torch.bfloat16
+    g = torch.Generator().manual_seed(seed)
+    kc = torch.randn(nb, hkv, bs, d, generator=g).to(dtype)
+    vc = torch.randn(nb, hkv, bs, d, generator=g).to(dtype)
+    n = int(rng.integers(1, nb // 2 + 1))
+    perm = rng.permutation(nb)
+    pairs = torch.from_numpy(np.stack([perm[:n], perm[n:2 * n]], 1).astype(np.int64))
+    dev = cuda_device
+    kd, vd = kc.to(dev), vc.to(dev)
+    pa.copy_blocks(kd, vd, kd, vd, pairs.to(dev))
+    assert oracle.copy_blocks(kc, vc, kc, vc, pairs) == 0
+    # out to a pinned host pool and back into the device pool, reversed
+    hk = torch.zeros(n, hkv, bs, d, dtype=dtype).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory()
+    out_pairs = torch.stack([pairs[:, 1], torch.arange(n)], 1)
+    back_pairs = torch.stack([torch.arange(n), pairs[:, 0]], 1)
+    pa.copy_blocks(kd, vd, hk, hv, out_pairs.to(dev))
+    pa.copy_blocks(hk, hv, kd, vd, back_pairs.to(dev))
+    hk_ref, hv_ref = torch.zeros(n, hkv, bs, d, dtype=dtype), torch.zeros(n, hkv, bs, d, dtype=dtype)
+    assert oracle.copy_blocks(kc, vc, hk_ref, hv_ref, out_pairs) == 0
+    assert oracle.copy_blocks(hk_ref, hv_ref, kc, vc, back_pairs) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(hk, hk_ref) and torch.equal(hv, hv_ref)
+    assert torch.equal(kd.cpu(), kc) and torch.equal(vd.cpu(), vc)
     assert pa.last_device_error() == 0
