@@ -175,3 +175,38 @@ def test_fuzz_copy_blocks(cuda_device, seed):
     assert torch.equal(hk, hk_ref) and torch.equal(hv, hv_ref)
     assert torch.equal(kd.cpu(), kc) and torch.equal(vd.cpu(), vc)
     assert pa.last_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fuzz_portable_shapes(cuda_device, seed):
+    """Shapes only the portable kernels take (G > 16, head dims other than 64
+    and 128): decode and prefill against the oracle, fp32 and bf16."""
+    rng = np.random.default_rng(5000 + seed)
+    hkv = int(rng.choice([1, 2]))
+    g = int(rng.choice([1, 4, 24, 32]))
+    d = int(rng.choice([8, 32, 96, 256])) if g <= 16 else int(rng.choice([64, 96, 128]))
+    bs = int(rng.choice([4, 8, 16, 32]))
+    lens = [int(x) for x in rng.integers(1, 400, size=int(rng.integers(1, 5)))]
+    hq = hkv * g
+    dtype = torch.float32 if rng.random() < 0.4 else torch.bfloat16
+    kc, vc, bt, gen = _pool(rng, hkv, d, bs, lens, dtype)
+    assert pa.decode_path(hq, kc) == 0
+    sl = torch.tensor(lens, dtype=torch.int32)
+    scale = float(rng.uniform(0.5, 1.5)) / math.sqrt(d)
+    atol, rtol = (F32_ATOL, 0.0) if dtype == torch.float32 else (BF16_ATOL, BF16_RTOL)
+    dev = cuda_device
+    q = torch.randn(len(lens), hq, d, generator=gen).to(dtype)
+    out = pa.decode(q.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), sl.to(dev), max(lens), scale)
+    torch.cuda.synchronize()
+    what = f"hq={hq} hkv={hkv} d={d} B={bs} lens={lens} {dtype}"
+    assert_close(out.cpu().double().numpy(), oracle.decode(q, kc, vc, bt, sl, scale), atol, rtol,
+                 "decode " + what)
+    qlens = [int(rng.integers(1, t + 1)) for t in lens]
+    qs = torch.tensor(np.concatenate([[0], np.cumsum(qlens)]), dtype=torch.int32)
+    qp = torch.randn(int(qs[-1]), hq, d, generator=gen).to(dtype)
+    outp = pa.prefill(qp.to(dev), qs.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), sl.to(dev),
+                      max(qlens), max(lens), scale)
+    torch.cuda.synchronize()
+    assert_close(outp.cpu().double().numpy(), oracle.prefill(qp, qs, kc, vc, bt, sl, scale),
+                 atol, rtol, "prefill " + what)
+    assert pa.last_device_error() == 0
