@@ -292,6 +292,47 @@ def time_oracle(wl, budget_s: float, max_reps: int = 50, gpu_outs=None,
     return out
 
 
+def time_oracle_prefill(wl, budget_s: float, piece: int = 256) -> dict:
+    """The oracle's chunked prefill on the host cores: the chunk write of every
+    sequence, then the causal attention of the chunk rows, `piece` rows per
+    call, until ~budget_s seconds (one full step is about a TFLOP in fp64).
+    Rows [a, b) of sequence i's chunk are the last b - a positions of a
+    sequence of length T_i - L_i + b, so each piece is a prefill call of its
+    own.  value = the step's bytes as the GPU line counts them (the write,
+    plus the attention's bytes scaled by the share of rows done) per second."""
+    import oracle
+    threads = oracle.max_threads()
+    st = wl.steps[0]
+    kc, vc = wl.k_cache.clone(), wl.v_cache.clone()
+    qs, lens = st.query_start.tolist(), st.seq_lens.tolist()
+    t0 = time.perf_counter()
+    oracle.write_kv(st.k_new, st.v_new, st.slot_mapping, kc, vc)
+    elapsed = time.perf_counter() - t0
+    rows = 0
+    for i in range(len(lens)):
+        L = qs[i + 1] - qs[i]
+        for a in range(0, L, piece):
+            b = min(L, a + piece)
+            t_len = lens[i] - L + b
+            t0 = time.perf_counter()
+            oracle.prefill(st.q[qs[i] + a:qs[i] + b], torch.tensor([0, b - a], dtype=torch.int32),
+                           kc, vc, st.block_tables[i:i + 1],
+                           torch.tensor([t_len], dtype=torch.int32), wl.scale)
+            elapsed += time.perf_counter() - t0
+            rows += b - a
+            if elapsed >= budget_s:
+                break
+        if elapsed >= budget_s:
+            break
+    by = step_bytes(wl, 0, split_traffic=False)
+    done = by["write"] + by["decode"] * rows / qs[-1]
+    return {"value": done / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds": round(elapsed, 3), "steps": 1,
+            "sample": f"the chunk write of all {len(lens)} sequences, then the causal prefill "
+                      f"of {rows} of the {qs[-1]} chunk rows ({piece} rows per call), fp64 C "
+                      f"oracle with OpenMP, {elapsed:.1f} s"}
+
+
 def time_oracle_copy(args) -> dict:
     """The oracle's block copy on the host, repeated for ~cpu_seconds."""
     import oracle
@@ -555,7 +596,8 @@ def run_prefill(args, rank, world, device):
         "e2e": e2e,
         "gpu_launches": 2 * K,
         "clocks": clocks.summary(),
-        "cpu_baseline": None,
+        "cpu_baseline": (time_oracle_prefill(wl, args.cpu_seconds)
+                         if rank == 0 and world == 1 and not args.no_cpu_baseline else None),
     }
 
 
@@ -812,7 +854,8 @@ def run_reference(args, rank):
                         "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     wl = workloads.make(args.workload, **overrides(args))
     steps = max(1, args.steps)
-    cpu = time_oracle(wl, args.cpu_seconds, max_reps=steps)
+    cpu = (time_oracle_prefill(wl, args.cpu_seconds) if args.workload == "prefill"
+           else time_oracle(wl, args.cpu_seconds, max_reps=steps))
     return {"impl": "reference", "metric": METRIC, "value": round(cpu["value"], 4),
             "unit": "GB/s", "n_gpus": 0, "steps": cpu["steps"], "warmup": 0,
             "ms_per_step": round(1e3 * cpu["seconds"] / cpu["steps"], 3),
