@@ -326,8 +326,10 @@ def time_oracle_prefill(wl, budget_s: float, piece: int = 256) -> dict:
             break
     by = step_bytes(wl, 0, split_traffic=False)
     done = by["write"] + by["decode"] * rows / qs[-1]
+    # steps: the share of one step done (the attention's rows), so that
+    # seconds / steps is the time of a whole step at this rate
     return {"value": done / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "seconds": round(elapsed, 3), "steps": 1,
+            "seconds": round(elapsed, 3), "steps": round(rows / qs[-1], 4),
             "sample": f"the chunk write of all {len(lens)} sequences, then the causal prefill "
                       f"of {rows} of the {qs[-1]} chunk rows ({piece} rows per call), fp64 C "
                       f"oracle with OpenMP, {elapsed:.1f} s"}
