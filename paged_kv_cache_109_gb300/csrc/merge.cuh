@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
                 const int32_t d = d0 + tid + c * kMergeThreads;
                 if (d < a.head_dim) {
                     float s = 0.f;
-#pragma unroll 8
+#pragma unroll 32
                     for (int32_t p = 0; p < cnt; ++p)
                         s += w_sm[p] * acc[(int64_t)(p0 + p) * a.head_dim + d];
                     o[c] += s;
