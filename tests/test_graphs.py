@@ -106,3 +106,39 @@ def test_copy_on_write_in_a_graph(cuda_device):
         torch.cuda.synchronize()
         assert torch.equal(kd[dst], kd[src]) and torch.equal(vd[dst], vd[src])
     assert pa.last_device_error() == 0
+
+
+def test_back_to_back_steps_without_synchronising(cuda_device):
+    """Continuous-batching steps issued back to back (each kernel may start
+    before the previous one ends, by programmatic dependent launch), with no
+    synchronisation until the end: every step's output and the final caches
+    match the oracle replaying the same steps in order."""
+    from paged_kv_cache_109_gb300 import workloads
+    dev = cuda_device
+    wl = workloads.make("cb", num_seqs=12, num_steps=4, num_blocks=4096)
+    kd, vd = wl.k_cache.to(dev), wl.v_cache.to(dev)
+    # every step's inputs on the device first: a copy from pageable memory
+    # inside the loop would wait for the stream
+    ds = [{k: getattr(st, k).to(dev) for k in ("q", "k_new", "v_new", "slot_mapping",
+                                               "block_tables", "seq_lens")} for st in wl.steps]
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(2):
+        for st, d in zip(wl.steps, ds):
+            pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kd, vd)
+            for part in (0, 64):
+                outs.append(pa.decode(d["q"], kd, vd, d["block_tables"], d["seq_lens"],
+                                      int(st.seq_lens.max()), wl.scale, partition_tokens=part))
+    torch.cuda.synchronize()
+    assert pa.last_device_error() == 0
+    kh, vh = wl.k_cache.clone(), wl.v_cache.clone()
+    i = 0
+    for _ in range(2):
+        for st in wl.steps:
+            assert oracle.write_kv(st.k_new, st.v_new, st.slot_mapping, kh, vh) == 0
+            ref = oracle.decode(st.q, kh, vh, st.block_tables, st.seq_lens, wl.scale)
+            for part in (0, 64):
+                assert_close(outs[i].cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL,
+                             f"step {i // 2} partition {part}")
+                i += 1
+    assert torch.equal(kd.cpu(), kh) and torch.equal(vd.cpu(), vh)
