@@ -40,8 +40,10 @@ int device_sm_count() {
 
 // ---- kernel selection --------------------------------------------------------
 
+// Groups of more than 16 query heads are split into sub-groups of 16, one CTA
+// each, reading the same K/V tiles (the later reads mostly hit L2).
 bool fast_shape(const pa_cache_desc* c, int32_t group) {
-    if (c->dtype != PA_BF16 || group < 1 || group > 16) return false;
+    if (c->dtype != PA_BF16 || group < 1) return false;
     const int D = c->head_dim, B = c->block_size;
     if (D != 64 && D != 128) return false;
     return B == 8 || (B % 16 == 0 && B <= 256);
@@ -76,7 +78,8 @@ int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_le
     // PA_MAX_PARTITION_TOKENS tokens
     const int64_t unit = 4LL * B;
     const int64_t sms = std::max(1, device_sm_count());
-    const int64_t work = (int64_t)num_seqs * c->num_kv_heads * std::max(max_seq_len, 1);
+    const int64_t work = (int64_t)num_seqs * c->num_kv_heads * ((group + 15) / 16) *
+                         std::max(max_seq_len, 1);
     const int64_t target = (int64_t)PA_TARGET_CTAS_PER_SM * sms;
     int64_t p = (work + target - 1) / target;
     p = (p + unit - 1) / unit * unit;

@@ -37,6 +37,7 @@ struct DecodeArgs {
     int32_t head_dim;
     int32_t part_tokens;
     int32_t max_parts;
+    int32_t sub_groups;   // tensor-core kernel: CTAs per kv head, 16 query heads each
     float scale_log2;     // scale * log2(e)
 };
 

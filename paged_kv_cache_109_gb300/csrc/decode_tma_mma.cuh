@@ -87,17 +87,20 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
 
-    const int32_t p = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
+    // blockIdx.y = kv head g, sub-group sg: this CTA carries the group's
+    // query heads sg * 16 .. sg * 16 + G - 1
+    const int32_t p = blockIdx.x, g = blockIdx.y / a.sub_groups, i = blockIdx.z;
+    const int32_t sg = blockIdx.y - g * a.sub_groups;
     const int32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t grp = lane >> 2, tig = lane & 3;
-    const int32_t G = a.group;
+    const int32_t G = min(16, a.group - sg * 16);
     const int32_t BS = a.block_size;
     // B >= 16: a block is cpb = B/16 chunks.  B = 8: a chunk is two blocks,
     // loaded as two 8-row boxes (the 128-byte swizzle atom is 8 rows).
     const int32_t cpb = BS >= C::kChunk ? BS / C::kChunk : 1;
     const int32_t P = a.part_tokens;
     const int32_t t0 = p * P;
-    const int64_t head0 = (int64_t)i * a.num_q_heads + (int64_t)g * G;
+    const int64_t head0 = (int64_t)i * a.num_q_heads + (int64_t)g * a.group + sg * 16;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kRingBytes);

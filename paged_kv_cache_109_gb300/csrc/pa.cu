@@ -131,7 +131,7 @@ cudaError_t launch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
 
 cudaError_t dispatch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
                           const DecodeArgs& a, cudaStream_t st) {
-    const bool g16 = a.group > 8;
+    const bool g16 = a.group > 8;                 // 16 rows: any CTA may carry 9-16 heads
     switch (a.head_dim) {
         case 64: return g16 ? launch_fast<64, true>(grid, mk, mv, a, st)
                             : launch_fast<64, false>(grid, mk, mv, a, st);
@@ -427,8 +427,10 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     a.part_tokens = part;
     a.max_parts = max_parts;
     a.scale_log2 = scale * kLog2e;
+    a.sub_groups = fast ? (group + 15) / 16 : 1;
+    if ((int64_t)cache->num_kv_heads * a.sub_groups > 65535) return PA_ERR_UNSUPPORTED;
 
-    dim3 grid(max_parts, cache->num_kv_heads, num_seqs);
+    dim3 grid(max_parts, cache->num_kv_heads * a.sub_groups, num_seqs);
     cudaError_t err;
     if (fast) {
         CUtensorMap mk, mv;
@@ -511,7 +513,7 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     constexpr int32_t kTilesPerCta = 2;
     a.scale_log2 = scale * kLog2e;
     // the tensor-core kernel takes its row maximum before scaling: scale >= 0
-    const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) &&
+    const bool fast = path == 1 && group <= 16 && a.tokens_per_tile > 0 && aligned(q, 16) &&
                       aligned(k_cache, 16) && aligned(v_cache, 16) && scale >= 0.f;
     cudaError_t err;
     if (fast) {

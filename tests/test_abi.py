@@ -53,7 +53,7 @@ def test_path_selection(lib):
     assert path(32, desc()) == 1                       # bf16, D=128, B=16, G=4
     assert path(64, desc(bs=32)) == 1                  # G=8, B=32
     assert path(128, desc(bs=32)) == 1                 # G=16
-    assert path(256, desc()) == 0                      # G=32: portable kernel
+    assert path(256, desc()) == 1                      # G=32: two 16-head sub-groups
     assert path(32, desc(dtype=pa.PA_F32)) == 0        # fp32: portable kernel
     assert path(32, desc(bs=64)) == 1                  # B=64: four 16-token chunks
     assert path(32, desc(bs=48)) == 1

@@ -97,6 +97,9 @@ FAST_CASES = [
     (16, 16, 64, 8, (3, 24, 25, 130)),                             # B=8, D=64, MHA
     (32, 8, 128, 256, (1, 255, 256, 257, 2000)),                   # B=256: 16 chunks/block
     (32, 2, 64, 32, (1, 95, 96, 97, 800)),                         # G=16, D=64, B=32
+    (64, 2, 128, 16, (5, 300, 1000)),                              # G=32: two sub-groups of 16
+    (48, 2, 128, 16, (1, 17, 700)),                                # G=24: sub-groups of 16 and 8
+    (40, 1, 64, 32, (33, 400)),                                    # G=40: 16, 16 and 8
 ]
 
 
@@ -116,7 +119,7 @@ def test_fast_kernel_matches_oracle(cuda_device, hq, hkv, d, bs, lengths, part):
 @pytest.mark.parametrize("hq,hkv,d,bs,lengths,dtype", [
     (8, 2, 8, 4, (10, 7, 1, 33), torch.float32),
     (32, 8, 128, 16, (1, 200, 1000), torch.float32),
-    (64, 2, 128, 16, (5, 300), torch.bfloat16),           # G=32: portable kernel
+    (64, 2, 96, 16, (5, 300), torch.bfloat16),            # G=32, D=96: portable kernel
     (6, 2, 96, 8, (1, 8, 9, 100), torch.bfloat16),       # D=96, B=8
     (4, 4, 256, 16, (17, 64), torch.bfloat16),           # D=256
 ])

@@ -19,7 +19,7 @@ BLOCK_SIZES = (8, 16, 32, 48, 64, 128)
 
 def _case(rng, prefill=False):
     hkv = int(rng.choice([1, 2, 4, 8]))
-    g = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+    g = int(rng.choice([1, 2, 3, 4, 5, 8, 16, 24, 32]))
     d = int(rng.choice([64, 128]))
     bs = int(rng.choice(BLOCK_SIZES))
     n = int(rng.integers(1, 7))
@@ -106,8 +106,9 @@ def test_fuzz_prefill(cuda_device, seed):
     if dtype == torch.float32:                     # the portable kernel, fp32 throughout
         assert_close(out.cpu().double().numpy(), ref, F32_ATOL, 0.0, what)
     else:
-        # the tensor-core kernel (128 rows a tile: G divides 128) multiplies bf16 P
-        extra = prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale) if 128 % g == 0 else None
+        # the tensor-core kernel (G <= 16 dividing 128) multiplies bf16 P
+        fast = g <= 16 and 128 % g == 0
+        extra = prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale) if fast else None
         assert_close(out.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, what, extra)
     assert pa.last_device_error() == 0
 
@@ -179,8 +180,9 @@ def test_fuzz_copy_blocks(cuda_device, seed):
 
 @pytest.mark.parametrize("seed", range(12))
 def test_fuzz_portable_shapes(cuda_device, seed):
-    """Shapes only the portable kernels take (G > 16, head dims other than 64
-    and 128): decode and prefill against the oracle, fp32 and bf16."""
+    """Shapes the portable kernels take: head dims other than 64 and 128, fp32,
+    and (prefill) groups of more than 16 query heads; decode and prefill
+    against the oracle."""
     rng = np.random.default_rng(5000 + seed)
     hkv = int(rng.choice([1, 2]))
     g = int(rng.choice([1, 4, 24, 32]))
@@ -190,7 +192,8 @@ def test_fuzz_portable_shapes(cuda_device, seed):
     hq = hkv * g
     dtype = torch.float32 if rng.random() < 0.4 else torch.bfloat16
     kc, vc, bt, gen = _pool(rng, hkv, d, bs, lens, dtype)
-    assert pa.decode_path(hq, kc) == 0
+    tma = dtype == torch.bfloat16 and d in (64, 128) and (bs == 8 or bs % 16 == 0)
+    assert pa.decode_path(hq, kc) == (1 if tma else 0)
     sl = torch.tensor(lens, dtype=torch.int32)
     scale = float(rng.uniform(0.5, 1.5)) / math.sqrt(d)
     atol, rtol = (F32_ATOL, 0.0) if dtype == torch.float32 else (BF16_ATOL, BF16_RTOL)
