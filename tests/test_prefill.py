@@ -61,6 +61,9 @@ FAST = [
     (32, 8, 128, 256, (600, 300, 40), (333, 0, 40)),              # B=256; a sequence with no rows
     (32, 8, 128, 48, (200, 97), (150, 60)),                       # B=48: three boxes per block
     (16, 1, 64, 16, (77, 300), (77, 129)),                        # G=16, D=64
+    (64, 2, 128, 16, (300, 41), (150, 41)),                       # G=32: 4 tokens a tile
+    (64, 1, 64, 32, (90,), (90,)),                                # G=64: 2 tokens a tile
+    (128, 1, 128, 16, (33, 70), (33, 20)),                        # G=128: 1 token a tile
 ]
 
 
