@@ -233,7 +233,7 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * max_q_len        host upper bound of L_i (sizes the grid).
  * Other arguments as pa_decode.  L_i > T_i is reported (PA_DEVERR_SEQ_LEN)
  * and that sequence's rows are left untouched.  bf16 with head_dim 64/128,
- * block_size 8 or a multiple of 16, a group size dividing 128 and scale >= 0
+ * block_size 8 or a multiple of 16, a group size of at most 128 and scale >= 0
  * runs on the TMA + tcgen05 kernel (tensor-memory accumulators); other valid
  * shapes (head_dim <= 256) and scales on a portable kernel.
  */

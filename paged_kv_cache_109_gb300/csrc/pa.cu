@@ -509,7 +509,9 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     a.num_blocks = cache->num_blocks;
     a.block_size = cache->block_size;
     a.head_dim = cache->head_dim;
-    a.tokens_per_tile = 128 % group == 0 ? 128 / group : 0;   // 128-row tcgen05 tiles
+    // 128-row tcgen05 tiles of floor(128 / G) tokens x G heads (the last
+    // 128 mod G rows idle)
+    a.tokens_per_tile = group <= 128 ? 128 / group : 0;
     constexpr int32_t kTilesPerCta = 2;
     a.scale_log2 = scale * kLog2e;
     // the tensor-core kernel takes its row maximum before scaling: scale >= 0

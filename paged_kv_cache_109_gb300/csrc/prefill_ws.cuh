@@ -147,7 +147,8 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int32_t w = warp >> 2, r = tid & (C::kRows - 1);
     const int32_t tok = w * tpt + r / G, head = r - (r / G) * G;
     const bool softmax = warp < C::kSoftmaxWarps && w < ntiles;
-    const bool row_ok = softmax && tok < ntok;
+    // rows past tpt * G (G not dividing 128) carry nothing: no Q, no output
+    const bool row_ok = softmax && r < tpt * G && tok < ntok;
     const int32_t pos = pos0 + min(tok, ntok - 1);
     const int64_t row_elem = ((int64_t)(q0 + tok0 + tok) * a.num_q_heads + g * G + head) * D;
     if (softmax) {

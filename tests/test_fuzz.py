@@ -106,8 +106,8 @@ def test_fuzz_prefill(cuda_device, seed):
     if dtype == torch.float32:                     # the portable kernel, fp32 throughout
         assert_close(out.cpu().double().numpy(), ref, F32_ATOL, 0.0, what)
     else:
-        # the tensor-core kernel (G dividing 128) multiplies bf16 P
-        fast = 128 % g == 0
+        # the tensor-core kernel (G <= 128) multiplies bf16 P
+        fast = g <= 128
         extra = prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale) if fast else None
         assert_close(out.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, what, extra)
     assert pa.last_device_error() == 0

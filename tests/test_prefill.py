@@ -64,6 +64,9 @@ FAST = [
     (64, 2, 128, 16, (300, 41), (150, 41)),                       # G=32: 4 tokens a tile
     (64, 1, 64, 32, (90,), (90,)),                                # G=64: 2 tokens a tile
     (128, 1, 128, 16, (33, 70), (33, 20)),                        # G=128: 1 token a tile
+    (28, 4, 128, 16, (300, 77), (200, 77)),                       # G=7: 18 tokens, 2 rows idle
+    (40, 8, 128, 16, (150,), (150,)),                             # G=5: 25 tokens, 3 rows idle
+    (24, 2, 64, 16, (61, 130), (61, 40)),                         # G=12: 10 tokens, 8 rows idle
 ]
 
 
@@ -81,7 +84,7 @@ def test_fast_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens):
 
 @pytest.mark.parametrize("hq,hkv,d,bs,ctx,qlens,dtype", [
     (4, 2, 8, 4, (10, 7), (10, 3), torch.float32),               # the worked-example shape
-    (12, 4, 128, 16, (100, 33), (20, 33), torch.bfloat16),       # G=3: portable kernel
+    (12, 4, 256, 16, (100, 33), (20, 33), torch.bfloat16),       # D=256: portable kernel
     (6, 2, 96, 8, (50,), (9,), torch.bfloat16),                  # D=96
     (32, 8, 128, 16, (300, 40), (64, 40), torch.float32),
 ])
