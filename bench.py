@@ -159,7 +159,7 @@ class ClockSampler:
 
 
 KERNEL_SOURCES = ("decode_tma_mma.cuh", "ptx.cuh", "merge.cuh", "decode_generic.cuh",
-                  "common.cuh", "decode_config.cuh")
+                  "common.cuh", "decode_config.cuh", "decode_tiled.cuh")
 
 
 # sources of the kernels whose traffic is recorded for the prefill and copy lines

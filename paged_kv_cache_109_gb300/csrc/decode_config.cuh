@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <cstdint>
 
+#include "decode_tiled.cuh"
 #include "pa.h"
 
 #ifndef PA_USE_PDL
@@ -49,6 +50,14 @@ bool fast_shape(const pa_cache_desc* c, int32_t group) {
     return B == 8 || (B % 16 == 0 && B <= 256);
 }
 
+// The tiled CUDA-core kernel: head dims up to 256 whose rows are whole
+// 16-byte pieces (its copies are 16 bytes; the caches must be 16-byte aligned,
+// which the caller checks).
+bool tiled_shape(const pa_cache_desc* c) {
+    const int e = c->dtype == PA_F32 ? 4 : 2;
+    return c->head_dim <= 256 && (c->head_dim * e) % 16 == 0;
+}
+
 // Largest partition (tokens) the generic kernel's shared memory holds.
 int32_t generic_max_partition(const pa_cache_desc* c, int32_t group) {
     const size_t budget = 96 * 1024;
@@ -68,24 +77,30 @@ int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_le
                        const pa_cache_desc* c) {
     const int32_t B = c->block_size;
     const int32_t group = num_q_heads / c->num_kv_heads;
-    if (!fast_shape(c, group)) {
+    const bool fast = fast_shape(c, group);
+    if (!fast && !tiled_shape(c)) {
         int32_t cap = generic_max_partition(c, group);
         int32_t want = std::max(B, (512 / B) * B);
         return std::max(B, std::min(cap, want));
     }
-    // one block per warp per step; aim for about PA_TARGET_CTAS_PER_SM CTAs
-    // per SM over the batch (counted at max_seq_len), between 4 blocks and
+    // TMA kernel: one block per warp per step; tiled kernel: a chunk for each
+    // of its four warps, rounded up to whole blocks.  Aim for about
+    // PA_TARGET_CTAS_PER_SM CTAs per SM over the batch (counted at
+    // max_seq_len, sub-groups included), between one unit and
     // PA_MAX_PARTITION_TOKENS tokens
-    const int64_t unit = 4LL * B;
+    const int64_t chunks = (int64_t)kTiledWarps * tiled_chunk(c->head_dim, c->dtype == PA_F32 ? 4 : 2);
+    const int64_t unit = fast ? 4LL * B : (chunks + B - 1) / B * B;   // whole blocks
     const int64_t sms = std::max(1, device_sm_count());
-    const int64_t work = (int64_t)num_seqs * c->num_kv_heads * ((group + 15) / 16) *
+    const int64_t heads_per_cta = fast ? 16 : 8;
+    const int64_t work = (int64_t)num_seqs * c->num_kv_heads *
+                         ((group + heads_per_cta - 1) / heads_per_cta) *
                          std::max(max_seq_len, 1);
     const int64_t target = (int64_t)PA_TARGET_CTAS_PER_SM * sms;
     int64_t p = (work + target - 1) / target;
     p = (p + unit - 1) / unit * unit;
     const int64_t cap = std::max<int64_t>(unit, PA_MAX_PARTITION_TOKENS / unit * unit);
     p = std::min(std::max(p, unit), cap);
-    p = std::min<int64_t>(p, fast_max_partition(c));
+    if (fast) p = std::min<int64_t>(p, fast_max_partition(c));
     return (int32_t)p;
 }
 

@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "debug_checks.h"
 #include "decode_generic.cuh"
+#include "decode_tiled.cuh"
 #include "decode_config.cuh"
 #include "decode_tma_mma.cuh"
 #include "merge.cuh"
@@ -127,6 +128,41 @@ cudaError_t launch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
     if (!set_smem(kern, C::smem_bytes_max())) return cudaErrorInvalidValue;
     const size_t smem = C::smem_bytes(a.part_tokens, a.block_size);
     return launch_pdl(kern, grid, dim3(C::kThreads), smem, st, mk, mv, a);
+}
+
+template <typename E, int HB, int CH, int C>
+cudaError_t launch_tiled_kernel(dim3 grid, size_t smem, cudaStream_t st, const DecodeArgs& a) {
+    auto kern = decode_tiled_kernel<E, HB, CH, C>;
+    if (!set_smem(kern, smem)) return cudaErrorInvalidValue;
+    return launch_pdl(kern, grid, dim3(kTiledThreads), smem, st, a);
+}
+
+template <typename E, int CH, int C>
+cudaError_t launch_tiled_hb(int32_t hb, dim3 grid, size_t smem, cudaStream_t st,
+                            const DecodeArgs& a) {
+    switch (hb) {
+        case 1: return launch_tiled_kernel<E, 1, CH, C>(grid, smem, st, a);
+        case 2: return launch_tiled_kernel<E, 2, CH, C>(grid, smem, st, a);
+        case 4: return launch_tiled_kernel<E, 4, CH, C>(grid, smem, st, a);
+        default: return launch_tiled_kernel<E, 8, CH, C>(grid, smem, st, a);
+    }
+}
+
+// The tiled kernel's instance for the shape: heads per CTA rounded to a power
+// of 2, chunk tokens and columns per lane from the row size.
+cudaError_t dispatch_tiled(const pa_cache_desc* c, int32_t group, dim3 grid,
+                           const DecodeArgs& a, cudaStream_t st) {
+    const int32_t D = c->head_dim, e = elem_bytes(c);
+    const int32_t hb = tiled_heads_rounded(tiled_sub_group(group));
+    const size_t smem = tiled_smem_bytes(D, e, hb);
+    const bool ch16 = tiled_chunk(D, e) == 16, c4 = tiled_cols(D) == 4;
+    if (c->dtype == PA_F32) {
+        if (ch16) return launch_tiled_hb<float, 16, 4>(hb, grid, smem, st, a);   // D <= 64
+        if (c4) return launch_tiled_hb<float, 8, 4>(hb, grid, smem, st, a);      // D <= 128
+        return launch_tiled_hb<float, 8, 8>(hb, grid, smem, st, a);
+    }
+    if (ch16) return launch_tiled_hb<__nv_bfloat16, 16, 4>(hb, grid, smem, st, a);   // D <= 128
+    return launch_tiled_hb<__nv_bfloat16, 8, 8>(hb, grid, smem, st, a);
 }
 
 cudaError_t dispatch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -383,7 +419,10 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     if (fast && (part > fast_max_partition(cache) || !aligned(k_cache, 16) ||
                  !aligned(v_cache, 16) || !aligned(q, 16)))
         fast = false;
-    if (!fast && part > generic_max_partition(cache, group)) return PA_ERR_UNSUPPORTED;
+    // other shapes: the tiled CUDA-core kernel, else (a head dim that is not
+    // whole 16-byte rows, or unaligned caches) the generic one
+    const bool tiled = !fast && tiled_shape(cache) && aligned(k_cache, 16) && aligned(v_cache, 16);
+    if (!fast && !tiled && part > generic_max_partition(cache, group)) return PA_ERR_UNSUPPORTED;
     if (!aligned(q, elem_bytes(cache)) || !aligned(out, elem_bytes(cache)) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PA_ERR_INVALID_ARG;
@@ -427,7 +466,7 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     a.part_tokens = part;
     a.max_parts = max_parts;
     a.scale_log2 = scale * kLog2e;
-    a.sub_groups = fast ? (group + 15) / 16 : 1;
+    a.sub_groups = fast ? (group + 15) / 16 : tiled ? (group + kTiledHeads - 1) / kTiledHeads : 1;
     if ((int64_t)cache->num_kv_heads * a.sub_groups > 65535) return PA_ERR_UNSUPPORTED;
 
     dim3 grid(max_parts, cache->num_kv_heads * a.sub_groups, num_seqs);
@@ -437,6 +476,9 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
         if (!cached_map(&mk, k_cache, cache, 0) || !cached_map(&mv, v_cache, cache, 1))
             return PA_ERR_CUDA;
         err = dispatch_fast(grid, mk, mv, a, st);
+    } else if (tiled) {
+        err = dispatch_tiled(cache, group, grid, a, st);
+        if (err == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
     } else {
         const size_t smem = generic_smem_bytes(group, cache->head_dim, part, B);
         if (cache->dtype == PA_F32) {

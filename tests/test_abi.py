@@ -83,6 +83,15 @@ def test_auto_partition_is_block_multiple(lib):
         d = desc(bs=bs)
         p = lib.pa_decode_partition_tokens(64, 32, maxlen, ctypes.byref(d))
         assert p > 0 and p % bs == 0
+    # every kernel's sizing, including block sizes that do not divide its
+    # natural unit (the CUDA-core kernel walks chunks of 8 or 16 tokens)
+    for dtype in (pa.PA_BF16, pa.PA_F32):
+        for dd in (40, 64, 96, 128, 200, 256):
+            for bs in (1, 3, 4, 5, 8, 16, 48, 96, 128, 256):
+                for hq, maxlen in ((8, 100), (32, 4096), (64, 70000)):
+                    d = desc(bs=bs, d=dd, dtype=dtype)
+                    p = lib.pa_decode_partition_tokens(4, hq, maxlen, ctypes.byref(d))
+                    assert p > 0 and p % bs == 0, (dtype, dd, bs, hq, maxlen, p)
 
 
 def test_invalid_arguments_rejected_before_any_launch(lib):
