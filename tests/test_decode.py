@@ -135,6 +135,48 @@ def test_portable_kernel_matches_oracle(cuda_device, hq, hkv, d, bs, lengths, dt
     assert_close(out.double().numpy(), ref, atol, rtol, "portable")
 
 
+@pytest.mark.parametrize("hq,hkv,d,bs,lengths,dtype,part", [
+    (12, 4, 200, 3, (1, 50, 257), torch.bfloat16, 0),      # 8-token chunks, 8 columns a lane
+    (12, 4, 200, 3, (1, 50, 257), torch.bfloat16, 21),     # partitions not whole chunks
+    (24, 2, 40, 5, (7, 333), torch.bfloat16, 0),           # G=12: sub-groups of 8 and 4
+    (24, 2, 40, 5, (7, 333), torch.bfloat16, 35),
+    (8, 8, 136, 7, (100, 1, 64), torch.float32, 0),        # fp32 rows over 256 bytes
+    (6, 2, 64, 1, (1100, 3), torch.float32, 1100),          # >512 blocks in one partition
+    (6, 3, 12, 16, (30, 70), torch.bfloat16, 0),           # 24-byte rows: the generic kernel
+    (6, 3, 12, 16, (30, 70), torch.bfloat16, 32),
+])
+def test_cuda_core_kernels_match_oracle(cuda_device, hq, hkv, d, bs, lengths, dtype, part):
+    """The CUDA-core kernels' own cases: chunk sizes, sub-groups, block sizes
+    that split chunks into several copies, a partition whose table entries do
+    not fit the kernel's shared copy, and rows that are not whole 16-byte
+    pieces."""
+    q, kc, vc, bt, sl = synthetic(hq, hkv, d, bs, lengths, dtype=dtype, seed=d * 7 + bs)
+    assert pa.decode_path(hq, kc) == 0
+    scale = 1.1 / math.sqrt(d)
+    out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=part)
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    atol, rtol = tolerance(dtype)
+    assert_close(out.double().numpy(), ref, atol, rtol, f"{hq}/{hkv}/{d}/{bs}/{dtype}/{part}")
+    assert pa.last_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype,d,bs,part", [(torch.float32, 64, 16, 64),
+                                             (torch.bfloat16, 96, 4, 0),
+                                             (torch.float32, 32, 1, 1024)])
+def test_bad_table_entry_on_cuda_core_kernel(cuda_device, dtype, d, bs, part):
+    """Out-of-range entries are reported and their tokens skipped, from the
+    partition's shared copy of the table and (blocks of one token, partition
+    of 1024) from the table itself."""
+    q, kc, vc, bt, sl = synthetic(8, 2, d, bs, (700, 300), dtype=dtype, seed=12)
+    assert pa.decode_path(8, kc) == 0
+    bt = bt.clone()
+    nb = kc.shape[0]
+    bt[0, 5] = nb            # == num_blocks: out of range
+    bt[1, 2] = -3
+    gpu_decode(cuda_device, q, kc, vc, bt, sl, 0.1, partition_tokens=part)
+    assert pa.last_device_error() & pa.DEVERR_TABLE_ENTRY
+
+
 # ---- split-K partials and merge --------------------------------------------------
 
 @pytest.mark.parametrize("hq,hkv,d,bs,part", [(32, 8, 128, 16, 64), (64, 8, 128, 32, 256),
