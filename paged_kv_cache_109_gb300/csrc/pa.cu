@@ -149,20 +149,26 @@ cudaError_t launch_tiled_hb(int32_t hb, dim3 grid, size_t smem, cudaStream_t st,
 }
 
 // The tiled kernel's instance for the shape: heads per CTA rounded to a power
-// of 2, chunk tokens and columns per lane from the row size.
+// of 2, chunk tokens and columns per lane from the row size (4 KB chunks:
+// bf16 (16, 4) up to D = 128, else (8, 8); fp32 (16, 4) up to D = 64, (8, 4)
+// up to 128, else (4, 8)).
 cudaError_t dispatch_tiled(const pa_cache_desc* c, int32_t group, dim3 grid,
                            const DecodeArgs& a, cudaStream_t st) {
     const int32_t D = c->head_dim, e = elem_bytes(c);
     const int32_t hb = tiled_heads_rounded(tiled_sub_group(group));
     const size_t smem = tiled_smem_bytes(D, e, hb);
-    const bool ch16 = tiled_chunk(D, e) == 16, c4 = tiled_cols(D) == 4;
+    const int32_t ch = tiled_chunk(D, e), cols = tiled_cols(D);
     if (c->dtype == PA_F32) {
-        if (ch16) return launch_tiled_hb<float, 16, 4>(hb, grid, smem, st, a);   // D <= 64
-        if (c4) return launch_tiled_hb<float, 8, 4>(hb, grid, smem, st, a);      // D <= 128
-        return launch_tiled_hb<float, 8, 8>(hb, grid, smem, st, a);
+        if (ch == 16 && cols == 4) return launch_tiled_hb<float, 16, 4>(hb, grid, smem, st, a);
+        if (ch == 8 && cols == 4) return launch_tiled_hb<float, 8, 4>(hb, grid, smem, st, a);
+        if (ch == 4 && cols == 8) return launch_tiled_hb<float, 4, 8>(hb, grid, smem, st, a);
+    } else {
+        if (ch == 16 && cols == 4)
+            return launch_tiled_hb<__nv_bfloat16, 16, 4>(hb, grid, smem, st, a);
+        if (ch == 8 && cols == 8)
+            return launch_tiled_hb<__nv_bfloat16, 8, 8>(hb, grid, smem, st, a);
     }
-    if (ch16) return launch_tiled_hb<__nv_bfloat16, 16, 4>(hb, grid, smem, st, a);   // D <= 128
-    return launch_tiled_hb<__nv_bfloat16, 8, 8>(hb, grid, smem, st, a);
+    return cudaErrorInvalidValue;   // no instance (cannot happen for D <= 256)
 }
 
 cudaError_t dispatch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
