@@ -235,7 +235,9 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * and that sequence's rows are left untouched.  bf16 with head_dim 64/128,
  * block_size 8 or a multiple of 16, a group size of at most 128 and scale >= 0
  * runs on the TMA + tcgen05 kernel (tensor-memory accumulators); other valid
- * shapes (head_dim <= 256) and scales on a portable kernel.
+ * shapes (head_dim <= 256) and scales on CUDA cores: a tiled kernel when the
+ * rows are whole 16-byte pieces and the caches 16-byte aligned, else a
+ * generic one.
  */
 pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t total_q,
                      int32_t max_q_len, const void* k_cache, const void* v_cache,

@@ -21,6 +21,7 @@
 #include "decode_tma_mma.cuh"
 #include "merge.cuh"
 #include "prefill_generic.cuh"
+#include "prefill_tiled.cuh"
 #include "prefill_ws.cuh"
 #include "wait_check.cuh"
 #include "write_kv.cuh"
@@ -169,6 +170,34 @@ cudaError_t dispatch_tiled(const pa_cache_desc* c, int32_t group, dim3 grid,
             return launch_tiled_hb<__nv_bfloat16, 8, 8>(hb, grid, smem, st, a);
     }
     return cudaErrorInvalidValue;   // no instance (cannot happen for D <= 256)
+}
+
+template <typename E, int RPT, int NF, int KC>
+cudaError_t launch_prefill_tiled(const pa_cache_desc* c, int32_t group, int32_t max_q_len,
+                                 int32_t num_seqs, cudaStream_t st, const PrefillArgs& a) {
+    using Cfg = PrefillTiledCfg<RPT, NF, KC>;
+    const int32_t ht = std::min(group, Cfg::kRows), qt = Cfg::kRows / ht;
+    const int32_t nsub = (group + ht - 1) / ht;
+    if ((int64_t)c->num_kv_heads * nsub > 65535) return cudaErrorInvalidValue;
+    const int32_t tiles = std::max(1, (max_q_len + qt - 1) / qt);
+    const size_t smem = Cfg::smem_bytes(c->head_dim, elem_bytes(c));
+    auto kern = prefill_tiled_kernel<E, RPT, NF, KC>;
+    if (!set_smem(kern, smem)) return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3(tiles, c->num_kv_heads * nsub, num_seqs), dim3(kPtThreads), smem,
+                      st, a);
+}
+
+// The CUDA-core prefill: 64-row tiles, 32-key chunks up to 128 columns;
+// 32-row tiles, 16-key chunks up to 256.
+cudaError_t dispatch_prefill_tiled(const pa_cache_desc* c, int32_t group, int32_t max_q_len,
+                                   int32_t num_seqs, cudaStream_t st, const PrefillArgs& a) {
+    const bool narrow = c->head_dim <= 128;
+    if (c->dtype == PA_F32)
+        return narrow ? launch_prefill_tiled<float, 4, 4, 32>(c, group, max_q_len, num_seqs, st, a)
+                      : launch_prefill_tiled<float, 2, 8, 16>(c, group, max_q_len, num_seqs, st, a);
+    return narrow
+               ? launch_prefill_tiled<__nv_bfloat16, 4, 4, 32>(c, group, max_q_len, num_seqs, st, a)
+               : launch_prefill_tiled<__nv_bfloat16, 2, 8, 16>(c, group, max_q_len, num_seqs, st, a);
 }
 
 cudaError_t dispatch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -584,6 +613,9 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
             if (!set_smem(kern, Cfg::smem_bytes())) return PA_ERR_UNSUPPORTED;
             err = launch_pdl(kern, grid, dim3(Cfg::kThreads), Cfg::smem_bytes(), st, mk, mv, a);
         }
+    } else if (tiled_shape(cache) && aligned(k_cache, 16) && aligned(v_cache, 16)) {
+        err = dispatch_prefill_tiled(cache, group, max_q_len, num_seqs, st, a);
+        if (err == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
     } else {
         if (cache->head_dim > 32 * kGenericMaxDimPerLane) return PA_ERR_UNSUPPORTED;
         dim3 grid(total_q, cache->num_kv_heads);

@@ -84,11 +84,19 @@ def test_fast_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens):
 
 @pytest.mark.parametrize("hq,hkv,d,bs,ctx,qlens,dtype", [
     (4, 2, 8, 4, (10, 7), (10, 3), torch.float32),               # the worked-example shape
-    (12, 4, 256, 16, (100, 33), (20, 33), torch.bfloat16),       # D=256: portable kernel
+    (12, 4, 256, 16, (100, 33), (20, 33), torch.bfloat16),       # D=256: 32-row tiles
     (6, 2, 96, 8, (50,), (9,), torch.bfloat16),                  # D=96
     (32, 8, 128, 16, (300, 40), (64, 40), torch.float32),
+    (32, 8, 128, 16, (2000, 700), (600, 700), torch.float32),    # many key chunks and tiles
+    (12, 4, 200, 3, (300, 70), (120, 70), torch.bfloat16),       # G=3: 21 tokens a tile, 1 row idle
+    (24, 2, 40, 5, (333, 7), (100, 7), torch.bfloat16),          # G=12, D=40, B=5
+    (160, 2, 64, 16, (90, 20), (90, 5), torch.float32),          # G=80: two CTAs per kv head
+    (8, 8, 136, 7, (129, 64), (129, 1), torch.float32),          # fp32 rows over 512 bytes
+    (6, 3, 12, 16, (30, 70), (30, 9), torch.bfloat16),           # 24-byte rows: generic kernel
 ])
 def test_portable_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens, dtype):
+    """The CUDA-core prefill kernels (tiled, and generic for rows that are not
+    whole 16-byte pieces) on the shapes the tensor-core kernel does not take."""
     q, qs, kc, vc, bt, sl = case(hq, hkv, d, bs, ctx, qlens, dtype=dtype, seed=d)
     scale = 0.8 / math.sqrt(d)
     out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
