@@ -235,9 +235,11 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * and that sequence's rows are left untouched.  bf16 with head_dim 64/128,
  * block_size 8 or a multiple of 16, a group size of at most 128 and scale >= 0
  * runs on the TMA + tcgen05 kernel (tensor-memory accumulators); other valid
- * shapes (head_dim <= 256) and scales on CUDA cores: a tiled kernel when the
- * rows are whole 16-byte pieces and the caches 16-byte aligned, else a
- * generic one.
+ * shapes (head_dim <= 256) and scales on a warp-level tensor-core kernel
+ * (bf16, head_dim a multiple of 16, 16-byte aligned q and caches), else on
+ * CUDA cores: a tiled kernel when the rows are whole 16-byte pieces and the
+ * caches 16-byte aligned, else a generic one.  The tensor-core kernels round
+ * the softmax weights to bf16 before P V.
  */
 pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t total_q,
                      int32_t max_q_len, const void* k_cache, const void* v_cache,

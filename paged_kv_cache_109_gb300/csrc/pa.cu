@@ -21,6 +21,7 @@
 #include "decode_tma_mma.cuh"
 #include "merge.cuh"
 #include "prefill_generic.cuh"
+#include "prefill_mma.cuh"
 #include "prefill_tiled.cuh"
 #include "prefill_ws.cuh"
 #include "wait_check.cuh"
@@ -198,6 +199,32 @@ cudaError_t dispatch_prefill_tiled(const pa_cache_desc* c, int32_t group, int32_
     return narrow
                ? launch_prefill_tiled<__nv_bfloat16, 4, 4, 32>(c, group, max_q_len, num_seqs, st, a)
                : launch_prefill_tiled<__nv_bfloat16, 2, 8, 16>(c, group, max_q_len, num_seqs, st, a);
+}
+
+template <int DMAX, int KC>
+cudaError_t launch_prefill_mma(const pa_cache_desc* c, int32_t group, int32_t max_q_len,
+                               int32_t num_seqs, cudaStream_t st, const PrefillArgs& a) {
+    const int32_t ht = std::min(group, kPmRows), qt = kPmRows / ht;
+    const int32_t nsub = (group + ht - 1) / ht;
+    if ((int64_t)c->num_kv_heads * nsub > 65535) return cudaErrorInvalidValue;
+    const int32_t tiles = std::max(1, (max_q_len + qt - 1) / qt);
+    const size_t smem = PrefillMmaCfg<DMAX, KC>::smem_bytes(c->head_dim);
+    auto kern = prefill_mma_kernel<DMAX, KC>;
+    if (!set_smem(kern, smem)) return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3(tiles, c->num_kv_heads * nsub, num_seqs), dim3(kPmThreads), smem,
+                      st, a);
+}
+
+// bf16 head dims that are multiples of 16: the mma.sync prefill, 64-key
+// chunks up to 128 columns, 32-key chunks up to 256.
+bool prefill_mma_shape(const pa_cache_desc* c) {
+    return c->dtype == PA_BF16 && c->head_dim % 16 == 0 && c->head_dim <= 256;
+}
+
+cudaError_t dispatch_prefill_mma(const pa_cache_desc* c, int32_t group, int32_t max_q_len,
+                                 int32_t num_seqs, cudaStream_t st, const PrefillArgs& a) {
+    return c->head_dim <= 128 ? launch_prefill_mma<128, 64>(c, group, max_q_len, num_seqs, st, a)
+                              : launch_prefill_mma<256, 32>(c, group, max_q_len, num_seqs, st, a);
 }
 
 cudaError_t dispatch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -613,6 +640,10 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
             if (!set_smem(kern, Cfg::smem_bytes())) return PA_ERR_UNSUPPORTED;
             err = launch_pdl(kern, grid, dim3(Cfg::kThreads), Cfg::smem_bytes(), st, mk, mv, a);
         }
+    } else if (prefill_mma_shape(cache) && aligned(q, 16) && aligned(out, 4) &&
+               aligned(k_cache, 16) && aligned(v_cache, 16)) {
+        err = dispatch_prefill_mma(cache, group, max_q_len, num_seqs, st, a);
+        if (err == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
     } else if (tiled_shape(cache) && aligned(k_cache, 16) && aligned(v_cache, 16)) {
         err = dispatch_prefill_tiled(cache, group, max_q_len, num_seqs, st, a);
         if (err == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;

@@ -210,9 +210,10 @@ def test_fuzz_portable_shapes(cuda_device, seed):
     outp = pa.prefill(qp.to(dev), qs.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), sl.to(dev),
                       max(qlens), max(lens), scale)
     torch.cuda.synchronize()
-    # the tensor-core prefill kernel (the same shapes as the TMA decode
-    # kernel) multiplies bf16 P
-    extra = prefill_weight_rounding(qp, qs, kc, vc, bt, sl, scale) if tma else None
+    # the tensor-core prefill kernels (tcgen05, and mma.sync for bf16 head
+    # dims that are multiples of 16) multiply bf16 P
+    bf16_p = dtype == torch.bfloat16 and d % 16 == 0
+    extra = prefill_weight_rounding(qp, qs, kc, vc, bt, sl, scale) if bf16_p else None
     assert_close(outp.cpu().double().numpy(), oracle.prefill(qp, qs, kc, vc, bt, sl, scale),
                  atol, rtol, "prefill " + what, extra)
     assert pa.last_device_error() == 0

@@ -93,16 +93,24 @@ def test_fast_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens):
     (160, 2, 64, 16, (90, 20), (90, 5), torch.float32),          # G=80: two CTAs per kv head
     (8, 8, 136, 7, (129, 64), (129, 1), torch.float32),          # fp32 rows over 512 bytes
     (6, 3, 12, 16, (30, 70), (30, 9), torch.bfloat16),           # 24-byte rows: generic kernel
+    (16, 8, 256, 16, (700, 300), (500, 300), torch.bfloat16),    # Gemma-like D=256, G=2: mma.sync
+    (12, 4, 160, 5, (333, 64), (200, 1), torch.bfloat16),        # D=160, B=5, a decode row
+    (32, 32, 80, 16, (257, 99), (257, 33), torch.bfloat16),      # D=80 MHA: 64 tokens a tile
 ])
 def test_portable_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens, dtype):
-    """The CUDA-core prefill kernels (tiled, and generic for rows that are not
-    whole 16-byte pieces) on the shapes the tensor-core kernel does not take."""
+    """The kernels for the shapes the tcgen05 kernel does not take: mma.sync
+    (bf16, head dims that are multiples of 16), CUDA-core tiled (fp32 and the
+    other bf16 head dims), generic (rows that are not whole 16-byte pieces)."""
     q, qs, kc, vc, bt, sl = case(hq, hkv, d, bs, ctx, qlens, dtype=dtype, seed=d)
     scale = 0.8 / math.sqrt(d)
     out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
     ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
     atol, rtol = tolerance(dtype)
-    assert_close(out.double().numpy(), ref, atol, rtol, "portable prefill")
+    # bf16 head dims that are multiples of 16 take the mma.sync kernel, which
+    # (like the tcgen05 one) multiplies bf16 P
+    extra = (prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale)
+             if dtype == torch.bfloat16 and d % 16 == 0 else None)
+    assert_close(out.double().numpy(), ref, atol, rtol, "portable prefill", extra)
 
 
 def test_long_context_slides_the_table_window(cuda_device):
@@ -182,12 +190,13 @@ def test_prefill_workload_reduced(cuda_device):
 
 
 def test_negative_scale_takes_the_portable_kernel(cuda_device):
-    """The tensor-core kernel needs scale >= 0; a negative scale is still
-    computed exactly by the portable kernel."""
+    """The tcgen05 kernel needs scale >= 0; a negative scale is computed by
+    the mma.sync kernel (bf16 P, as in the tcgen05 kernel)."""
     q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (150, 60), (40, 60), seed=8)
     out = run(cuda_device, q, qs, kc, vc, bt, sl, -0.05)
-    ref = oracle.prefill(q, qs, kc, vc, bt, sl, -0.05)
-    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "negative scale")
+    args = (q, qs, kc, vc, bt, sl, -0.05)
+    assert_close(out.double().numpy(), oracle.prefill(*args), BF16_ATOL, BF16_RTOL,
+                 "negative scale", prefill_weight_rounding(*args))
 
 
 @pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (4, 2, 8)])
