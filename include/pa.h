@@ -252,10 +252,13 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
  * Which decode kernel these arguments select: 1 = the TMA + tensor-core
  * kernel (bf16, head_dim 64 or 128, block_size 8 or a multiple of 16 up to
  * 256, any group size: a group of more than 16 query heads is split into
- * CTAs of 16 that read the same K/V tiles), 0 = a CUDA-core kernel (any
- * other valid shape, and every fp32 cache: the tiled kernel when head_dim is
- * at most 256 with rows of whole 16-byte pieces and the caches are 16-byte
- * aligned, else the generic one), < 0 = invalid arguments.
+ * CTAs of 16 that read the same K/V tiles), 2 = the warp-level tensor-core
+ * kernel (bf16, head_dim a multiple of 16 up to 128 that kernel 1 does not
+ * take, groups of 5 or more query heads; used when q is 4-byte and the caches
+ * 16-byte aligned), 0 = a CUDA-core kernel (any other valid shape, and every
+ * fp32 cache: the tiled kernel when head_dim is at most 256 with rows of
+ * whole 16-byte pieces and the caches are 16-byte aligned, else the generic
+ * one), < 0 = invalid arguments.
  */
 int32_t pa_decode_path(int32_t num_q_heads, const pa_cache_desc* cache);
 

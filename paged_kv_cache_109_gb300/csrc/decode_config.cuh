@@ -58,6 +58,24 @@ bool tiled_shape(const pa_cache_desc* c) {
     return c->head_dim <= 256 && (c->head_dim * e) % 16 == 0;
 }
 
+#ifndef PA_DECODE_MMA_MIN_GROUP
+#define PA_DECODE_MMA_MIN_GROUP 5
+#endif
+
+// The mma.sync kernel: bf16 head dims that are multiples of 16 up to 128 the
+// TMA kernel does not take (other head dims, other block sizes), for groups
+// of at least PA_DECODE_MMA_MIN_GROUP query heads.  Smaller groups stay on
+// the tiled CUDA-core kernel: its run copies move a block's rows with one
+// copy each, where this kernel copies every row on its own (to pad it), and
+// at up to four heads the CUDA cores keep up with HBM.  Measured, fraction
+// of the copy peak (tiled / mma.sync): G = 1, D = 96: 0.886 / 0.467;
+// G = 4, D = 96: 0.487 / 0.452; G = 4, B = 4: 0.615 / 0.582; G = 8, D = 64,
+// B = 4: 0.210 / 0.374; G = 16, D = 112: 0.169 / 0.433.
+bool mma_shape(const pa_cache_desc* c, int32_t group) {
+    return c->dtype == PA_BF16 && c->head_dim % 16 == 0 && c->head_dim <= 128 &&
+           group >= PA_DECODE_MMA_MIN_GROUP && !fast_shape(c, group);
+}
+
 // Largest partition (tokens) the generic kernel's shared memory holds.
 int32_t generic_max_partition(const pa_cache_desc* c, int32_t group) {
     const size_t budget = 96 * 1024;
@@ -78,20 +96,23 @@ int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_le
     const int32_t B = c->block_size;
     const int32_t group = num_q_heads / c->num_kv_heads;
     const bool fast = fast_shape(c, group);
-    if (!fast && !tiled_shape(c)) {
+    const bool mma = mma_shape(c, group);
+    if (!fast && !mma && !tiled_shape(c)) {
         int32_t cap = generic_max_partition(c, group);
         int32_t want = std::max(B, (512 / B) * B);
         return std::max(B, std::min(cap, want));
     }
-    // TMA kernel: one block per warp per step; tiled kernel: a chunk for each
-    // of its four warps, rounded up to whole blocks.  Aim for about
+    // TMA kernel: one block per warp per step; mma.sync and tiled kernels: a
+    // chunk for each of their four warps, rounded up to whole blocks.  Aim for about
     // PA_TARGET_CTAS_PER_SM CTAs per SM over the batch (counted at
     // max_seq_len, sub-groups included), between one unit and
     // PA_MAX_PARTITION_TOKENS tokens
-    const int64_t chunks = (int64_t)kTiledWarps * tiled_chunk(c->head_dim, c->dtype == PA_F32 ? 4 : 2);
+    const int64_t chunks = mma ? 4 * 16
+                               : (int64_t)kTiledWarps *
+                                     tiled_chunk(c->head_dim, c->dtype == PA_F32 ? 4 : 2);
     const int64_t unit = fast ? 4LL * B : (chunks + B - 1) / B * B;   // whole blocks
     const int64_t sms = std::max(1, device_sm_count());
-    const int64_t heads_per_cta = fast ? 16 : 8;
+    const int64_t heads_per_cta = fast || mma ? 16 : 8;
     const int64_t work = (int64_t)num_seqs * c->num_kv_heads *
                          ((group + heads_per_cta - 1) / heads_per_cta) *
                          std::max(max_seq_len, 1);

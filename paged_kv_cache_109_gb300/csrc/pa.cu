@@ -18,6 +18,7 @@
 #include "decode_generic.cuh"
 #include "decode_tiled.cuh"
 #include "decode_config.cuh"
+#include "decode_mma.cuh"
 #include "decode_tma_mma.cuh"
 #include "merge.cuh"
 #include "prefill_generic.cuh"
@@ -438,7 +439,8 @@ pa_status pa_copy_blocks(const void* src_k, const void* src_v, int32_t src_num_b
 
 int32_t pa_decode_path(int32_t num_q_heads, const pa_cache_desc* cache) {
     if (!desc_ok(cache) || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return -1;
-    return fast_shape(cache, num_q_heads / cache->num_kv_heads) ? 1 : 0;
+    const int32_t group = num_q_heads / cache->num_kv_heads;
+    return fast_shape(cache, group) ? 1 : mma_shape(cache, group) ? 2 : 0;
 }
 
 int32_t pa_decode_partition_tokens(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
@@ -481,10 +483,14 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     if (fast && (part > fast_max_partition(cache) || !aligned(k_cache, 16) ||
                  !aligned(v_cache, 16) || !aligned(q, 16)))
         fast = false;
-    // other shapes: the tiled CUDA-core kernel, else (a head dim that is not
+    // other shapes: the mma.sync kernel (bf16, head dims that are multiples of
+    // 16 up to 128), the tiled CUDA-core kernel, else (a head dim that is not
     // whole 16-byte rows, or unaligned caches) the generic one
-    const bool tiled = !fast && tiled_shape(cache) && aligned(k_cache, 16) && aligned(v_cache, 16);
-    if (!fast && !tiled && part > generic_max_partition(cache, group)) return PA_ERR_UNSUPPORTED;
+    const bool caches16 = aligned(k_cache, 16) && aligned(v_cache, 16);
+    const bool mma = path == 2 && caches16 && aligned(q, 4);
+    const bool tiled = !fast && !mma && tiled_shape(cache) && caches16;
+    if (!fast && !mma && !tiled && part > generic_max_partition(cache, group))
+        return PA_ERR_UNSUPPORTED;
     if (!aligned(q, elem_bytes(cache)) || !aligned(out, elem_bytes(cache)) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PA_ERR_INVALID_ARG;
@@ -528,7 +534,9 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     a.part_tokens = part;
     a.max_parts = max_parts;
     a.scale_log2 = scale * kLog2e;
-    a.sub_groups = fast ? (group + 15) / 16 : tiled ? (group + kTiledHeads - 1) / kTiledHeads : 1;
+    a.sub_groups = fast || mma ? (group + 15) / 16
+                   : tiled     ? (group + kTiledHeads - 1) / kTiledHeads
+                               : 1;
     if ((int64_t)cache->num_kv_heads * a.sub_groups > 65535) return PA_ERR_UNSUPPORTED;
 
     dim3 grid(max_parts, cache->num_kv_heads * a.sub_groups, num_seqs);
@@ -538,6 +546,11 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
         if (!cached_map(&mk, k_cache, cache, 0) || !cached_map(&mv, v_cache, cache, 1))
             return PA_ERR_CUDA;
         err = dispatch_fast(grid, mk, mv, a, st);
+    } else if (mma) {
+        const size_t smem = decode_mma_smem_bytes(cache->head_dim);
+        auto kern = group > 8 ? decode_mma_kernel<true> : decode_mma_kernel<false>;
+        if (!set_smem(kern, smem)) return PA_ERR_UNSUPPORTED;
+        err = launch_pdl(kern, grid, dim3(kMmaThreads), smem, st, a);
     } else if (tiled) {
         err = dispatch_tiled(cache, group, grid, a, st);
         if (err == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;

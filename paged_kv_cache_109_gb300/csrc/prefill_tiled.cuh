@@ -26,6 +26,7 @@
 //     acc = a acc + sum_k p[k] V[k][:].
 #pragma once
 
+#include "cp_async.cuh"
 #include "prefill_args.cuh"
 
 namespace pa {
@@ -45,21 +46,6 @@ struct PrefillTiledCfg {
         return (size_t)kRows * head_dim * 4 + 2 * 2 * (size_t)KC * stride + (size_t)kRows * KC * 4;
     }
 };
-
-// 16-byte global -> shared copy; src_bytes = 0 fills the destination with
-// zeros and reads nothing.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 // Four consecutive values of a shared-memory row as floats (8- or 16-byte
 // aligned).

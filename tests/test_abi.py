@@ -58,9 +58,15 @@ def test_path_selection(lib):
     assert path(32, desc(bs=64)) == 1                  # B=64: four 16-token chunks
     assert path(32, desc(bs=48)) == 1
     assert path(32, desc(bs=8)) == 1                   # B=8: two blocks per chunk
-    assert path(32, desc(bs=24)) == 0                  # neither 8 nor a multiple of 16
+    assert path(32, desc(bs=24)) == 0                  # neither 8 nor a multiple of 16, G=4
     assert path(32, desc(bs=4)) == 0
     assert path(32, desc(bs=512)) == 0
+    assert path(64, desc(bs=24)) == 2                  # G=8: mma.sync
+    assert path(64, desc(bs=4)) == 2
+    assert path(40, desc(d=96)) == 2                   # G=5, bf16 head dim a multiple of 16
+    assert path(32, desc(d=96)) == 0                   # G=4: CUDA cores
+    assert path(64, desc(d=40)) == 0                   # not a multiple of 16: CUDA cores
+    assert path(64, desc(d=256)) == 0                  # over 128: CUDA cores
     assert path(16, desc(d=64, bs=64, hkv=4)) == 1
     assert path(8, desc(d=8, bs=4, hkv=2, dtype=pa.PA_F32)) == 0
     assert path(30, desc()) == -1                      # Hq not a multiple of Hkv

@@ -14,7 +14,7 @@ import oracle
 import paged_kv_cache_109_gb300 as pa
 from paged_kv_cache_109_gb300 import workloads
 from tests._gpu import (BF16_ATOL, BF16_RTOL, F32_ATOL, DeviceState, HostState, assert_close,
-                        sample_pairs, tolerance)
+                        sample_pairs, tolerance, decode_kernel)
 
 pytestmark = pytest.mark.gpu
 
@@ -126,7 +126,7 @@ def test_fast_kernel_matches_oracle(cuda_device, hq, hkv, d, bs, lengths, part):
 @pytest.mark.parametrize("part", [0, "B", "5B"])
 def test_portable_kernel_matches_oracle(cuda_device, hq, hkv, d, bs, lengths, dtype, part):
     q, kc, vc, bt, sl = synthetic(hq, hkv, d, bs, lengths, dtype=dtype, seed=d + bs)
-    assert pa.decode_path(hq, kc) == 0
+    assert pa.decode_path(hq, kc) == decode_kernel(dtype, d, bs, hq // hkv)
     scale = 0.9 / math.sqrt(d)
     ptok = 0 if part == 0 else bs * int(part[:-1] or 1)
     out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=ptok)
@@ -144,6 +144,10 @@ def test_portable_kernel_matches_oracle(cuda_device, hq, hkv, d, bs, lengths, dt
     (6, 2, 64, 1, (1100, 3), torch.float32, 1100),          # >512 blocks in one partition
     (6, 3, 12, 16, (30, 70), torch.bfloat16, 0),           # 24-byte rows: the generic kernel
     (6, 3, 12, 16, (30, 70), torch.bfloat16, 32),
+    (40, 8, 96, 16, (1, 100, 257), torch.bfloat16, 0),     # mma.sync, G=5 (lo parts in rows 8-15)
+    (96, 8, 80, 5, (700, 33), torch.bfloat16, 35),         # mma.sync, G=12, B=5
+    (64, 4, 64, 1, (1100, 3), torch.bfloat16, 1100),       # mma.sync, G=16, >512 blocks a partition
+    (256, 8, 112, 24, (500, 1, 90), torch.bfloat16, 0),    # mma.sync, G=32: two sub-groups
 ])
 def test_cuda_core_kernels_match_oracle(cuda_device, hq, hkv, d, bs, lengths, dtype, part):
     """The CUDA-core kernels' own cases: chunk sizes, sub-groups, block sizes
@@ -151,7 +155,7 @@ def test_cuda_core_kernels_match_oracle(cuda_device, hq, hkv, d, bs, lengths, dt
     not fit the kernel's shared copy, and rows that are not whole 16-byte
     pieces."""
     q, kc, vc, bt, sl = synthetic(hq, hkv, d, bs, lengths, dtype=dtype, seed=d * 7 + bs)
-    assert pa.decode_path(hq, kc) == 0
+    assert pa.decode_path(hq, kc) == decode_kernel(dtype, d, bs, hq // hkv)
     scale = 1.1 / math.sqrt(d)
     out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=part)
     ref = oracle.decode(q, kc, vc, bt, sl, scale)
@@ -160,15 +164,17 @@ def test_cuda_core_kernels_match_oracle(cuda_device, hq, hkv, d, bs, lengths, dt
     assert pa.last_device_error() == 0
 
 
-@pytest.mark.parametrize("dtype,d,bs,part", [(torch.float32, 64, 16, 64),
-                                             (torch.bfloat16, 96, 4, 0),
-                                             (torch.float32, 32, 1, 1024)])
-def test_bad_table_entry_on_cuda_core_kernel(cuda_device, dtype, d, bs, part):
+@pytest.mark.parametrize("dtype,d,bs,part,hq", [(torch.float32, 64, 16, 64, 8),
+                                                (torch.bfloat16, 96, 4, 0, 8),
+                                                (torch.float32, 32, 1, 1024, 8),
+                                                (torch.bfloat16, 96, 4, 0, 16),
+                                                (torch.bfloat16, 64, 1, 1024, 32)])
+def test_bad_table_entry_on_cuda_core_kernel(cuda_device, dtype, d, bs, part, hq):
     """Out-of-range entries are reported and their tokens skipped, from the
     partition's shared copy of the table and (blocks of one token, partition
-    of 1024) from the table itself."""
-    q, kc, vc, bt, sl = synthetic(8, 2, d, bs, (700, 300), dtype=dtype, seed=12)
-    assert pa.decode_path(8, kc) == 0
+    of 1024) from the table itself; CUDA-core and mma.sync kernels."""
+    q, kc, vc, bt, sl = synthetic(hq, 2, d, bs, (700, 300), dtype=dtype, seed=12)
+    assert pa.decode_path(hq, kc) == decode_kernel(dtype, d, bs, hq // 2)
     bt = bt.clone()
     nb = kc.shape[0]
     bt[0, 5] = nb            # == num_blocks: out of range

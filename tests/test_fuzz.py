@@ -10,7 +10,8 @@ import torch
 
 import oracle
 import paged_kv_cache_109_gb300 as pa
-from tests._gpu import BF16_ATOL, BF16_RTOL, F32_ATOL, assert_close, prefill_weight_rounding
+from tests._gpu import (BF16_ATOL, BF16_RTOL, F32_ATOL, assert_close, decode_kernel,
+                        prefill_weight_rounding)
 
 pytestmark = pytest.mark.gpu
 
@@ -192,8 +193,7 @@ def test_fuzz_portable_shapes(cuda_device, seed):
     hq = hkv * g
     dtype = torch.float32 if rng.random() < 0.4 else torch.bfloat16
     kc, vc, bt, gen = _pool(rng, hkv, d, bs, lens, dtype)
-    tma = dtype == torch.bfloat16 and d in (64, 128) and (bs == 8 or bs % 16 == 0)
-    assert pa.decode_path(hq, kc) == (1 if tma else 0)
+    assert pa.decode_path(hq, kc) == decode_kernel(dtype, d, bs, g)
     sl = torch.tensor(lens, dtype=torch.int32)
     scale = float(rng.uniform(0.5, 1.5)) / math.sqrt(d)
     atol, rtol = (F32_ATOL, 0.0) if dtype == torch.float32 else (BF16_ATOL, BF16_RTOL)
