@@ -632,7 +632,7 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     constexpr int32_t kTilesPerCta = 2;
     a.scale_log2 = scale * kLog2e;
     // the tensor-core kernel takes its row maximum before scaling: scale >= 0
-    const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) &&
+    const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) && aligned(out, 16) &&
                       aligned(k_cache, 16) && aligned(v_cache, 16) && scale >= 0.f;
     cudaError_t err;
     if (fast) {
@@ -657,7 +657,9 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
                aligned(k_cache, 16) && aligned(v_cache, 16)) {
         err = dispatch_prefill_mma(cache, group, max_q_len, num_seqs, st, a);
         if (err == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
-    } else if (tiled_shape(cache) && aligned(k_cache, 16) && aligned(v_cache, 16)) {
+    } else if (tiled_shape(cache) && aligned(k_cache, 16) && aligned(v_cache, 16) &&
+               aligned(out, 16)) {
+        // (the output is stored four values at a time)
         err = dispatch_prefill_tiled(cache, group, max_q_len, num_seqs, st, a);
         if (err == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
     } else {

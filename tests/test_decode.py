@@ -488,3 +488,34 @@ def test_stale_workspace_contents_do_not_matter(cuda_device):
                      partition_tokens=512)
     assert_close(out2.cpu().double().numpy(), ref[:2], BF16_ATOL, BF16_RTOL, "reused workspace")
     assert pa.last_device_error() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,dtype", [(32, 8, 128, 16, torch.bfloat16),   # TMA
+                                              (64, 8, 96, 16, torch.bfloat16),    # mma.sync
+                                              (16, 8, 96, 16, torch.bfloat16),    # tiled
+                                              (8, 2, 64, 16, torch.float32)])     # tiled fp32
+@pytest.mark.parametrize("shift", ["q", "out"])
+def test_unaligned_query_or_output(cuda_device, hq, hkv, d, bs, dtype, shift):
+    """q or out one element off their allocation's alignment: each kernel
+    takes only the alignments it can use, the others fall back, and the
+    result is the oracle's either way."""
+    q, kc, vc, bt, sl = synthetic(hq, hkv, d, bs, (300, 77, 1000), dtype=dtype, seed=41)
+    scale = 1 / math.sqrt(d)
+    dev = cuda_device
+
+    def shifted(t):
+        buf = torch.zeros(t.numel() + 1, dtype=t.dtype, device=dev)
+        view = buf[1:].view(t.shape)
+        view.copy_(t.to(dev))
+        return view
+
+    qd = shifted(q) if shift == "q" else q.to(dev)
+    out = shifted(torch.zeros_like(q)) if shift == "out" else None
+    for part in (0, 64):
+        got = pa.decode(qd, kc.to(dev), vc.to(dev), bt.to(dev), sl.to(dev), int(sl.max()), scale,
+                        out=out, partition_tokens=part)
+        torch.cuda.synchronize()
+        atol, rtol = tolerance(dtype)
+        assert_close(got.cpu().double().numpy(), oracle.decode(q, kc, vc, bt, sl, scale), atol,
+                     rtol, f"shifted {shift}, partition {part}")
+    assert pa.last_device_error() == 0

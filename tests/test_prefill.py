@@ -265,3 +265,33 @@ def test_prefill_workload_full_size_sampled(cuda_device):
     got = out[torch.from_numpy(rows), torch.from_numpy(heads)].double().numpy()
     assert_close(got, ref[np.arange(48), heads], BF16_ATOL, BF16_RTOL, "prefill full size",
                  P_ROUND * wv[np.arange(48), heads])
+
+
+@pytest.mark.parametrize("d,dtype,hq,hkv", [(64, torch.float32, 8, 2), (96, torch.bfloat16, 8, 2),
+                                           (128, torch.bfloat16, 32, 8)])
+@pytest.mark.parametrize("shift", ["q", "out"])
+def test_unaligned_query_or_output(cuda_device, d, dtype, hq, hkv, shift):
+    """q or out one element off their allocation's alignment: each kernel
+    takes only the alignments it can use (16-byte copies and stores), and the
+    others fall back; the result is the oracle's either way."""
+    q, qs, kc, vc, bt, sl = case(hq, hkv, d, 16, (200, 90), (70, 90), dtype=dtype, seed=31)
+    scale = 1 / math.sqrt(d)
+    dev = cuda_device
+
+    def shifted(t):
+        buf = torch.zeros(t.numel() + 1, dtype=t.dtype, device=dev)
+        view = buf[1:].view(t.shape)
+        view.copy_(t.to(dev))
+        return view
+
+    qd = shifted(q) if shift == "q" else q.to(dev)
+    out = shifted(torch.zeros_like(q)) if shift == "out" else None
+    got = pa.prefill(qd, qs.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), sl.to(dev),
+                     int((qs[1:] - qs[:-1]).max()), int(sl.max()), scale, out=out)
+    torch.cuda.synchronize()
+    args = (q, qs, kc, vc, bt, sl, scale)
+    atol, rtol = tolerance(dtype)
+    extra = prefill_weight_rounding(*args) if dtype == torch.bfloat16 else None
+    assert_close(got.cpu().double().numpy(), oracle.prefill(*args), atol, rtol,
+                 f"shifted {shift}", extra)
+    assert pa.last_device_error() == 0
