@@ -96,6 +96,7 @@ def test_fast_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens):
     (16, 8, 256, 16, (700, 300), (500, 300), torch.bfloat16),    # Gemma-like D=256, G=2: mma.sync
     (12, 4, 160, 5, (333, 64), (200, 1), torch.bfloat16),        # D=160, B=5, a decode row
     (32, 32, 80, 16, (257, 99), (257, 33), torch.bfloat16),      # D=80 MHA: 64 tokens a tile
+    (160, 2, 96, 16, (90, 20), (90, 5), torch.bfloat16),         # mma.sync, G=80: two CTAs per kv head
 ])
 def test_portable_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens, dtype):
     """The kernels for the shapes the tcgen05 kernel does not take: mma.sync
