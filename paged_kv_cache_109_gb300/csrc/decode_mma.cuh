@@ -10,7 +10,7 @@
 //
 // One CTA of four warps per (partition, kv head x sub-group of 16 query
 // heads, sequence).  Warp w takes the partition's 16-token chunks w, w + 4,
-// ... through its own three-stage ring.  Each token's K row and V row is one
+// ... through its own two-stage ring.  Each token's K row and V row is one
 // bulk copy (lane r copies row r's K, lane 16 + r its V), so blocks of any
 // size work and every row can be padded by 16 bytes: the eight rows an
 // ldmatrix reads then fall in eight bank groups.  A stage's copies are
@@ -30,7 +30,11 @@ namespace pa {
 constexpr int kMmaWarps = 4;
 constexpr int kMmaThreads = 32 * kMmaWarps;
 constexpr int kMmaChunk = 16;     // tokens per chunk
-constexpr int kMmaStages = 3;     // chunks per warp in shared memory
+// Chunks per warp in shared memory.  Two, with launch bounds of three CTAs
+// per SM: the kernel is latency-bound, and three stages held it to two CTAs
+// per SM (0.43-0.45 against 0.52-0.55 of the copy peak at G = 16, D = 112 and
+// G = 5, D = 96).
+constexpr int kMmaStages = 2;
 constexpr int kMmaMaxDim = 128;
 
 // Dynamic shared memory: the warps' rings, reused at the end for the
@@ -43,7 +47,7 @@ inline size_t decode_mma_smem_bytes(int32_t head_dim) {
 }
 
 template <bool G16>
-__global__ void __launch_bounds__(kMmaThreads)
+__global__ void __launch_bounds__(kMmaThreads, 3)
 decode_mma_kernel(const DecodeArgs a) {
     constexpr int KS = kMmaMaxDim / 16;   // k steps of S (at most)
     constexpr int DT = kMmaMaxDim / 8;    // n-tiles of acc (at most)
