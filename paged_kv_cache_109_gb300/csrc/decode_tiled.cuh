@@ -45,7 +45,7 @@ constexpr int kTiledThreads = 32 * kTiledWarps;
 constexpr int kTiledHeads = 8;        // query heads per CTA
 // Chunks per warp in shared memory.  Two, so that more CTAs fit on an SM:
 // the copy in flight during a chunk's arithmetic keeps HBM busy as long as
-// enough warps are resident (a third buffer cost a quarter of the throughput).
+// enough warps are resident (a third buffer cost 14-22% of the throughput).
 constexpr int kTiledStages = 2;
 constexpr int kTiledMaxChunk = 16;
 constexpr int kTiledMaxIds = 512;     // table entries of a partition held in shared memory
