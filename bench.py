@@ -885,7 +885,8 @@ def run_reference(args, rank):
             "ms_per_step": round(1e3 * cpu["seconds"] / cpu["steps"], 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload],
-                                            "name": args.workload},
+                                            "name": args.workload,
+                                            "overrides": overrides_json(args) or None},
             "cpu_baseline": cpu,
             "e2e": {"value": round(cpu["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
