@@ -3,8 +3,11 @@
 the whole batch (every row of the hot path), on synthetic inputs resident in
 HBM.  Prints one JSON line.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mha|gqa|long|cb]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long|mha|gqa|cb|...]
                     [--impl ours|reference] [--partition P]
+
+The default workload is the long-context GQA batch (4 x 131072 tokens, the
+largest single-GPU case, 2 GiB of K/V per decode).
 
 Metric: paged-decode KV GB/s = algorithmic bytes of the step / step time;
 also % of the measured HBM peak and decode tokens/s per layer (sequences
@@ -34,7 +37,11 @@ from paged_kv_cache_109_gb300 import workloads  # noqa: E402
 
 METRIC = "paged decode KV GB/s and % of GB300 HBM peak; decode tokens/s per layer"
 L2_BYTES = 129 * 1024 * 1024
-DEC_SAMPLE = 8          # decode calls bracketed by events: every 8th step
+DEC_SAMPLE = 8          # prefill / copy calls bracketed by events: every 8th step
+ROOF_MIN_CALLS = 200    # the roofline block: at least this many back-to-back decode calls
+ROOF_MIN_MS = 250.0     # ... and at least this long (several clock samples)
+ROOF_SAMPLED = 50       # isolated decode calls, each between its own events (quantiles)
+ROOF_STEP_SLACK = 1.02  # self-check: per-call time <= ms_per_step x this
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0     # GB300 HBM3e nominal, reported beside the measured denominator
 F32_BOUND = 1e-5             # fp32 outputs: max abs error against the fp64 oracle
@@ -383,19 +390,19 @@ def run_ours(args, rank, world, device):
     outs = [torch.empty_like(d["q"]) for d in dsteps]
     stream = torch.cuda.current_stream(device)
 
-    def step(k, ev=None):
+    def decode(k):
+        d = dsteps[k]
+        pa.decode(d["q"], kc, vc, d["block_tables"], d["seq_lens"], maxlens[k], wl.scale,
+                  out=outs[k], workspace=ws, partition_tokens=part)
+
+    def step(k):
         d = dsteps[k]
         if args.positions:
             pa.write_kv_positions(d["k_new"], d["v_new"], d["seq_ids"], d["positions"],
                                   d["block_tables"], kc, vc)
         else:
             pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
-        if ev is not None:
-            ev[0].record(stream)
-        pa.decode(d["q"], kc, vc, d["block_tables"], d["seq_lens"], maxlens[k], wl.scale,
-                  out=outs[k], workspace=ws, partition_tokens=part)
-        if ev is not None:
-            ev[1].record(stream)
+        decode(k)
 
     for w in range(args.warmup):
         step(w % nsteps_wl)
@@ -403,13 +410,10 @@ def run_ours(args, rank, world, device):
     if pa.last_device_error() != 0:
         raise RuntimeError("device error flag raised during warm-up")
 
+    # The step loop: nothing between the steps' kernels, exactly as a user's
+    # loop would issue them (an event between two kernels would stop the
+    # programmatic-launch overlap).
     K = args.steps
-    # The decode call is bracketed by events on every DEC_SAMPLE-th step only:
-    # an event between two kernels stops the programmatic-launch overlap, so
-    # the other steps run exactly as a user's loop would.
-    sampled = list(range(0, K, DEC_SAMPLE))
-    dec_ev = {it: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for it in sampled}
     rank_barrier()
     torch.cuda.synchronize(device)
     with ClockSampler(device.index or 0) as clocks:
@@ -417,22 +421,24 @@ def run_ours(args, rank, world, device):
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for it in range(K):
-            step(it % nsteps_wl, dec_ev.get(it))
+            step(it % nsteps_wl)
         end.record(stream)
         torch.cuda.synchronize(device)
     rank_barrier()
     total_ms = max_over_ranks(start.elapsed_time(end), device)
-    dec_ms = [dec_ev[it][0].elapsed_time(dec_ev[it][1]) for it in sampled]
     step_bytes_sum = sum(bytes_[it % nsteps_wl]["decode"] + bytes_[it % nsteps_wl]["write"]
                          for it in range(K))
-    dec_bytes_sum = sum(bytes_[it % nsteps_wl]["decode"] for it in sampled)
     seqs = wl.num_seqs * K
     value = world * step_bytes_sum / (total_ms / 1e3) / 1e9
-    dec_achieved = dec_bytes_sum / (sum(dec_ms) / 1e3) / 1e9
     peak, peak_kind = measured_peak()
     err = pa.last_device_error()
     if err != 0:
         raise RuntimeError(f"device error flag {err} raised in the timed region")
+
+    roof = time_decode_calls(decode, nsteps_wl, bytes_, device, stream, peak, peak_kind,
+                             total_ms / K)
+    if pa.last_device_error() != 0:
+        raise RuntimeError("device error flag raised in the roofline block")
 
     # end to end: host buffers, H2D of the step inputs and D2H of the output
     e2e = run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, world)
@@ -450,8 +456,6 @@ def run_ours(args, rank, world, device):
         cpu = time_oracle(wl, args.cpu_seconds, max_reps=100000, gpu_outs=outs,
                           one_core_s=min(5.0, args.cpu_seconds / 2))
     b0 = bytes_[0]
-    q10, _, _, _, _, _, _, _, q90 = statistics.quantiles(dec_ms, n=10) if len(dec_ms) > 1 \
-        else [dec_ms[0]] * 9
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
@@ -475,22 +479,80 @@ def run_ours(args, rank, world, device):
         "decode_tokens_per_s_per_layer": round(world * seqs / (total_ms / 1e3), 1),
         "bytes_per_step": {"unique_kv": b0["unique_kv"], "logical_kv": b0["logical_kv"],
                            "decode": b0["decode"], "write": b0["write"]},
-        "roofline": {"bound": "hbm", "kernel": "pa_decode call (partition kernel + merge)",
-                     "achieved": round(dec_achieved, 2), "peak": peak,
-                     "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
-                     "frac": round(dec_achieved / peak, 4),
-                     "traffic": None if overrides(args) else measured_traffic(args.workload),
-                     "decode_ms_median": round(statistics.median(dec_ms), 5),
-                     "decode_ms_p10": round(q10, 5), "decode_ms_p90": round(q90, 5),
-                     "timed_launches": len(dec_ms),
-                     "how": f"events around the pa_decode call on every {DEC_SAMPLE}th timed "
-                            "step (launch on the caller's stream)"},
+        "roofline": {**roof,
+                     "traffic": None if overrides(args) else measured_traffic(args.workload)},
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
     }
     return result
+
+
+def time_decode_calls(decode, nsteps, bytes_, device, stream, peak, peak_kind,
+                      ms_per_step) -> dict:
+    """The roofline figure of the pa_decode call (partition kernel + merge).
+
+    Block: at least ROOF_MIN_CALLS calls and ROOF_MIN_MS milliseconds issued
+    back to back on the caller's stream between one pair of CUDA events, with
+    nothing between the calls (programmatic-launch overlap intact); achieved =
+    the calls' algorithmic bytes / the block's time, so the mean call.  Clocks
+    are sampled over the block.  Then ROOF_SAMPLED isolated calls, each
+    between its own pair of events, give the median and p10/p90 of one call
+    (an event between calls stops the overlap, so these include the launch).
+    Self-check: the block's mean call must not be longer than a whole step
+    (write + decode) of the step loop, within ROOF_STEP_SLACK."""
+    # one call's time, to size the block
+    for c in range(3):
+        decode(c % nsteps)
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for c in range(10):
+        decode(c % nsteps)
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    est = a.elapsed_time(b) / 10
+    calls = max(ROOF_MIN_CALLS, math.ceil(ROOF_MIN_MS / max(est, 1e-3)))
+    calls = max_over_ranks(float(calls), device)      # every rank issues the same block
+    calls = int(calls)
+    rank_barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index or 0) as clocks:
+        a.record(stream)
+        for c in range(calls):
+            decode(c % nsteps)
+        b.record(stream)
+        torch.cuda.synchronize(device)
+    rank_barrier()
+    block_ms = max_over_ranks(a.elapsed_time(b), device)
+    block_bytes = sum(bytes_[c % nsteps]["decode"] for c in range(calls))
+    achieved = block_bytes / (block_ms / 1e3) / 1e9
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(ROOF_SAMPLED)]
+    for c, (e0, e1) in enumerate(evs):
+        e0.record(stream)
+        decode(c % nsteps)
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    one = [e0.elapsed_time(e1) for e0, e1 in evs]
+    q = statistics.quantiles(one, n=10)
+    mean_ms = block_ms / calls
+    return {"bound": "hbm", "kernel": "pa_decode call (partition kernel + merge)",
+            "achieved": round(achieved, 2), "peak": peak,
+            "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "timed_launches": calls, "block_ms": round(block_ms, 3),
+            "decode_ms_mean": round(mean_ms, 5),
+            "decode_ms_median": round(statistics.median(one), 5),
+            "decode_ms_p10": round(q[0], 5), "decode_ms_p90": round(q[-1], 5),
+            "sampled_calls": len(one),
+            "per_call_le_step": bool(mean_ms <= ms_per_step * ROOF_STEP_SLACK),
+            "clocks": clocks.summary(),
+            "how": f"{calls} pa_decode calls back to back on the caller's stream between "
+                   f"one pair of CUDA events (achieved = their algorithmic bytes / that "
+                   f"time); median and p10/p90 from {len(one)} isolated calls, each between "
+                   f"its own events"}
 
 
 def prefill_flops(wl) -> int:
@@ -892,12 +954,12 @@ def run_reference(args, rank):
                     "d2h_bytes_per_step": 0}}
 
 
-def main():
+def make_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="mha")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="long")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -915,6 +977,11 @@ def main():
     ap.add_argument("--head-dim", type=int, default=0,
                     help="head dim of a decode workload (other than 64 and 128: the "
                          "CUDA-core decode kernel)")
+    return ap
+
+
+def main():
+    ap = make_parser()
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -273,11 +273,16 @@ int32_t pa_decode_path(int32_t num_q_heads, const pa_cache_desc* cache);
  * the library, held by every GPU that loads libpa.so until the process exits.
  * The call allocates nothing itself.
  * - The first call on each device looks the array's device address up (with
- *   that device current) and caches it; make that first call before any
- *   stream capture.
- * - A request whose workspace (pa_decode_workspace_bytes with the same
- *   arguments) exceeds PA_NO_ALLOC_WORKSPACE_BYTES returns PA_ERR_WORKSPACE
- *   and launches nothing.
+ *   that device current) and caches it, with the id of the device's current
+ *   context, for the life of the process; make that first call before any
+ *   stream capture.  After a cudaDeviceReset the context, and with it the
+ *   array's address, changes: the next call notices the new context and looks
+ *   the address up again, so that call too must come before any capture.
+ * - A request of more than 65535 partitions (the longest sequence over the
+ *   partition size) returns PA_ERR_UNSUPPORTED, as pa_decode does.  A request
+ *   whose workspace (pa_decode_workspace_bytes with the same arguments)
+ *   exceeds PA_NO_ALLOC_WORKSPACE_BYTES returns PA_ERR_WORKSPACE.  Neither
+ *   launches anything.
  * - All calls on a device share the one array, which keeps the last call's
  *   contents.  Nothing in it needs to start at zero: every cell the merge reads
  *   is written earlier in the same call.  Calls whose execution overlaps on the

@@ -125,15 +125,17 @@ int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_le
     return (int32_t)p;
 }
 
-int32_t num_parts(int32_t max_seq_len, int32_t part) {
-    return std::max(1, (max_seq_len + part - 1) / part);
+// Partitions of the longest sequence, in 64-bit arithmetic (max_seq_len + part
+// overflows int32 near INT32_MAX).  The launch refuses more than 65535.
+int64_t num_parts(int32_t max_seq_len, int32_t part) {
+    return std::max<int64_t>(1, ((int64_t)max_seq_len + part - 1) / part);
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 size_t workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
                        int32_t part, const pa_cache_desc* c) {
-    const int32_t P = num_parts(max_seq_len, part);
+    const int64_t P = num_parts(max_seq_len, part);
     if (P <= 1) return 0;
     const size_t cells = (size_t)num_seqs * num_q_heads * P;
     return align256(cells * c->head_dim * sizeof(float)) + align256(cells * 2 * sizeof(float));

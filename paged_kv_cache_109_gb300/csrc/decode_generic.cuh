@@ -68,7 +68,7 @@ decode_generic_kernel(const DecodeArgs a) {
     const int32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t G = a.group, D = a.head_dim, Bs = a.block_size, P = a.part_tokens;
     const int32_t T = checked_len(a, i);
-    const int32_t nparts = (T + P - 1) / P;
+    const int32_t nparts = (int32_t)(((int64_t)T + P - 1) / P);
     const E* q = static_cast<const E*>(a.q);
     const E* kc = static_cast<const E*>(a.k_cache);
     const E* vc = static_cast<const E*>(a.v_cache);

@@ -71,7 +71,7 @@ decode_mma_kernel(const DecodeArgs a) {
     const int32_t g = blockIdx.y / a.sub_groups, sg = blockIdx.y - g * a.sub_groups;
     const int32_t G = min(16, a.group - sg * 16);           // this CTA's query heads
     const int32_t T = checked_len(a, i);
-    const int32_t nparts = (T + P - 1) / P;
+    const int32_t nparts = (int32_t)(((int64_t)T + P - 1) / P);
     const int64_t head0 = (int64_t)i * a.num_q_heads + (int64_t)g * a.group + sg * 16;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
     if (T == 0) {          // no visible token: zero output rows

@@ -164,7 +164,7 @@ decode_tiled_kernel(const DecodeArgs a) {
     const int32_t Bs = a.block_size, P = a.part_tokens;
     const int32_t H = min(kTiledHeads, a.group - sg * kTiledHeads);   // this CTA's heads
     const int32_t T = checked_len(a, i);
-    const int32_t nparts = (T + P - 1) / P;
+    const int32_t nparts = (int32_t)(((int64_t)T + P - 1) / P);
     const int64_t head0 = (int64_t)i * a.num_q_heads + (int64_t)g * a.group + sg * kTiledHeads;
     E* out = static_cast<E*>(a.out);
     if (T == 0) {          // no visible token: zero output rows

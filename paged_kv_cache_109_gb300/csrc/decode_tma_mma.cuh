@@ -156,7 +156,7 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
 
     const int32_t T = clamp_len(a, T_raw);
-    const int32_t nparts = (T + P - 1) / P;
+    const int32_t nparts = (int32_t)(((int64_t)T + P - 1) / P);
     if (T == 0) {
         if (p == 0)
             for (int32_t x = tid; x < G * D; x += C::kThreads)

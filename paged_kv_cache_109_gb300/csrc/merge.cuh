@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
     const int64_t pair = blockIdx.x;                  // sequence * Hq + head
     const int32_t i = (int32_t)(pair / a.num_q_heads);
     const int32_t T = checked_len(a, i);
-    const int32_t n = (T + a.part_tokens - 1) / a.part_tokens;
+    const int32_t n = (int32_t)(((int64_t)T + a.part_tokens - 1) / a.part_tokens);
     if (n <= 1) return;   // written directly by the partition kernel
     const int32_t tid = threadIdx.x;
     const int64_t cell0 = pair * a.max_parts;

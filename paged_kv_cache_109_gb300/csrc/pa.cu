@@ -497,8 +497,8 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     if (!map_step_arg(q) || !map_step_arg(block_tables) || !map_step_arg(seq_lens) ||
         !map_step_arg(out) || !device_memory(k_cache) || !device_memory(v_cache))
         return PA_ERR_INVALID_ARG;
-    const int32_t max_parts = num_parts(max_seq_len, part);
-    if (max_parts > 65535) return PA_ERR_UNSUPPORTED;
+    if (num_parts(max_seq_len, part) > 65535) return PA_ERR_UNSUPPORTED;
+    const int32_t max_parts = (int32_t)num_parts(max_seq_len, part);
     const size_t need = workspace_bytes(num_seqs, num_q_heads, max_seq_len, part, cache);
     if (need > 0 && (!workspace || workspace_bytes_given < need || !aligned(workspace, 256) ||
                      !device_memory(workspace)))
@@ -715,28 +715,65 @@ int32_t pa_last_device_error(void) {
 // a file-scope device variable, so every GPU that loads libpa.so holds it
 // until the process exits.  In host code the name g_no_alloc_workspace is
 // only a host-side stand-in, not a device address: the real address is looked
-// up once per device with cudaGetSymbolAddress and cached.
+// up with cudaGetSymbolAddress, with the device current, and cached per device
+// together with the id of the context it was found in.  A later call whose
+// current context differs (the device was reset, so the module was loaded
+// again and the array may have moved) looks it up again.
 
 static __device__ __align__(256) unsigned char g_no_alloc_workspace[PA_NO_ALLOC_WORKSPACE_BYTES];
 
 namespace pa {
 namespace {
 
-void* g_no_alloc_ptr[kMaxDevices] = {nullptr};
+struct NoAllocEntry {
+    void* ptr = nullptr;
+    unsigned long long ctx = 0;   // cuCtxGetId of the context ptr belongs to
+};
+NoAllocEntry g_no_alloc[kMaxDevices];
 std::mutex g_no_alloc_mutex;
 
+// Id of the calling thread's current context, 0 when none is current yet or
+// the driver entry points are unavailable.
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 // Device address of the static workspace for the current device, or nullptr
-// if the lookup failed.  Runs cudaGetSymbolAddress on the first use per device.
+// if the lookup failed.  Runs cudaGetSymbolAddress on the first use per device
+// and again whenever the current context is not the one the cached address
+// came from (or cannot be identified).
 void* no_alloc_workspace() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_no_alloc_mutex);
-    if (g_no_alloc_ptr[dev] == nullptr) {
+    NoAllocEntry& e = g_no_alloc[dev];
+    const unsigned long long ctx = current_context_id();
+    if (e.ptr == nullptr || ctx == 0 || ctx != e.ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_no_alloc_workspace) != cudaSuccess) return nullptr;
-        g_no_alloc_ptr[dev] = p;
+        e.ptr = p;
+        e.ctx = current_context_id();   // the lookup made the device's context current
     }
-    return g_no_alloc_ptr[dev];
+    return e.ptr;
 }
 
 }  // namespace
@@ -751,6 +788,13 @@ extern "C" pa_status pa_decode_no_alloc(const void* q, const void* k_cache, cons
     if (pa_decode_path(num_q_heads, cache) < 0 || num_seqs < 0 || max_seq_len < 0 ||
         partition_tokens < 0)
         return PA_ERR_INVALID_ARG;
+    // the partition count first: a request pa_decode would refuse for it is
+    // refused the same way here, before the workspace is sized
+    const int32_t part = partition_tokens > 0
+                             ? partition_tokens
+                             : pa::auto_partition(num_seqs, num_q_heads, max_seq_len, cache);
+    if (part <= 0) return PA_ERR_INVALID_ARG;
+    if (pa::num_parts(max_seq_len, part) > 65535) return PA_ERR_UNSUPPORTED;
     const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, max_seq_len,
                                                   partition_tokens, cache);
     if (need > PA_NO_ALLOC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;

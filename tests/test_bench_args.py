@@ -40,3 +40,13 @@ def test_decode_only_flags_are_refused_elsewhere():
         r = subprocess.run([sys.executable, "bench.py", "--workload", w, "--dtype", "f32"],
                            capture_output=True, text=True, cwd=ROOT)
         assert r.returncode != 0 and "decode workloads" in r.stderr
+
+
+def test_default_line_is_the_long_context_decode():
+    """With no flags the bench measures the long-context GQA batch (the
+    largest single-GPU workload, 2 GiB of K/V per decode)."""
+    args = bench.make_parser().parse_args([])
+    assert args.workload == "long" and args.gpus == 1 and args.warmup >= 3
+    assert "131072" in bench.WORKLOAD_TEXT[args.workload]
+    # the roofline block is long enough to be a per-call mean, not a sample
+    assert bench.ROOF_MIN_CALLS >= 200 and bench.ROOF_SAMPLED >= 20

@@ -4,9 +4,12 @@ during execution, or a process with a fixed memory budget).  It keeps the
 split-K workspace in a fixed array inside libpa.so instead of taking one from
 the caller.
 
-Checked through the C ABI against pa_decode with a caller-owned workspace, on
-two calls in a row (the second must not see stale data from the first), and
-for the size limit.  This file is collected last on purpose.
+Checked through the C ABI against pa_decode with a caller-owned workspace:
+the two run the same kernels on the same arguments, so the outputs must be
+equal bit for bit.  Three calls in a row (case 1, case 2, case 1 again) with
+different workspace layouts: the third call must reproduce the first exactly,
+whatever the second left in the shared array.  Also the size and partition
+limits.  This file is collected last on purpose.
 """
 import ctypes
 import math
@@ -15,7 +18,6 @@ import pytest
 import torch
 
 import paged_kv_cache_109_gb300 as pa
-from tests._gpu import BF16_ATOL, BF16_RTOL, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -56,27 +58,31 @@ def _no_alloc(f, q, kc, vc, bt, sl, max_len, part, out):
              out.data_ptr(), ctypes.byref(desc), torch.cuda.current_stream().cuda_stream)
 
 
-def test_no_alloc_matches_pa_decode_on_two_calls(cuda_device):
+def test_no_alloc_matches_pa_decode_on_calls_in_a_row(cuda_device):
     f = _fn(pa.load_library())
     cases = [(_case(cuda_device, 1, (3000, 17, 1, 900, 2049)), 256),
              (_case(cuda_device, 2, (40, 5000, 700)), 64)]
-    for (q, kc, vc, bt, sl), part in cases:
+    got = []
+    for (q, kc, vc, bt, sl), part in (cases[0], cases[1], cases[0]):
         max_len = int(sl.max())
         assert 0 < pa.decode_workspace_bytes(q.shape[0], q.shape[1], max_len, kc, part) <= LIMIT
         ref = pa.decode(q, kc, vc, bt, sl, max_len, partition_tokens=part)
         out = torch.full_like(q, float("nan"))
         assert _no_alloc(f, q, kc, vc, bt, sl, max_len, part, out) == pa.PA_OK
         torch.cuda.synchronize()
-        assert_close(out.double().cpu().numpy(), ref.double().cpu().numpy(), BF16_ATOL,
-                     BF16_RTOL, "no-alloc vs pa_decode")
+        assert torch.equal(out, ref), "no-alloc output differs from pa_decode's"
+        got.append(out)
+    # the replayed first case after the second left another layout in the array
+    assert torch.equal(got[2], got[0])
     assert pa.last_device_error() == 0
 
 
 def test_no_alloc_rejects_requests_beyond_its_array(cuda_device):
     f = _fn(pa.load_library())
     q, kc, vc, bt, sl = _case(cuda_device, 3, (64,))
-    # a shape whose workspace exceeds the fixed array: refused, nothing launched
-    huge_len = 1 << 20
+    # a shape whose workspace exceeds the fixed array (4096 partitions of 16
+    # tokens, within the grid's limit): refused, nothing launched
+    huge_len = 1 << 16
     need = pa.decode_workspace_bytes(1024, 32, huge_len, kc, 16)
     assert need > LIMIT
     out = torch.zeros_like(q)
@@ -84,5 +90,18 @@ def test_no_alloc_rejects_requests_beyond_its_array(cuda_device):
            1024, huge_len, 32, 0.1, 16, out.data_ptr(), ctypes.byref(pa.cache_desc(kc)),
            torch.cuda.current_stream().cuda_stream)
     assert st == pa.PA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert not out.any()
+
+
+def test_no_alloc_refuses_more_than_65535_partitions(cuda_device):
+    f = _fn(pa.load_library())
+    q, kc, vc, bt, sl = _case(cuda_device, 4, (64,))
+    out = torch.zeros_like(q)
+    # 2^31 - 1 tokens in 16-token partitions: far more partitions than a grid takes
+    st = f(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), (1 << 31) // 16,
+           sl.data_ptr(), 1, (1 << 31) - 1, 32, 0.1, 16, out.data_ptr(),
+           ctypes.byref(pa.cache_desc(kc)), torch.cuda.current_stream().cuda_stream)
+    assert st == pa.PA_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert not out.any()
