@@ -116,6 +116,26 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+template <typename E, int VEC>
+cudaError_t launch_merge_w(int warps, dim3 grid, cudaStream_t st, const DecodeArgs& a) {
+    switch (warps) {
+        case 2: return launch_pdl(merge_kernel<E, 2, VEC>, grid, dim3(64), 0, st, a);
+        case 4: return launch_pdl(merge_kernel<E, 4, VEC>, grid, dim3(128), 0, st, a);
+        default: return launch_pdl(merge_kernel<E, 8, VEC>, grid, dim3(256), 0, st, a);
+    }
+}
+
+// The merge launch of a call: one CTA per (sequence, query head), after the
+// partition kernel on the same stream (programmatic dependent launch).
+template <typename E>
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t st) {
+    const dim3 grid((unsigned)((int64_t)a.num_seqs * a.num_q_heads));
+    const int warps = merge_warps(a.max_parts);
+    return a.head_dim % 4 == 0 ? launch_merge_w<E, 4>(warps, grid, st, a)
+                               : launch_merge_w<E, 1>(warps, grid, st, a);
+}
+
+
 template <typename Kern>
 bool set_smem(Kern kern, size_t bytes) {
     if (bytes <= 48 * 1024) return true;
@@ -566,12 +586,8 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     }
     if (err != cudaSuccess) return PA_ERR_CUDA;
     if (max_parts > 1) {
-        const unsigned mblocks = (unsigned)((int64_t)num_seqs * num_q_heads);
-        const cudaError_t merr =
-            cache->dtype == PA_F32
-                ? launch_pdl(merge_kernel<float>, dim3(mblocks), dim3(kMergeThreads), 0, st, a)
-                : launch_pdl(merge_kernel<__nv_bfloat16>, dim3(mblocks), dim3(kMergeThreads), 0,
-                             st, a);
+        const cudaError_t merr = cache->dtype == PA_F32 ? launch_merge<float>(a, st)
+                                                        : launch_merge<__nv_bfloat16>(a, st);
         if (merr != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;

@@ -251,6 +251,26 @@ def test_many_partitions_merge(cuda_device, dtype, d, hq, hkv):
         assert_close(out.double().numpy(), ref, atol, rtol, f"partitions of {part}")
 
 
+@pytest.mark.parametrize("dtype,d,hq,hkv", [(torch.float32, 10, 4, 2),
+                                             (torch.float32, 256, 8, 2),
+                                             (torch.bfloat16, 96, 16, 2),
+                                             (torch.bfloat16, 160, 8, 8)])
+def test_merge_column_slabs_and_warp_counts(cuda_device, dtype, d, hq, hkv):
+    """The merge on head dims that are not a multiple of 4 (one column per
+    lane), wider than one 128-column slab, and at partition sizes whose
+    longest sequence needs 2, 4 and 8 merge warps, with short sequences
+    (fewer partitions than warps) in the same batch."""
+    q, kc, vc, bt, sl = synthetic(hq, hkv, d, 16, (2000, 40, 16 * 33, 16 * 65 + 1),
+                                  dtype=dtype, seed=21)
+    scale = 1 / math.sqrt(d)
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    atol, rtol = tolerance(dtype)
+    for part in (16, 32, 64):          # 125, 63 and 32 partitions in the longest sequence
+        out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=part)
+        assert_close(out.double().numpy(), ref, atol, rtol, f"partitions of {part}")
+    assert pa.last_device_error() == 0
+
+
 def test_relabelling_physical_blocks_changes_nothing(cuda_device):
     q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (500, 33, 1200), seed=3, num_blocks=200)
     scale = 1 / math.sqrt(128)
