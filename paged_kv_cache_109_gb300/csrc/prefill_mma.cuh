@@ -18,9 +18,8 @@
 // owns rows 16 w .. 16 w + 15:
 //   S = Q K^T               (ldmatrix of Q and K, fp32 accumulators)
 //   online softmax in base 2 on the S fragments (scale log2 e applied to S)
-//   O += P V                (P rounded to bf16 from the S registers, V by
+//   O += P V                (P from the S registers as bf16 hi + lo, V by
 //                            ldmatrix.trans)
-// as the tcgen05 kernel does, P is rounded to bf16 once.
 #pragma once
 
 #include "prefill_tiled.cuh"
@@ -212,14 +211,17 @@ prefill_mma_kernel(const PrefillArgs a) {
                 acc[nd][3] *= al[1];
             }
 
-            // O += P V, P from the S registers (two key n-tiles = one k step)
+            // O += P V, P from the S registers (two key n-tiles = one k step).
+            // P = hi + lo, both bf16 (the rounding error of hi rounded again):
+            // two products against the same V fragments keep about 16
+            // significant bits of each weight instead of 8.
 #pragma unroll
             for (int32_t kp = 0; kp < KC / 16; ++kp) {
-                uint32_t pf[4];
-                pf[0] = pack_bf16x2(s[2 * kp][0], s[2 * kp][1]);
-                pf[1] = pack_bf16x2(s[2 * kp][2], s[2 * kp][3]);
-                pf[2] = pack_bf16x2(s[2 * kp + 1][0], s[2 * kp + 1][1]);
-                pf[3] = pack_bf16x2(s[2 * kp + 1][2], s[2 * kp + 1][3]);
+                uint32_t pf[4], pl[4];
+                split_bf16x2(s[2 * kp][0], s[2 * kp][1], pf[0], pl[0]);
+                split_bf16x2(s[2 * kp][2], s[2 * kp][3], pf[1], pl[1]);
+                split_bf16x2(s[2 * kp + 1][0], s[2 * kp + 1][1], pf[2], pl[2]);
+                split_bf16x2(s[2 * kp + 1][2], s[2 * kp + 1][3], pf[3], pl[3]);
 #pragma unroll
                 for (int32_t dp = 0; dp < DMAX / 16; ++dp) {
                     if (dp < D / 16) {
@@ -229,6 +231,8 @@ prefill_mma_kernel(const PrefillArgs a) {
                                       b0, b1, b2, b3);
                         mma_bf16_16816(acc[2 * dp], pf, b0, b1);
                         mma_bf16_16816(acc[2 * dp + 1], pf, b2, b3);
+                        mma_bf16_16816(acc[2 * dp], pl, b0, b1);
+                        mma_bf16_16816(acc[2 * dp + 1], pl, b2, b3);
                     }
                 }
             }

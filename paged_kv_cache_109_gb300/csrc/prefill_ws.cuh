@@ -20,13 +20,17 @@
 //                S_t  = Q_t K^T   M128 x N KEYS, A and B from shared memory
 //                O_t += P_t V     M128 x N D, A = P_t from tensor memory
 //
-// Tensor memory per tile: S_t (KEYS fp32 columns) and O_t (D columns).  The
-// softmax writes P_t (bf16 pairs) over the first KEYS/2 columns of S_t, one
-// 64-key half at a time, and publishes each half.  Per key block kb the MMA
-// warp issues, for t = 0, 1: O_t += P_t(kb-1) V(kb-1) for keys 0-63 as soon
-// as that half is published (while the softmax computes keys 64-127), then
-// for keys 64-127, then S_t(kb) into the same columns (tcgen05 MMAs of one
-// thread run in issue order, so P_t is read before it is overwritten).  Each
+// Tensor memory per tile: S_t (KEYS fp32 columns) and O_t (D columns).  P is
+// taken as two bf16 parts, P = hi + lo (lo: the rounding error of hi, rounded
+// again), so P V keeps about 16 significant bits of each weight instead of
+// the 8 of one bf16 operand.  The softmax takes S_t one 64-key half at a time;
+// once a half's 64 columns are in registers, its hi parts (bf16 pairs) go to
+// the first 32 of them and its lo parts to the other 32, and the half is
+// published.  Per key block kb the MMA warp issues, for t = 0, 1: O_t +=
+// hi V + lo V for keys 0-63 of block kb - 1 as soon as that half is published
+// (while the softmax computes keys 64-127), then the same for keys 64-127,
+// then S_t(kb) into the same columns (tcgen05 MMAs of one thread run in issue
+// order, so P_t is read before it is overwritten).  Each
 // softmax warpgroup overlaps the other tile's tensor-core work, and with P
 // off shared memory the K/V ring holds enough blocks to hide the copies'
 // latency.
@@ -35,8 +39,8 @@
 // row's position (diagonal blocks only), take the half's maximum, p = 2^(s c
 // - m) with c = scale log2(e) and a lazily moved reference maximum m (it
 // moves only when the maximum exceeds it by more than 8, so O is rescaled
-// rarely, p <= 2^8 and O / l does not depend on m), accumulate l, store P.
-// O is divided by l at the end.
+// rarely, p <= 2^8 and O / l does not depend on m), accumulate l (from the
+// fp32 p), store hi and lo.  O is divided by l at the end.
 //
 // Synchronisation is by mbarriers only; every wait is bounded, and a timeout
 // raises PA_DEVERR_TIMEOUT and ends the role's work (the others then time
@@ -297,8 +301,8 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const uint32_t s_t = tmem + t * C::kTileCols;
                 if (kb > 0) {
                     // O_t += P_t(kb - 1) V(kb - 1) in two halves: keys 0-63 as soon
-                    // as softmax t publishes them, keys 64-127 after; P: 16 keys
-                    // = 8 columns per step
+                    // as softmax t publishes them, keys 64-127 after; each half
+                    // as hi V + lo V
 #pragma unroll
                     for (int32_t hf = 0; hf < 2; ++hf) {
                         if (!warp_wait(hf ? p_full(t) : p_half(t), (kb - 1) & 1)) {
@@ -307,11 +311,17 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         }
                         tc_fence_after();
                         if (leader) {
+                            // half hf: hi at columns 64 hf .. 64 hf + 31,
+                            // lo at the next 32; 16 keys = 8 columns per step
 #pragma unroll
-                            for (int32_t k = hf * 4; k < hf * 4 + 4; ++k)
-                                umma_bf16_ts(s_t + C::kOCol, s_t + k * 8,
-                                             vdesc + (uint64_t)(k * 128), kIdO,
-                                             (kb > 1 || k > 0) ? 1u : 0u);
+                            for (int32_t k = 0; k < 4; ++k)
+                                umma_bf16_ts(s_t + C::kOCol, s_t + hf * 64 + k * 8,
+                                             vdesc + (uint64_t)((hf * 4 + k) * 128), kIdO,
+                                             (kb > 1 || hf > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                            for (int32_t k = 0; k < 4; ++k)
+                                umma_bf16_ts(s_t + C::kOCol, s_t + hf * 64 + 32 + k * 8,
+                                             vdesc + (uint64_t)((hf * 4 + k) * 128), kIdO, 1u);
                             umma_commit(hf ? o_done(t) : o_half(t));
                         }
                         __syncwarp();
@@ -358,9 +368,9 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const bool full = key0 + C::kKeys - 1 <= pos;
             // Each 64-key half of S: load it, take its maximum, move this row's
             // reference m_ref if that maximum exceeds it by more than 8, p =
-            // 2^(s c - m_ref) (packed fp32 FMA and add), P -> tensor memory over
-            // the first 64 columns of S_t (half hh of P lands on columns of keys
-            // already read; P_t(kb - 1) V(kb - 1) ran before S_t(kb)), rescale O
+            // 2^(s c - m_ref) (packed fp32 FMA and add), P as hi + lo -> tensor
+            // memory over the half's own 64 columns of S_t (read by then;
+            // P_t(kb - 1) V(kb - 1) ran before S_t(kb)), rescale O
             // if the reference moved (once the P V it holds has finished), and
             // publish the half: the MMA warp starts O += P V on keys 0-63 while
             // keys 64-127 are still being computed.
@@ -396,7 +406,7 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const float ref = m_ref == -INFINITY ? 0.f : m_ref;
                     const float2 nm2 = make_float2(-ref, -ref);
                     float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                    uint32_t pk[32];
+                    uint32_t pk[32], plo[32];                 // hi and lo parts of P
 #pragma unroll
                     for (int32_t jj = 0; jj < 32; ++jj) {
                         const int32_t j = 2 * jj;
@@ -409,9 +419,12 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             pp.y = key0 + hh * 64 + j + 1 <= pos ? pp.y : 0.f;
                         }
                         rs[jj & 1] = __fadd2_rn(rs[jj & 1], pp);
-                        pk[jj] = pack_bf16x2(pp.x, pp.y);
+                        split_bf16x2(pp.x, pp.y, pk[jj], plo[jj]);
                     }
-                    tmem_st32_async(s_tm + hh * 32, pk);
+                    // this half's 64 columns of S are in registers: hi and lo
+                    // take them
+                    tmem_st32_async(s_tm + hh * 64, pk);
+                    tmem_st32_async(s_tm + hh * 64 + 32, plo);
                     l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
                     // the second half's scores load while this half is published
                     if (hh == 0) {

@@ -146,6 +146,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// Two fp32 -> bf16x2 pair (hi, lo) with x ~ hi + lo per element: hi is x
+// rounded to bf16, lo the rounding error x - hi rounded to bf16 again, so
+// hi + lo keeps about 16 significant bits of x.
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(x, y);
+    lo = pack_bf16x2(x - __uint_as_float(hi << 16), y - __uint_as_float(hi & 0xffff0000u));
+}
+
 }  // namespace pa
 
 namespace pa {

@@ -10,19 +10,6 @@ BF16_ATOL, BF16_RTOL = 3e-3, 1e-2     # bf16 path vs fp64 oracle on the same bf1
 F32_ATOL = 1e-5                        # fp32 path: max abs error
 
 
-# The tensor-core prefill multiplies P rounded to bf16 (the operand type of
-# its P V product) by V: each softmax weight w_j moves by at most 2^-9 w_j, so
-# an output moves by at most 2^-9 sum_j w_j |v_j| beyond the stated tolerance.
-P_ROUND = 2.0 ** -9
-
-
-def prefill_weight_rounding(q, query_start, k_cache, v_cache, block_tables, seq_lens, scale):
-    """Per output of the tensor-core prefill: 2^-9 sum_j w_j |v_j|, the oracle's
-    attention over |V|."""
-    return P_ROUND * oracle.prefill(q, query_start, k_cache, v_cache.abs(), block_tables,
-                                    seq_lens, scale)
-
-
 def assert_close(got, ref, atol, rtol, what="", extra=None):
     """|got - ref| <= atol + rtol |ref| (+ extra, per element, where given)."""
     got = np.asarray(got, dtype=np.float64)

@@ -10,8 +10,7 @@ import torch
 
 import oracle
 import paged_kv_cache_109_gb300 as pa
-from tests._gpu import (BF16_ATOL, BF16_RTOL, F32_ATOL, assert_close, decode_kernel,
-                        prefill_weight_rounding)
+from tests._gpu import BF16_ATOL, BF16_RTOL, F32_ATOL, assert_close, decode_kernel
 
 pytestmark = pytest.mark.gpu
 
@@ -107,10 +106,7 @@ def test_fuzz_prefill(cuda_device, seed):
     if dtype == torch.float32:                     # the portable kernel, fp32 throughout
         assert_close(out.cpu().double().numpy(), ref, F32_ATOL, 0.0, what)
     else:
-        # the tensor-core kernel (G <= 128) multiplies bf16 P
-        fast = g <= 128
-        extra = prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale) if fast else None
-        assert_close(out.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, what, extra)
+        assert_close(out.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, what)
     assert pa.last_device_error() == 0
 
 
@@ -210,10 +206,6 @@ def test_fuzz_portable_shapes(cuda_device, seed):
     outp = pa.prefill(qp.to(dev), qs.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), sl.to(dev),
                       max(qlens), max(lens), scale)
     torch.cuda.synchronize()
-    # the tensor-core prefill kernels (tcgen05, and mma.sync for bf16 head
-    # dims that are multiples of 16) multiply bf16 P
-    bf16_p = dtype == torch.bfloat16 and d % 16 == 0
-    extra = prefill_weight_rounding(qp, qs, kc, vc, bt, sl, scale) if bf16_p else None
     assert_close(outp.cpu().double().numpy(), oracle.prefill(qp, qs, kc, vc, bt, sl, scale),
-                 atol, rtol, "prefill " + what, extra)
+                 atol, rtol, "prefill " + what)
     assert pa.last_device_error() == 0

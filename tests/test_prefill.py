@@ -9,8 +9,7 @@ import torch
 import oracle
 import paged_kv_cache_109_gb300 as pa
 from paged_kv_cache_109_gb300 import workloads
-from tests._gpu import (BF16_ATOL, BF16_RTOL, P_ROUND, assert_close, prefill_weight_rounding,
-                        tolerance)
+from tests._gpu import BF16_ATOL, BF16_RTOL, assert_close, tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -77,8 +76,7 @@ def test_fast_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens):
     scale = 1 / math.sqrt(d)
     out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
     ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
-    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "prefill",
-                 prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale))
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "prefill")
     assert pa.last_device_error() == 0
 
 
@@ -107,11 +105,7 @@ def test_portable_prefill_matches_oracle(cuda_device, hq, hkv, d, bs, ctx, qlens
     out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
     ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
     atol, rtol = tolerance(dtype)
-    # bf16 head dims that are multiples of 16 take the mma.sync kernel, which
-    # (like the tcgen05 one) multiplies bf16 P
-    extra = (prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale)
-             if dtype == torch.bfloat16 and d % 16 == 0 else None)
-    assert_close(out.double().numpy(), ref, atol, rtol, "portable prefill", extra)
+    assert_close(out.double().numpy(), ref, atol, rtol, "portable prefill")
 
 
 def test_long_context_slides_the_table_window(cuda_device):
@@ -121,8 +115,7 @@ def test_long_context_slides_the_table_window(cuda_device):
     scale = 1 / math.sqrt(128)
     out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
     ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
-    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "long context",
-                 prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale))
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "long context")
 
 
 def test_decode_rows_agree_with_pa_decode(cuda_device):
@@ -151,13 +144,12 @@ def test_garbage_past_the_last_key_is_ignored(cuda_device):
     q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (37, 90), (5, 90), seed=6)
     scale = 1 / math.sqrt(128)
     ref = oracle.prefill(q, qs, kc, vc, bt, sl, scale)
-    extra = prefill_weight_rounding(q, qs, kc, vc, bt, sl, scale)
     for i, t in enumerate(sl.tolist()):
         last = int(bt[i, (t - 1) // 16])
         kc[last, :, t % 16:] = float("nan")
         vc[last, :, t % 16:] = float("inf")
     out = run(cuda_device, q, qs, kc, vc, bt, sl, scale)
-    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "nan tail", extra)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "nan tail")
 
 
 def test_query_longer_than_sequence_is_reported(cuda_device):
@@ -170,7 +162,7 @@ def test_query_longer_than_sequence_is_reported(cuda_device):
     assert pa.last_device_error() & pa.DEVERR_SEQ_LEN
     rest = (q[10:], torch.tensor([0, 20], dtype=torch.int32), kc, vc, bt[1:], sl[1:], 0.1)
     assert_close(out[10:].double().cpu().numpy(), oracle.prefill(*rest), BF16_ATOL, BF16_RTOL,
-                 "other sequence", prefill_weight_rounding(*rest))
+                 "other sequence")
 
 
 def test_prefill_workload_reduced(cuda_device):
@@ -187,17 +179,17 @@ def test_prefill_workload_reduced(cuda_device):
     oracle.write_kv(st.k_new, st.v_new, st.slot_mapping, kh, vh)
     args = (st.q, st.query_start, kh, vh, st.block_tables, st.seq_lens, wl.scale)
     assert_close(out.double().numpy(), oracle.prefill(*args), BF16_ATOL, BF16_RTOL,
-                 "prefill workload", prefill_weight_rounding(*args))
+                 "prefill workload")
 
 
 def test_negative_scale_takes_the_portable_kernel(cuda_device):
     """The tcgen05 kernel needs scale >= 0; a negative scale is computed by
-    the mma.sync kernel (bf16 P, as in the tcgen05 kernel)."""
+    the mma.sync kernel."""
     q, qs, kc, vc, bt, sl = case(32, 8, 128, 16, (150, 60), (40, 60), seed=8)
     out = run(cuda_device, q, qs, kc, vc, bt, sl, -0.05)
     args = (q, qs, kc, vc, bt, sl, -0.05)
     assert_close(out.double().numpy(), oracle.prefill(*args), BF16_ATOL, BF16_RTOL,
-                 "negative scale", prefill_weight_rounding(*args))
+                 "negative scale")
 
 
 @pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (4, 2, 8)])
@@ -212,8 +204,7 @@ def test_bad_table_entry_is_reported(cuda_device, hq, hkv, d):
     bad[0, 3] = kc.shape[0] + 5
     out = run(cuda_device, q, qs, kc, vc, bad, sl, 1 / math.sqrt(d))
     assert pa.last_device_error() & pa.DEVERR_TABLE_ENTRY
-    assert_close(out[100:].double().numpy(), ref, BF16_ATOL, BF16_RTOL, "other sequence",
-                 prefill_weight_rounding(*rest))
+    assert_close(out[100:].double().numpy(), ref, BF16_ATOL, BF16_RTOL, "other sequence")
 
 
 def test_prefill_from_pinned_host_arguments(cuda_device):
@@ -262,10 +253,8 @@ def test_prefill_workload_full_size_sampled(cuda_device):
     sl1 = torch.from_numpy((pos + 1).astype(np.int32))
     pairs = np.stack([np.arange(48), heads], axis=1)
     ref = oracle.decode(q1, wl.k_cache, wl.v_cache, bt1, sl1, wl.scale, pairs=pairs)
-    wv = oracle.decode(q1, wl.k_cache, wl.v_cache.abs(), bt1, sl1, wl.scale, pairs=pairs)
     got = out[torch.from_numpy(rows), torch.from_numpy(heads)].double().numpy()
-    assert_close(got, ref[np.arange(48), heads], BF16_ATOL, BF16_RTOL, "prefill full size",
-                 P_ROUND * wv[np.arange(48), heads])
+    assert_close(got, ref[np.arange(48), heads], BF16_ATOL, BF16_RTOL, "prefill full size")
 
 
 @pytest.mark.parametrize("d,dtype,hq,hkv", [(64, torch.float32, 8, 2), (96, torch.bfloat16, 8, 2),
@@ -292,7 +281,6 @@ def test_unaligned_query_or_output(cuda_device, d, dtype, hq, hkv, shift):
     torch.cuda.synchronize()
     args = (q, qs, kc, vc, bt, sl, scale)
     atol, rtol = tolerance(dtype)
-    extra = prefill_weight_rounding(*args) if dtype == torch.bfloat16 else None
     assert_close(got.cpu().double().numpy(), oracle.prefill(*args), atol, rtol,
-                 f"shifted {shift}", extra)
+                 f"shifted {shift}")
     assert pa.last_device_error() == 0
