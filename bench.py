@@ -69,10 +69,12 @@ WORKLOAD_TEXT = {
 
 # ---- byte model ---------------------------------------------------------------
 
-def step_bytes(wl, k: int, split_traffic: bool = True) -> dict:
+def step_bytes(wl, k: int, split_traffic: bool = True, shared_prefix: bool = False) -> dict:
     """Algorithmic bytes of step k (see the design notes for the model).
     With ``split_traffic`` the split-K partial write + read of the library's
-    automatic partition size is included (asks libpa.so for that size)."""
+    automatic partition size is included (asks libpa.so for that size); with
+    ``shared_prefix`` the partials of the shared-prefix decode (every group
+    member writes its group's prefix partitions and its own)."""
     st = wl.steps[k]
     e = wl.elem_bytes
     row = wl.head_dim * e
@@ -95,8 +97,18 @@ def step_bytes(wl, k: int, split_traffic: bool = True) -> dict:
         import paged_kv_cache_109_gb300 as pa
         ws = pa.decode_workspace_bytes(n, hq, int(lens.max()), wl.k_cache, 0)
         part = pa.decode_partition_tokens(n, hq, int(lens.max()), wl.k_cache)
+        member_pk = {}
+        if shared_prefix:
+            for members, blocks in wl.prefix_groups:
+                for i in members:
+                    member_pk[i] = blocks * bs
         # each split sequence writes and re-reads (D + 2) floats per partition and head
-        for t in lens.tolist():
+        for i, t in enumerate(lens.tolist()):
+            if i in member_pk:
+                pk = member_pk[i]
+                parts = -(-pk // part) + -(-max(0, t - pk) // part)
+                split += 2 * parts * hq * (wl.head_dim + 2) * 4
+                continue
             parts = -(-t // part)
             if parts > 1:
                 split += 2 * parts * hq * (wl.head_dim + 2) * 4
@@ -381,10 +393,16 @@ def run_ours(args, rank, world, device):
         dsteps.append({k: getattr(st, k).to(device) for k in
                        ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens",
                         "seq_ids", "positions")})
-    bytes_ = [step_bytes(wl, k) for k in range(nsteps_wl)]
+    # groups sharing leading blocks: the shared-prefix decode reads them once
+    shared = bool(wl.prefix_groups) and not args.no_shared_prefix
+    groups = pa.prefix_groups(wl.prefix_groups, wl.num_seqs, device) if shared else None
+    bytes_ = [step_bytes(wl, k, shared_prefix=shared) for k in range(nsteps_wl)]
     maxlens = [int(st.seq_lens.max()) for st in wl.steps]
     part = args.partition or 0
-    ws_need = max(pa.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, m, kc, part)
+    ws_need = max(pa.decode_shared_prefix_workspace_bytes(wl.num_seqs, wl.num_q_heads, m,
+                                                          groups.max_prefix_blocks, kc, part)
+                  if shared else
+                  pa.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, m, kc, part)
                   for m in maxlens)
     ws = torch.empty(max(ws_need, 256), dtype=torch.uint8, device=device)
     outs = [torch.empty_like(d["q"]) for d in dsteps]
@@ -392,8 +410,13 @@ def run_ours(args, rank, world, device):
 
     def decode(k):
         d = dsteps[k]
-        pa.decode(d["q"], kc, vc, d["block_tables"], d["seq_lens"], maxlens[k], wl.scale,
-                  out=outs[k], workspace=ws, partition_tokens=part)
+        if shared:
+            pa.decode_shared_prefix(d["q"], kc, vc, d["block_tables"], d["seq_lens"],
+                                    maxlens[k], groups, wl.scale, out=outs[k], workspace=ws,
+                                    partition_tokens=part)
+        else:
+            pa.decode(d["q"], kc, vc, d["block_tables"], d["seq_lens"], maxlens[k], wl.scale,
+                      out=outs[k], workspace=ws, partition_tokens=part)
 
     def step(k):
         d = dsteps[k]
@@ -441,14 +464,15 @@ def run_ours(args, rank, world, device):
         raise RuntimeError("device error flag raised in the roofline block")
 
     # end to end: host buffers, H2D of the step inputs and D2H of the output
-    e2e = run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, world)
+    e2e = run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, world,
+                  shared)
 
     launches_per_step = []
     for k in range(nsteps_wl):
         n = 1 if wl.steps[k].slot_mapping.numel() else 0
         n += 1
         need = pa.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, maxlens[k], kc, part)
-        n += 1 if need else 0
+        n += 1 if need or shared else 0                # the merge
         launches_per_step.append(n)
     launches = sum(launches_per_step[it % nsteps_wl] for it in range(K))
     cpu = None
@@ -466,6 +490,14 @@ def run_ours(args, rank, world, device):
                    "overrides": overrides_json(args) or None,
                    "write": "device slots from (seq, position)" if args.positions
                             else "slot_mapping",
+                   "decode": ("pa_decode_shared_prefix, automatic mode (%s): %d group(s), "
+                              "%s shared blocks"
+                              % ("shared blocks read once" if pa.decode_shared_prefix_mode(
+                                     wl.num_q_heads, groups.max_prefix_blocks, kc) == 1
+                                 else "plain decode: reading them once would not pay here",
+                                 len(wl.prefix_groups),
+                                 "/".join(str(b) for _, b in wl.prefix_groups))
+                              if shared else "pa_decode"),
                    "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
                    "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                    "block_size": wl.block_size, "max_seq_len": max(maxlens),
@@ -858,25 +890,40 @@ def pipelined_steps(host, outs_like, launch, K, device, stream):
     return max_over_ranks(s.elapsed_time(e), device)
 
 
-def run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, world=1):
+def run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, world=1,
+            shared=False):
     """Same step through the public API from pinned host buffers: the step's
-    inputs (q, new K/V, slots, tables, lengths) packed in one page-locked
-    buffer cross in one H2D copy; write + decode; the output returns in one
-    D2H copy (pipelined as in pipelined_steps)."""
+    inputs (q, new K/V, slots, tables, lengths, and the shared-prefix groups
+    when used) packed in one page-locked buffer cross in one H2D copy; write +
+    decode; the output returns in one D2H copy (pipelined as in
+    pipelined_steps)."""
     names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens")
+    gnames = ("seq_group", "member_start", "members", "prefix_blocks")
+    hgroups = pa.prefix_groups(wl.prefix_groups, wl.num_seqs) if shared else None
     host = []
     for st in wl.steps:
-        hbuf, hv = _packed({k: getattr(st, k) for k in names}, pinned=True)
-        for k in names:
-            hv[k].copy_(getattr(st, k))
+        src = {k: getattr(st, k) for k in names}
+        if shared:
+            src.update({k: getattr(hgroups, k) for k in gnames})
+        hbuf, hv = _packed(src, pinned=True)
+        for k, t in src.items():
+            hv[k].copy_(t)
         host.append((hbuf, hv))
     n = len(host)
     K = max(1, min(args.steps, 200))
 
     def launch(k, d, out):
         pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
-        pa.decode(d["q"], kc, vc, d["block_tables"], d["seq_lens"], maxlens[k], wl.scale,
-                  out=out, workspace=ws, partition_tokens=part)
+        if shared:
+            grp = pa.PrefixGroups(d["seq_group"], d["member_start"], d["members"],
+                                  d["prefix_blocks"], hgroups.max_group_size,
+                                  hgroups.max_prefix_blocks)
+            pa.decode_shared_prefix(d["q"], kc, vc, d["block_tables"], d["seq_lens"],
+                                    maxlens[k], grp, wl.scale, out=out, workspace=ws,
+                                    partition_tokens=part)
+        else:
+            pa.decode(d["q"], kc, vc, d["block_tables"], d["seq_lens"], maxlens[k], wl.scale,
+                      out=out, workspace=ws, partition_tokens=part)
 
     ms = pipelined_steps(host, [hv["q"] for _, hv in host], launch, K, device, stream)
     total = world * sum(bytes_[it % n]["decode"] + bytes_[it % n]["write"] for it in range(K))
@@ -969,6 +1016,9 @@ def make_parser() -> argparse.ArgumentParser:
     ap.add_argument("--num-blocks", type=int, default=0, help="smaller block pool (profiling)")
     ap.add_argument("--block-size", type=int, default=0,
                     help="block-size sweep: tokens per block (pool bytes kept constant)")
+    ap.add_argument("--no-shared-prefix", action="store_true",
+                    help="decode a workload with shared-prefix groups (gqa) with the plain "
+                         "pa_decode instead of pa_decode_shared_prefix")
     ap.add_argument("--positions", action="store_true",
                     help="write with slots computed on the device from (seq, position)")
     ap.add_argument("--dtype", choices=["bf16", "f32"], default="bf16",

@@ -98,6 +98,7 @@ typedef struct {
 #define PA_DEVERR_SLOT        4u  /* a slot was >= num_blocks * block_size            */
 #define PA_DEVERR_TIMEOUT     8u  /* a pipeline wait gave up after its bound          */
 #define PA_DEVERR_BLOCK_PAIR 16u  /* a copy pair named a block outside its cache       */
+#define PA_DEVERR_GROUP      32u  /* a shared-prefix group, member or length out of range */
 
 /*
  * pa_write_kv -- cache write through slot_mapping.
@@ -213,6 +214,77 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     const pa_cache_desc* cache, void* stream);
 
 /*
+ * pa_decode_shared_prefix -- pa_decode for a batch in which groups of
+ * sequences share their leading blocks: a common prompt prefix held once and
+ * referenced by several block tables ("vLLM source walkthrough: PagedAttention
+ * and Continuous Batching" §1.6: blocks with ref_cnt > 1 shared by sequences
+ * with a common prefix; "PagedAttention engineering notes" (nxmr.cn) §4.1:
+ * forked sequences point at the same prompt blocks; "vLLM PagedAttention:
+ * from memory fragmentation to slot mapping" §5).  The result is pa_decode's
+ * over the same tables, within the same tolerance: one softmax over every
+ * visible key, now taken as the log-sum-exp merge of the shared blocks'
+ * partials with each member's own ("Efficient Memory Management for LLM
+ * Serving with PagedAttention" paper notes, blockwise softmax example).  What
+ * changes is the reads: the shared blocks are read once per kv head and tile
+ * of (member, query head) rows (16 rows, 8 for groups of up to 8 query heads
+ * per kv head) instead of once per member.
+ *
+ * Group k (0 <= k < num_groups) has the member sequences
+ * members[member_start[k] .. member_start[k+1]), each sequence in at most
+ * one group.  Its members' first prefix_blocks[k] table entries name the same
+ * physical blocks (the caller's promise, checked under PA_DEBUG).  A member
+ * may be shorter than the shared blocks: it sees only its own T_i keys.
+ *
+ * seq_group      device or pinned int32 [num_seqs]: k for a member of group k,
+ *                -1 for a sequence in no group.
+ * member_start   device or pinned int32 [num_groups + 1], from 0, non-decreasing.
+ * members        device or pinned int32 [member_start[num_groups]], sequence ids.
+ * prefix_blocks  device or pinned int32 [num_groups], each in [0, max_prefix_blocks].
+ * max_group_size    host bound of the groups' sizes (sizes the grid).
+ * max_prefix_blocks host bound of prefix_blocks, <= max_blocks_per_seq.
+ * workspace      device, >= pa_decode_shared_prefix_workspace_bytes(...) bytes,
+ *                256-byte aligned (never NULL when num_groups > 0 on the TMA
+ *                kernel's shapes: every member is merged).
+ * mode           PA_SHARED_ONCE: read the shared blocks once per row tile;
+ *                PA_SHARED_PLAIN: run the plain pa_decode over the same tables;
+ *                PA_SHARED_AUTO: once when a row tile holds m >= 2 members
+ *                (m = 8 rows, 16 for groups of more than 8 query heads per kv
+ *                head, over that group size) and max_prefix_blocks * B *
+ *                (1 - 1/m) >= 1024 tokens, plain otherwise.  The plain decode
+ *                reads each member's shared blocks, mostly from L2; reading
+ *                them once costs an extra merge per member, which pays only
+ *                when enough reads are saved (measured: a 512-token prefix at
+ *                4 query heads per kv head is 1.5% faster plain, a 4096-token
+ *                one 16% faster once; one member per tile is 13% faster plain).
+ * Other arguments as pa_decode.  A group id, member id or shared-block count
+ * out of range on the device is skipped and reported (PA_DEVERR_GROUP).
+ * Shapes that pa_decode_path does not send to kernel 1, and num_groups == 0,
+ * run the plain pa_decode over the same tables in every mode: same result.
+ */
+typedef enum { PA_SHARED_AUTO = 0, PA_SHARED_ONCE = 1, PA_SHARED_PLAIN = 2 } pa_shared_mode;
+
+/* 1 when pa_decode_shared_prefix with these arguments reads the shared
+ * blocks once per row tile, 0 when it runs the plain decode, < 0 for invalid
+ * arguments. */
+int32_t pa_decode_shared_prefix_mode(int32_t num_q_heads, int32_t max_prefix_blocks,
+                                     int32_t mode, const pa_cache_desc* cache);
+size_t pa_decode_shared_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                               int32_t max_seq_len, int32_t max_prefix_blocks,
+                                               int32_t partition_tokens,
+                                               const pa_cache_desc* cache);
+pa_status pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, int32_t num_seqs,
+                                  int32_t max_seq_len, int32_t num_q_heads, float scale,
+                                  int32_t partition_tokens, const int32_t* seq_group,
+                                  const int32_t* member_start, const int32_t* members,
+                                  const int32_t* prefix_blocks, int32_t num_groups,
+                                  int32_t max_group_size, int32_t max_prefix_blocks,
+                                  int32_t mode, void* out, void* workspace,
+                                  size_t workspace_bytes, const pa_cache_desc* cache,
+                                  void* stream);
+
+/*
  * pa_prefill -- multi-query (chunked prefill) paged attention with a causal
  * mask ("vLLM source walkthrough: PagedAttention and Continuous Batching"
  * §2.8: prefill rows and decode rows in one batch, long prompts in chunks;
@@ -238,8 +310,9 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * shapes (head_dim <= 256) and scales on a warp-level tensor-core kernel
  * (bf16, head_dim a multiple of 16, 16-byte aligned q and caches), else on
  * CUDA cores: a tiled kernel when the rows are whole 16-byte pieces and the
- * caches 16-byte aligned, else a generic one.  The tensor-core kernels round
- * the softmax weights to bf16 before P V.
+ * caches 16-byte aligned, else a generic one.  The tensor-core kernels take
+ * the softmax weights into P V as two bf16 parts (the weight rounded, and its
+ * rounding error rounded), about 16 significant bits.
  */
 pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t total_q,
                      int32_t max_q_len, const void* k_cache, const void* v_cache,

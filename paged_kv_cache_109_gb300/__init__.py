@@ -21,13 +21,18 @@ from ._build import LIB as LIBRARY_PATH
 from ._build import build
 from .block_pool import BlockPool, SharedTailWrite
 
-__all__ = ["write_kv", "write_kv_positions", "copy_blocks", "decode", "prefill", "decode_workspace_bytes", "decode_partition_tokens",
+__all__ = ["write_kv", "write_kv_positions", "copy_blocks", "decode", "decode_shared_prefix",
+           "prefix_groups", "PrefixGroups", "decode_shared_prefix_workspace_bytes",
+           "decode_shared_prefix_mode", "prefill",
+           "decode_workspace_bytes", "decode_partition_tokens",
            "decode_path", "last_device_error", "PaError", "build", "BlockPool",
            "SharedTailWrite", "LIBRARY_PATH", "load_library", "CacheDesc"]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
 PA_F32, PA_BF16 = 0, 1
 DEVERR_TABLE_ENTRY, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_BLOCK_PAIR = 1, 2, 4, 8, 16
+DEVERR_GROUP = 32
+SHARED_AUTO, SHARED_ONCE, SHARED_PLAIN = 0, 1, 2
 
 
 class CacheDesc(ctypes.Structure):
@@ -72,6 +77,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.pa_decode.argtypes = [P, P, P, P, I32, P, I32, I32, I32, ctypes.c_float, I32, P, P, SZ,
                               DP, P]
     lib.pa_decode.restype = ctypes.c_int
+    lib.pa_decode_shared_prefix_workspace_bytes.argtypes = [I32, I32, I32, I32, I32, DP]
+    lib.pa_decode_shared_prefix_workspace_bytes.restype = SZ
+    lib.pa_decode_shared_prefix.argtypes = [P, P, P, P, I32, P, I32, I32, I32, ctypes.c_float,
+                                            I32, P, P, P, P, I32, I32, I32, I32, P, P, SZ, DP,
+                                            P]
+    lib.pa_decode_shared_prefix_mode.argtypes = [I32, I32, I32, DP]
+    lib.pa_decode_shared_prefix_mode.restype = I32
+    lib.pa_decode_shared_prefix.restype = ctypes.c_int
     lib.pa_decode_path.argtypes = [I32, DP]
     lib.pa_decode_path.restype = I32
     lib.pa_status_str.argtypes = [ctypes.c_int]
@@ -252,6 +265,112 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int,
         _ptr(seq_lens), n, max_seq_len, hq, float(scale), partition_tokens, _ptr(out),
         _ptr(workspace), ws_bytes, ctypes.byref(desc), _stream(stream))
     _check(st, "pa_decode")
+    return out
+
+
+class PrefixGroups:
+    """The groups of a shared-prefix decode as the C ABI takes them: int32
+    tensors ``seq_group`` [num_seqs] (group of each sequence, -1 for none),
+    ``member_start`` [num_groups + 1], ``members`` and ``prefix_blocks``
+    [num_groups], with the host bounds ``max_group_size`` and
+    ``max_prefix_blocks``."""
+
+    def __init__(self, seq_group, member_start, members, prefix_blocks, max_group_size: int,
+                 max_prefix_blocks: int):
+        self.seq_group = seq_group
+        self.member_start = member_start
+        self.members = members
+        self.prefix_blocks = prefix_blocks
+        self.max_group_size = int(max_group_size)
+        self.max_prefix_blocks = int(max_prefix_blocks)
+
+    @property
+    def num_groups(self) -> int:
+        return int(self.prefix_blocks.numel())
+
+    def to(self, device) -> "PrefixGroups":
+        return PrefixGroups(self.seq_group.to(device), self.member_start.to(device),
+                            self.members.to(device), self.prefix_blocks.to(device),
+                            self.max_group_size, self.max_prefix_blocks)
+
+
+def prefix_groups(groups, num_seqs: int, device=None) -> PrefixGroups:
+    """PrefixGroups from a list of (member sequence ids, shared leading
+    blocks), e.g. ``BlockPool.shared_prefix_groups``; groups of fewer than
+    two members are dropped."""
+    groups = [(list(map(int, m)), int(b)) for m, b in groups if len(m) >= 2]
+    seq_group = [-1] * num_seqs
+    starts, members, blocks = [0], [], []
+    for k, (mem, b) in enumerate(groups):
+        for i in mem:
+            seq_group[i] = k
+        members += mem
+        starts.append(len(members))
+        blocks.append(b)
+
+    def i32(x):
+        return torch.tensor(x, dtype=torch.int32, device=device)
+
+    return PrefixGroups(i32(seq_group), i32(starts), i32(members), i32(blocks),
+                        max((len(m) for m, _ in groups), default=0),
+                        max(blocks, default=0))
+
+
+def decode_shared_prefix_workspace_bytes(num_seqs: int, num_q_heads: int, max_seq_len: int,
+                                         max_prefix_blocks: int, k_cache,
+                                         partition_tokens: int = 0) -> int:
+    desc = k_cache if isinstance(k_cache, CacheDesc) else cache_desc(k_cache)
+    return int(load_library().pa_decode_shared_prefix_workspace_bytes(
+        num_seqs, num_q_heads, max_seq_len, max_prefix_blocks, partition_tokens,
+        ctypes.byref(desc)))
+
+
+def decode_shared_prefix_mode(num_q_heads: int, max_prefix_blocks: int, k_cache,
+                              mode: int = SHARED_AUTO) -> int:
+    """1 when decode_shared_prefix reads the shared blocks once per row tile
+    for these arguments, 0 when it runs the plain decode."""
+    desc = k_cache if isinstance(k_cache, CacheDesc) else cache_desc(k_cache)
+    return int(load_library().pa_decode_shared_prefix_mode(num_q_heads, max_prefix_blocks,
+                                                           mode, ctypes.byref(desc)))
+
+
+def decode_shared_prefix(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int,
+                         groups: PrefixGroups, scale: float | None = None, out=None,
+                         workspace=None, partition_tokens: int = 0, mode: int = SHARED_AUTO,
+                         stream=None) -> torch.Tensor:
+    """``decode`` for a batch whose ``groups`` of sequences share leading
+    blocks: the same result, with each group's shared blocks read once per
+    kv head and row tile instead of once per member (``mode``: SHARED_ONCE,
+    SHARED_PLAIN, or SHARED_AUTO to choose by the expected saving)."""
+    _dev(k_cache, v_cache)
+    _dev_or_pinned(q, block_tables, seq_lens, groups.seq_group, groups.member_start,
+                   groups.members, groups.prefix_blocks)
+    for t in (block_tables, seq_lens, groups.seq_group, groups.member_start, groups.members,
+              groups.prefix_blocks):
+        if t.dtype != torch.int32:
+            raise ValueError("tables, lengths and group arrays must be int32")
+    desc = cache_desc(k_cache)
+    n, hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q, device=k_cache.device)
+    _dev_or_pinned(out)
+    need = decode_shared_prefix_workspace_bytes(n, hq, max_seq_len, groups.max_prefix_blocks,
+                                                desc, partition_tokens)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=k_cache.device)
+    if workspace is not None:
+        _dev(workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().pa_decode_shared_prefix(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), n, max_seq_len, hq, float(scale), partition_tokens,
+        _ptr(groups.seq_group), _ptr(groups.member_start), _ptr(groups.members),
+        _ptr(groups.prefix_blocks), groups.num_groups, groups.max_group_size,
+        groups.max_prefix_blocks, mode, _ptr(out), _ptr(workspace), ws_bytes,
+        ctypes.byref(desc), _stream(stream))
+    _check(st, "pa_decode_shared_prefix")
     return out
 
 

@@ -192,6 +192,30 @@ class BlockPool:
             rows.append(t + [-1] * (width - len(t)))
         return rows
 
+    def shared_prefix_groups(self, seqs: Sequence[Hashable]) -> list[tuple[list[int], int]]:
+        """Groups of the batch ``seqs`` whose tables start with the same
+        shared blocks, for the shared-prefix decode: a list of (member
+        positions in ``seqs``, leading blocks every member holds in common).
+        Sequences group by their first block when its reference count is
+        above one (a prefix added with ``prefix_of`` or a ``fork``); a
+        group's count is the longest run of leading entries all its members'
+        tables agree on.  A sequence alone in its group is left out."""
+        by_first: dict[int, list[int]] = {}
+        for idx, s in enumerate(seqs):
+            t = self.tables[s]
+            if t and self.ref_cnt[t[0]] > 1:
+                by_first.setdefault(t[0], []).append(idx)
+        groups = []
+        for members in by_first.values():
+            if len(members) < 2:
+                continue
+            rows = [self.tables[seqs[m]] for m in members]
+            k, n = 0, min(len(r) for r in rows)
+            while k < n and all(r[k] == rows[0][k] for r in rows):
+                k += 1
+            groups.append((members, k))
+        return groups
+
     # -- statistics ----------------------------------------------------------
     def unique_blocks(self) -> int:
         return sum(1 for c in self.ref_cnt if c > 0)

@@ -117,6 +117,49 @@ inline pa_status check_tables(const int32_t* tables, int32_t max_blocks, const i
     return PA_OK;
 }
 
+// Shared-prefix groups: member lists ordered from 0, within the host bounds,
+// every member a valid sequence in exactly one group whose seq_group entry
+// names it (and -1 for the other sequences), and every member's first
+// prefix_blocks table entries the same physical blocks as the group's first
+// member's.
+inline pa_status check_groups(const int32_t* tables, int32_t max_blocks, int32_t num_seqs,
+                              const int32_t* seq_group, const int32_t* member_start,
+                              const int32_t* members, const int32_t* prefix_blocks,
+                              int32_t num_groups, int32_t max_group_size,
+                              int32_t max_prefix_blocks, cudaStream_t st) {
+    std::vector<int32_t> tab, sg, ms, mem, pb;
+    if (!fetch(tab, tables, (size_t)num_seqs * max_blocks, st) ||
+        !fetch(sg, seq_group, (size_t)num_seqs, st) ||
+        !fetch(ms, member_start, (size_t)num_groups + 1, st) ||
+        !fetch(pb, prefix_blocks, (size_t)num_groups, st))
+        return PA_ERR_CUDA;
+    if (ms[0] != 0) return fail("member_start[0] is not 0 (group, start)", 0, ms[0]);
+    for (int32_t k = 0; k < num_groups; ++k) {
+        const int32_t cnt = ms[k + 1] - ms[k];
+        if (cnt < 0 || cnt > max_group_size)
+            return fail("group size outside [0, max_group_size] (group, size)", k, cnt);
+        if (pb[k] < 0 || pb[k] > max_prefix_blocks)
+            return fail("shared blocks outside [0, max_prefix_blocks] (group, blocks)", k, pb[k]);
+    }
+    if (!fetch(mem, members, (size_t)ms[num_groups], st)) return PA_ERR_CUDA;
+    std::vector<int32_t> owner((size_t)num_seqs, -1);
+    for (int32_t k = 0; k < num_groups; ++k) {
+        for (int32_t j = ms[k]; j < ms[k + 1]; ++j) {
+            const int32_t i = mem[j];
+            if (i < 0 || i >= num_seqs) return fail("member outside the batch (group, id)", k, i);
+            if (owner[i] >= 0) return fail("sequence in two groups (sequence, group)", i, k);
+            owner[i] = k;
+            for (int32_t b = 0; b < pb[k]; ++b)
+                if (tab[(size_t)i * max_blocks + b] != tab[(size_t)mem[ms[k]] * max_blocks + b])
+                    return fail("member's leading block differs from the group's (sequence, block)",
+                                i, b);
+        }
+    }
+    for (int32_t i = 0; i < num_seqs; ++i)
+        if (sg[i] != owner[i]) return fail("seq_group disagrees with the members (sequence, group)", i, sg[i]);
+    return PA_OK;
+}
+
 // Copy pairs inside both pools; no block is written twice, and inside one pool
 // no destination is also a source (the result would depend on the order).
 inline pa_status check_pairs(const int64_t* pairs, int32_t n, int32_t src_blocks,

@@ -39,7 +39,40 @@ struct DecodeArgs {
     int32_t max_parts;
     int32_t sub_groups;   // tensor-core kernel: CTAs per kv head, 16 query heads each
     float scale_log2;     // scale * log2(e)
+    // Shared-prefix decode (nullptr / 0 otherwise): group of each sequence
+    // (-1: none), the groups' member lists (CSR) and shared leading blocks.
+    const int32_t* seq_group;
+    const int32_t* member_start;
+    const int32_t* members;
+    const int32_t* prefix_blocks;
+    int32_t num_groups;
+    int32_t max_prefix_blocks;
+    int32_t prefix_ztiles;   // grid z per group taken by its prefix CTAs
+    int32_t prefix_z;        // num_groups * prefix_ztiles: z below this is a prefix CTA
 };
+
+// Shared leading blocks of group k, clamped to the host bound (an entry past
+// it is reported and read as 0).
+__device__ __forceinline__ int32_t group_prefix_blocks(const DecodeArgs& a, int32_t k) {
+    const int32_t b = a.prefix_blocks[k];
+    if (b < 0 || b > a.max_prefix_blocks) {
+        if (threadIdx.x == 0) raise_error(PA_DEVERR_GROUP);
+        return 0;
+    }
+    return b;
+}
+
+// Group of sequence i in a shared-prefix call (-1: none); an id outside
+// [0, num_groups) is reported and read as -1.
+__device__ __forceinline__ int32_t seq_group_of(const DecodeArgs& a, int32_t i) {
+    if (a.seq_group == nullptr) return -1;
+    const int32_t k = a.seq_group[i];
+    if (k >= a.num_groups) {
+        if (threadIdx.x == 0) raise_error(PA_DEVERR_GROUP);
+        return -1;
+    }
+    return k < 0 ? -1 : k;
+}
 
 // Effective length from a raw seq_lens value: clamps (and reports) lengths
 // the table or the host bound cannot cover.

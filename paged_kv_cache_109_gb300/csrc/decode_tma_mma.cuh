@@ -77,23 +77,33 @@ struct TmaMmaCfg {
     static size_t smem_bytes_max() { return smem_bytes(kMaxTableSlice, 1); }
 };
 
-template <int D, bool G16>
+template <int D, bool G16, bool CAS>
 __global__ void __launch_bounds__(128, PA_MIN_CTAS_PER_SM)
 decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
     using C = TmaMmaCfg<D, G16>;
     extern __shared__ uint8_t sm_raw[];
     __shared__ int s_fail;
+    // CAS (shared-prefix decode) only: per MMA row of a prefix CTA, its q (and
+    // output) row, -1 for none, and the keys of the prefix it sees
+    __shared__ int64_t s_qrow[CAS ? C::kRows : 1];
+    __shared__ int32_t s_lim[CAS ? C::kRows : 1];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
 
     // blockIdx.y = kv head g, sub-group sg: this CTA carries the group's
-    // query heads sg * 16 .. sg * 16 + G - 1
-    const int32_t p = blockIdx.x, g = blockIdx.y / a.sub_groups, i = blockIdx.z;
+    // query heads sg * 16 .. sg * 16 + G - 1.  With CAS, blockIdx.z below
+    // a.prefix_z is a prefix CTA: the shared leading blocks of one group of
+    // sequences, its rows (member, query head) pairs; the other CTAs run
+    // sequence blockIdx.z - a.prefix_z, a group member past its group's
+    // shared blocks.
+    const bool pre = CAS && (int32_t)blockIdx.z < a.prefix_z;
+    const int32_t p = blockIdx.x, g = blockIdx.y / a.sub_groups;
+    const int32_t i = CAS ? (int32_t)blockIdx.z - a.prefix_z : (int32_t)blockIdx.z;
     const int32_t sg = blockIdx.y - g * a.sub_groups;
     const int32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t grp = lane >> 2, tig = lane & 3;
-    const int32_t G = min(16, a.group - sg * 16);
+    const int32_t G = pre ? C::kRows : min(16, a.group - sg * 16);
     const int32_t BS = a.block_size;
     // B >= 16: a block is cpb = B/16 chunks.  B = 8: a chunk is two blocks,
     // loaded as two 8-row boxes (the 128-byte swizzle atom is 8 rows).
@@ -127,10 +137,58 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // copy.  CTAs of later partitions are often empty (short sequences in a
     // batch sized by max_seq_len): they read the length first and leave at
     // once when there is nothing to do.
-    const int32_t T_raw = a.seq_lens[i];
-    if (p > 0 && T_raw <= t0 && T_raw <= a.max_seq_len) return;
-    const int32_t slice = max(0, min((P + BS - 1) / BS, a.max_blocks - t0 / BS));
-    const int32_t* table = a.block_tables + (int64_t)i * a.max_blocks + t0 / BS;
+    // CAS: skip = tokens of the table row before this CTA's token 0 (a
+    // member's shared blocks), slot0 = its partitions' first workspace slot
+    // (after the group's prefix partitions), direct = may write out itself.
+    int32_t T_raw, skip = 0, slot0 = 0;
+    bool direct = true;
+    const int32_t* row = nullptr;
+    if (pre) {
+        direct = false;
+        const int32_t z = blockIdx.z, k = z / a.prefix_ztiles;
+        const int32_t rt = (z - k * a.prefix_ztiles) * a.sub_groups + sg;   // row tile
+        const int32_t ms = a.member_start[k], mc = a.member_start[k + 1] - ms;
+        const int32_t pk = group_prefix_blocks(a, k) * BS;
+        if (mc <= 0 || t0 >= pk) return;
+        if (tid < C::kRows) {
+            // MMA row tid = pair rt * kRows + tid of the group's (member, head)
+            // pairs, head fastest
+            const int32_t u = rt * C::kRows + tid, mi = u / a.group, h = u - mi * a.group;
+            int64_t qr = -1;
+            int32_t lim = 0;
+            if (mi < mc) {
+                const int32_t sq = a.members[ms + mi];
+                if (sq >= 0 && sq < a.num_seqs) {
+                    qr = (int64_t)sq * a.num_q_heads + (int64_t)g * a.group + h;
+                    lim = min(clamp_len(a, a.seq_lens[sq]), pk) - t0;   // keys of this partition
+                } else {
+                    raise_error(PA_DEVERR_GROUP);
+                }
+            }
+            s_qrow[tid] = qr;
+            s_lim[tid] = qr >= 0 ? max(0, min(lim, P)) : 0;
+        }
+        const int32_t first = a.members[ms];
+        row = a.block_tables + (int64_t)(first >= 0 && first < a.num_seqs ? first : 0) *
+                                   a.max_blocks;
+        T_raw = pk;
+        __syncthreads();
+    } else {
+        T_raw = a.seq_lens[i];
+        if (CAS) {
+            const int32_t k = seq_group_of(a, i);
+            if (k >= 0) {
+                const int32_t pk = group_prefix_blocks(a, k) * BS;
+                direct = false;
+                skip = pk;
+                slot0 = (int32_t)(((int64_t)pk + P - 1) / P);
+            }
+        }
+        if (p > 0 && T_raw - skip <= t0 && T_raw <= a.max_seq_len) return;
+        row = a.block_tables + (int64_t)i * a.max_blocks;
+    }
+    const int32_t slice = max(0, min((P + BS - 1) / BS, a.max_blocks - (skip + t0) / BS));
+    const int32_t* table = row + (skip + t0) / BS;
     constexpr int kIdsPerThread = (C::kMaxTableSlice + C::kThreads - 1) / C::kThreads;
     int32_t raw_ids[kIdsPerThread];
 #pragma unroll
@@ -142,9 +200,16 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint32_t qa[C::kKSteps][4];
     {
         const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-        const bool r0 = grp < G, r1 = G16 && (grp + 8) < G;
-        const __nv_bfloat16* q0 = q + (head0 + grp) * D;
-        const __nv_bfloat16* q1 = q + (head0 + grp + 8) * D;
+        bool r0 = grp < G, r1 = G16 && (grp + 8) < G;
+        int64_t qr0 = head0 + grp, qr1 = head0 + grp + 8;
+        if (pre) {
+            qr0 = s_qrow[grp];
+            qr1 = G16 ? s_qrow[grp + 8] : -1;
+            r0 = qr0 >= 0;
+            r1 = qr1 >= 0;
+        }
+        const __nv_bfloat16* q0 = q + (r0 ? qr0 : 0) * D;
+        const __nv_bfloat16* q1 = q + (r1 ? qr1 : 0) * D;
 #pragma unroll
         for (int ks = 0; ks < C::kKSteps; ++ks) {
             const int d0 = ks * 16 + 2 * tig;
@@ -155,17 +220,29 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
 
-    const int32_t T = clamp_len(a, T_raw);
+    // tokens of the row this CTA walks (a member: past its shared blocks)
+    const int32_t T = pre ? T_raw : max(0, clamp_len(a, T_raw) - skip);
     const int32_t nparts = (int32_t)(((int64_t)T + P - 1) / P);
     if (T == 0) {
-        if (p == 0)
+        if (p == 0 && direct)
             for (int32_t x = tid; x < G * D; x += C::kThreads)
                 out[head0 * D + x] = __float2bfloat16_rn(0.f);
         return;
     }
     if (p >= nparts) return;
 
-    const int32_t n = min(P, T - t0);
+    int32_t n = min(P, T - t0);
+    // a prefix CTA loads the keys up to its longest member's last one; each
+    // row masks the keys past its own member's length (rlim0 / rlim1)
+    int32_t rlim0 = n, rlim1 = n;
+    if (pre) {
+        int32_t most = 0;
+#pragma unroll
+        for (int r = 0; r < C::kRows; ++r) most = max(most, s_lim[r]);
+        n = min(n, most);
+        rlim0 = s_lim[grp];
+        rlim1 = G16 ? s_lim[grp + 8] : 0;
+    }
     const int32_t nblk = (n + BS - 1) / BS;
     const int32_t nchunk = (n + C::kChunk - 1) / C::kChunk;
 #pragma unroll
@@ -298,25 +375,33 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const bool valid = nt * 8 + 2 * tig + e < nvalid;
+                    // CAS: per row (a prefix CTA's rows end at their members'
+                    // lengths); otherwise one end for all rows
+                    const int32_t col = c * C::kChunk + nt * 8 + 2 * tig + e;
+                    const bool valid = CAS ? col < rlim0 : nt * 8 + 2 * tig + e < nvalid;
+                    const bool valid1 = CAS ? col < rlim1 : valid;
                     s[nt][e] = valid ? s[nt][e] * a.scale_log2 : -INFINITY;
                     mx0 = fmaxf(mx0, s[nt][e]);
                     if (G16) {
-                        s[nt][2 + e] = valid ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
+                        s[nt][2 + e] = valid1 ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
                         mx1 = fmaxf(mx1, s[nt][2 + e]);
                     }
                 }
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             const float mn0 = fmaxf(m0, mx0);
-            const float al0 = exp2f(m0 - mn0);
+            // CAS: a prefix row may have seen no key yet (m stays -inf, its
+            // weights are 0); the reference then is 0, not -inf - -inf
+            const float ref0 = CAS && mn0 == -INFINITY ? 0.f : mn0;
+            const float al0 = exp2f(m0 - ref0);
             m0 = mn0;
-            float al1 = 1.f;
+            float al1 = 1.f, ref1 = 0.f;
             if (G16) {
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
                 const float mn1 = fmaxf(m1, mx1);
-                al1 = exp2f(m1 - mn1);
+                ref1 = CAS && mn1 == -INFINITY ? 0.f : mn1;
+                al1 = exp2f(m1 - ref1);
                 m1 = mn1;
             }
             float rs0 = 0.f, rs1 = 0.f;
@@ -324,10 +409,10 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    s[nt][e] = exp2f(s[nt][e] - m0);
+                    s[nt][e] = exp2f(s[nt][e] - ref0);
                     rs0 += s[nt][e];
                     if (G16) {
-                        s[nt][2 + e] = exp2f(s[nt][2 + e] - m1);
+                        s[nt][2 + e] = exp2f(s[nt][2 + e] - ref1);
                         rs1 += s[nt][2 + e];
                     }
                 }
@@ -457,14 +542,19 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
             }
         }
-        if (nparts == 1) {
+        if (nparts == 1 && direct) {
             out[(head0 + h) * D + d] = __float2bfloat16_rn(L > 0.f ? A / L : 0.f);
         } else {
-            const int64_t cell = (head0 + h) * a.max_parts + p;
-            a.ws_acc[cell * D + d] = A;
-            if (d == 0) {
-                a.ws_ml[2 * cell] = M;
-                a.ws_ml[2 * cell + 1] = L;
+            // a prefix CTA's partials go to slot p of its rows' cells; a
+            // member's after its group's prefix slots
+            const int64_t qr = pre ? s_qrow[h] : head0 + h;
+            if (qr >= 0) {
+                const int64_t cell = qr * a.max_parts + slot0 + p;
+                a.ws_acc[cell * D + d] = A;
+                if (d == 0) {
+                    a.ws_ml[2 * cell] = M;
+                    a.ws_ml[2 * cell + 1] = L;
+                }
             }
         }
     }

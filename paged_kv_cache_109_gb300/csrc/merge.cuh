@@ -102,8 +102,18 @@ __global__ void __launch_bounds__(32 * W) merge_kernel(const DecodeArgs a) {
     const int64_t pair = blockIdx.x;             // sequence * Hq + head
     const int32_t i = (int32_t)(pair / a.num_q_heads);
     const int32_t T = checked_len(a, i);
-    const int32_t n = (int32_t)(((int64_t)T + a.part_tokens - 1) / a.part_tokens);
-    if (n <= 1) return;                          // written directly by the partition kernel
+    int32_t n = (int32_t)(((int64_t)T + a.part_tokens - 1) / a.part_tokens);
+    const int32_t k = seq_group_of(a, i);       // -1 outside a shared-prefix call
+    if (k >= 0) {
+        // a group member: its group's prefix partitions (slots 0 ..), then its
+        // own past the shared blocks; merged even when there is one (its
+        // partials are not normalised), zeros when there is none
+        const int64_t pk = (int64_t)group_prefix_blocks(a, k) * a.block_size;
+        n = (int32_t)((pk + a.part_tokens - 1) / a.part_tokens +
+                      (max((int64_t)0, T - pk) + a.part_tokens - 1) / a.part_tokens);
+    } else if (n <= 1) {
+        return;                                  // written directly by the partition kernel
+    }
     const int32_t D = a.head_dim;
     const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t cell0 = pair * a.max_parts;

@@ -126,11 +126,12 @@ cudaError_t launch_merge_w(int warps, dim3 grid, cudaStream_t st, const DecodeAr
 }
 
 // The merge launch of a call: one CTA per (sequence, query head), after the
-// partition kernel on the same stream (programmatic dependent launch).
+// partition kernel on the same stream (programmatic dependent launch); its
+// warps are sized for typical_parts partitions (any count merges correctly).
 template <typename E>
-cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t st) {
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t st, int32_t typical_parts) {
     const dim3 grid((unsigned)((int64_t)a.num_seqs * a.num_q_heads));
-    const int warps = merge_warps(a.max_parts);
+    const int warps = merge_warps(typical_parts);
     return a.head_dim % 4 == 0 ? launch_merge_w<E, 4>(warps, grid, st, a)
                                : launch_merge_w<E, 1>(warps, grid, st, a);
 }
@@ -143,11 +144,11 @@ bool set_smem(Kern kern, size_t bytes) {
                                 (int)bytes) == cudaSuccess;
 }
 
-template <int D, bool G16>
+template <int D, bool G16, bool CAS>
 cudaError_t launch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
                         const DecodeArgs& a, cudaStream_t st) {
     using C = TmaMmaCfg<D, G16>;
-    auto kern = decode_tma_mma_kernel<D, G16>;
+    auto kern = decode_tma_mma_kernel<D, G16, CAS>;
     if (!set_smem(kern, C::smem_bytes_max())) return cudaErrorInvalidValue;
     const size_t smem = C::smem_bytes(a.part_tokens, a.block_size);
     return launch_pdl(kern, grid, dim3(C::kThreads), smem, st, mk, mv, a);
@@ -248,16 +249,25 @@ cudaError_t dispatch_prefill_mma(const pa_cache_desc* c, int32_t group, int32_t 
                               : launch_prefill_mma<256, 32>(c, group, max_q_len, num_seqs, st, a);
 }
 
-cudaError_t dispatch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
-                          const DecodeArgs& a, cudaStream_t st) {
+template <bool CAS>
+cudaError_t dispatch_fast_cas(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
+                              const DecodeArgs& a, cudaStream_t st) {
     const bool g16 = a.group > 8;                 // 16 rows: any CTA may carry 9-16 heads
     switch (a.head_dim) {
-        case 64: return g16 ? launch_fast<64, true>(grid, mk, mv, a, st)
-                            : launch_fast<64, false>(grid, mk, mv, a, st);
-        case 128: return g16 ? launch_fast<128, true>(grid, mk, mv, a, st)
-                             : launch_fast<128, false>(grid, mk, mv, a, st);
+        case 64: return g16 ? launch_fast<64, true, CAS>(grid, mk, mv, a, st)
+                            : launch_fast<64, false, CAS>(grid, mk, mv, a, st);
+        case 128: return g16 ? launch_fast<128, true, CAS>(grid, mk, mv, a, st)
+                             : launch_fast<128, false, CAS>(grid, mk, mv, a, st);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// cas: the shared-prefix instance (prefix CTAs, members past their shared
+// blocks); otherwise the plain decode kernel.
+cudaError_t dispatch_fast(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
+                          const DecodeArgs& a, cudaStream_t st, bool cas) {
+    return cas ? dispatch_fast_cas<true>(grid, mk, mv, a, st)
+               : dispatch_fast_cas<false>(grid, mk, mv, a, st);
 }
 
 // Address through which kernels reach `p`: device and managed memory as is,
@@ -360,6 +370,227 @@ struct CallRange {
 }  // namespace pa
 
 using namespace pa;
+
+namespace pa {
+namespace {
+
+// Groups of a shared-prefix decode call (host view of its arguments).
+struct ShareGroups {
+    const int32_t* seq_group;
+    const int32_t* member_start;
+    const int32_t* members;
+    const int32_t* prefix_blocks;
+    int32_t num_groups, max_group_size, max_prefix_blocks;
+    int32_t mode;   // pa_shared_mode
+};
+
+// Workspace slots per (sequence, head) of a shared-prefix call: the longest
+// shared prefix's partitions, then the longest sequence's own.
+int64_t cascade_slots(int32_t max_seq_len, int32_t max_prefix_blocks, int32_t part,
+                      const pa_cache_desc* c) {
+    return ((int64_t)max_prefix_blocks * c->block_size + part - 1) / part +
+           num_parts(max_seq_len, part);
+}
+
+// Whether a shared-prefix call reads the shared blocks once per row tile
+// (1) or runs the plain decode over the same tables (0); < 0 for invalid
+// arguments.  Automatic: once when a row tile holds m >= 2 members (m = 8
+// or 16 rows / query heads per kv head) and the shared prefix saves
+// tokens * (1 - 1/m) >= PA_SHARED_MIN_SAVED tokens of reads per member.
+// Measured on GQA-shaped batches (per call, shared / plain): G = 4 with a
+// 512-token prefix (m = 2, 256 saved) 0.985; 2048 tokens (1024) 1.007; 4096
+// tokens and 64 members 1.156; G = 1 with 2048 tokens (m = 8) 1.21; G = 8
+// (m = 1) 0.87.  Below the threshold the members' extra merges cost more than
+// the shared reads, which the plain decode takes from L2, save.
+#ifndef PA_SHARED_MIN_SAVED
+#define PA_SHARED_MIN_SAVED 1024
+#endif
+int32_t shared_mode(int32_t num_q_heads, int32_t max_prefix_blocks, int32_t mode,
+                    const pa_cache_desc* c) {
+    if (!desc_ok(c) || num_q_heads <= 0 || num_q_heads % c->num_kv_heads ||
+        max_prefix_blocks < 0 || mode < PA_SHARED_AUTO || mode > PA_SHARED_PLAIN)
+        return -1;
+    const int32_t group = num_q_heads / c->num_kv_heads;
+    if (!fast_shape(c, group) || mode == PA_SHARED_PLAIN) return 0;
+    if (mode == PA_SHARED_ONCE) return 1;
+    const int64_t rows = group > 8 ? 16 : 8;
+    const int64_t m = rows / group;                       // members per row tile
+    if (m < 2) return 0;
+    const int64_t saved = (int64_t)max_prefix_blocks * c->block_size * (m - 1) / m;
+    return saved >= PA_SHARED_MIN_SAVED ? 1 : 0;
+}
+
+// Bytes of `cells` workspace cells: acc (head_dim floats) then (m, l).
+size_t cells_bytes(size_t cells, const pa_cache_desc* c) {
+    return align256(cells * c->head_dim * sizeof(float)) + align256(cells * 2 * sizeof(float));
+}
+
+// pa_decode, and with `sh` (groups sharing leading blocks) the shared-prefix
+// decode: on the TMA kernel, extra CTAs attend each group's shared blocks once
+// for all its members' query heads, members' own CTAs start past them, and
+// the merge combines both.  Other kernels run the plain decode over the same
+// tables (same result).
+pa_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                      const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                      int32_t num_q_heads, float scale, int32_t partition_tokens, void* out,
+                      void* workspace, size_t workspace_bytes_given, const pa_cache_desc* cache,
+                      void* stream, const ShareGroups* sh) {
+    const int32_t path = !desc_ok(cache) || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads
+                             ? -1
+                             : fast_shape(cache, num_q_heads / cache->num_kv_heads) ? 1
+                             : mma_shape(cache, num_q_heads / cache->num_kv_heads)  ? 2
+                                                                                    : 0;
+    if (path < 0 || num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq < 0 ||
+        partition_tokens < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+        return PA_ERR_INVALID_ARG;
+    if ((int64_t)max_blocks_per_seq * cache->block_size < max_seq_len) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 65535 || cache->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    const int32_t group = num_q_heads / cache->num_kv_heads;
+    const int32_t B = cache->block_size;
+    int32_t part = partition_tokens ? partition_tokens
+                                    : auto_partition(num_seqs, num_q_heads, max_seq_len, cache);
+    if (part <= 0 || part % B) return PA_ERR_INVALID_ARG;
+    bool fast = path == 1;
+    if (fast && (part > fast_max_partition(cache) || !aligned(k_cache, 16) ||
+                 !aligned(v_cache, 16) || !aligned(q, 16)))
+        fast = false;
+    // other shapes: the mma.sync kernel (bf16, head dims that are multiples of
+    // 16 up to 128), the tiled CUDA-core kernel, else (a head dim that is not
+    // whole 16-byte rows, or unaligned caches) the generic one
+    const bool caches16 = aligned(k_cache, 16) && aligned(v_cache, 16);
+    const bool mma = path == 2 && caches16 && aligned(q, 4);
+    const bool tiled = !fast && !mma && tiled_shape(cache) && caches16;
+    if (!fast && !mma && !tiled && part > generic_max_partition(cache, group))
+        return PA_ERR_UNSUPPORTED;
+    if (!aligned(q, elem_bytes(cache)) || !aligned(out, elem_bytes(cache)) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!map_step_arg(q) || !map_step_arg(block_tables) || !map_step_arg(seq_lens) ||
+        !map_step_arg(out) || !device_memory(k_cache) || !device_memory(v_cache))
+        return PA_ERR_INVALID_ARG;
+    if (num_parts(max_seq_len, part) > 65535) return PA_ERR_UNSUPPORTED;
+    // shared-prefix decode on the TMA kernel: workspace slots for the
+    // groups' prefix partitions in front of each member's own
+    const bool cas = sh != nullptr && fast &&
+                     shared_mode(num_q_heads, sh->max_prefix_blocks, sh->mode, cache) == 1;
+    const int64_t slots = cas ? cascade_slots(max_seq_len, sh->max_prefix_blocks, part, cache)
+                              : num_parts(max_seq_len, part);
+    if (slots > 65535) return PA_ERR_UNSUPPORTED;
+    const int32_t max_parts = (int32_t)slots;
+    const size_t need = cas ? cells_bytes((size_t)num_seqs * num_q_heads * slots, cache)
+                            : workspace_bytes(num_seqs, num_q_heads, max_seq_len, part, cache);
+    if (need > 0 && (!workspace || workspace_bytes_given < need || !aligned(workspace, 256) ||
+                     !device_memory(workspace)))
+        return PA_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (debug::enabled()) {
+        const pa_status r = debug::check_tables(block_tables, max_blocks_per_seq, seq_lens,
+                                                num_seqs, max_seq_len, nullptr, 0, cache, st);
+        if (r != PA_OK) return r;
+        if (sh) {
+            const pa_status r2 = debug::check_groups(block_tables, max_blocks_per_seq, num_seqs,
+                                                     sh->seq_group, sh->member_start,
+                                                     sh->members, sh->prefix_blocks,
+                                                     sh->num_groups, sh->max_group_size,
+                                                     sh->max_prefix_blocks, st);
+            if (r2 != PA_OK) return r2;
+        }
+    }
+
+    DecodeArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    const size_t cells = (size_t)num_seqs * num_q_heads * max_parts;
+    a.ws_acc = need ? static_cast<float*>(workspace) : nullptr;
+    a.ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                              align256(cells * cache->head_dim * sizeof(float)))
+                   : nullptr;
+    a.num_seqs = num_seqs;
+    a.max_blocks = max_blocks_per_seq;
+    a.max_seq_len = max_seq_len;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = cache->num_kv_heads;
+    a.group = group;
+    a.num_blocks = cache->num_blocks;
+    a.block_size = B;
+    a.head_dim = cache->head_dim;
+    a.part_tokens = part;
+    a.max_parts = max_parts;
+    a.scale_log2 = scale * kLog2e;
+    a.sub_groups = fast || mma ? (group + 15) / 16
+                   : tiled     ? (group + kTiledHeads - 1) / kTiledHeads
+                               : 1;
+    if ((int64_t)cache->num_kv_heads * a.sub_groups > 65535) return PA_ERR_UNSUPPORTED;
+
+    dim3 grid(max_parts, cache->num_kv_heads * a.sub_groups, num_seqs);
+    if (cas) {
+        // prefix CTAs: per group, tiles of kRows (member, head) rows, spread
+        // over the sub-group index and prefix_ztiles grid z slots
+        const int64_t rows = group > 8 ? 16 : 8;
+        const int64_t tiles = ((int64_t)sh->max_group_size * group + rows - 1) / rows;
+        const int64_t zt = (tiles + a.sub_groups - 1) / a.sub_groups;
+        const int64_t pz = zt * sh->num_groups;
+        if (pz + num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+        a.seq_group = sh->seq_group;
+        a.member_start = sh->member_start;
+        a.members = sh->members;
+        a.prefix_blocks = sh->prefix_blocks;
+        a.num_groups = sh->num_groups;
+        a.max_prefix_blocks = sh->max_prefix_blocks;
+        a.prefix_ztiles = (int32_t)zt;
+        a.prefix_z = (int32_t)pz;
+        const int64_t own = num_parts(max_seq_len, part);
+        const int64_t pre = ((int64_t)sh->max_prefix_blocks * B + part - 1) / part;
+        grid = dim3((unsigned)std::max(own, pre), cache->num_kv_heads * a.sub_groups,
+                    (unsigned)(pz + num_seqs));
+    }
+    cudaError_t err;
+    if (fast) {
+        CUtensorMap mk, mv;
+        if (!cached_map(&mk, k_cache, cache, 0) || !cached_map(&mv, v_cache, cache, 1))
+            return PA_ERR_CUDA;
+        err = dispatch_fast(grid, mk, mv, a, st, cas);
+    } else if (mma) {
+        const size_t smem = decode_mma_smem_bytes(cache->head_dim);
+        auto kern = group > 8 ? decode_mma_kernel<true> : decode_mma_kernel<false>;
+        if (!set_smem(kern, smem)) return PA_ERR_UNSUPPORTED;
+        err = launch_pdl(kern, grid, dim3(kMmaThreads), smem, st, a);
+    } else if (tiled) {
+        err = dispatch_tiled(cache, group, grid, a, st);
+        if (err == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
+    } else {
+        const size_t smem = generic_smem_bytes(group, cache->head_dim, part, B);
+        if (cache->dtype == PA_F32) {
+            if (!set_smem(decode_generic_kernel<float>, smem)) return PA_ERR_UNSUPPORTED;
+            err = launch_pdl(decode_generic_kernel<float>, grid, dim3(128), smem, st, a);
+        } else {
+            if (!set_smem(decode_generic_kernel<__nv_bfloat16>, smem)) return PA_ERR_UNSUPPORTED;
+            err = launch_pdl(decode_generic_kernel<__nv_bfloat16>, grid, dim3(128), smem, st, a);
+        }
+    }
+    if (err != cudaSuccess) return PA_ERR_CUDA;
+    if (max_parts > 1 || cas) {
+        // the longest sequence's own partitions (a shared-prefix call's extra
+        // prefix slots are mostly one or two per member)
+        const int32_t typical = (int32_t)num_parts(max_seq_len, part);
+        const cudaError_t merr = cache->dtype == PA_F32
+                                     ? launch_merge<float>(a, st, typical)
+                                     : launch_merge<__nv_bfloat16>(a, st, typical);
+        if (merr != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
 
 extern "C" {
 
@@ -485,112 +716,73 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     void* workspace, size_t workspace_bytes_given, const pa_cache_desc* cache,
                     void* stream) {
     const CallRange range("pa_decode");
-    const int32_t path = pa_decode_path(num_q_heads, cache);
-    if (path < 0 || num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq < 0 ||
-        partition_tokens < 0)
-        return PA_ERR_INVALID_ARG;
-    if (num_seqs == 0) return PA_OK;
-    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
-        return PA_ERR_INVALID_ARG;
-    if ((int64_t)max_blocks_per_seq * cache->block_size < max_seq_len) return PA_ERR_INVALID_ARG;
-    if (num_seqs > 65535 || cache->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
-    const int32_t group = num_q_heads / cache->num_kv_heads;
-    const int32_t B = cache->block_size;
-    int32_t part = partition_tokens ? partition_tokens
-                                    : auto_partition(num_seqs, num_q_heads, max_seq_len, cache);
-    if (part <= 0 || part % B) return PA_ERR_INVALID_ARG;
-    bool fast = path == 1;
-    if (fast && (part > fast_max_partition(cache) || !aligned(k_cache, 16) ||
-                 !aligned(v_cache, 16) || !aligned(q, 16)))
-        fast = false;
-    // other shapes: the mma.sync kernel (bf16, head dims that are multiples of
-    // 16 up to 128), the tiled CUDA-core kernel, else (a head dim that is not
-    // whole 16-byte rows, or unaligned caches) the generic one
-    const bool caches16 = aligned(k_cache, 16) && aligned(v_cache, 16);
-    const bool mma = path == 2 && caches16 && aligned(q, 4);
-    const bool tiled = !fast && !mma && tiled_shape(cache) && caches16;
-    if (!fast && !mma && !tiled && part > generic_max_partition(cache, group))
-        return PA_ERR_UNSUPPORTED;
-    if (!aligned(q, elem_bytes(cache)) || !aligned(out, elem_bytes(cache)) ||
-        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
-        return PA_ERR_INVALID_ARG;
-    if (!map_step_arg(q) || !map_step_arg(block_tables) || !map_step_arg(seq_lens) ||
-        !map_step_arg(out) || !device_memory(k_cache) || !device_memory(v_cache))
-        return PA_ERR_INVALID_ARG;
-    if (num_parts(max_seq_len, part) > 65535) return PA_ERR_UNSUPPORTED;
-    const int32_t max_parts = (int32_t)num_parts(max_seq_len, part);
-    const size_t need = workspace_bytes(num_seqs, num_q_heads, max_seq_len, part, cache);
-    if (need > 0 && (!workspace || workspace_bytes_given < need || !aligned(workspace, 256) ||
-                     !device_memory(workspace)))
-        return PA_ERR_WORKSPACE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (debug::enabled()) {
-        const pa_status r = debug::check_tables(block_tables, max_blocks_per_seq, seq_lens,
-                                                num_seqs, max_seq_len, nullptr, 0, cache, st);
-        if (r != PA_OK) return r;
-    }
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                       num_seqs, max_seq_len, num_q_heads, scale, partition_tokens, out,
+                       workspace, workspace_bytes_given, cache, stream, nullptr);
+}
 
-    DecodeArgs a;
-    a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
-    a.block_tables = block_tables;
-    a.seq_lens = seq_lens;
-    a.out = out;
-    const size_t cells = (size_t)num_seqs * num_q_heads * max_parts;
-    a.ws_acc = need ? static_cast<float*>(workspace) : nullptr;
-    a.ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                              align256(cells * cache->head_dim * sizeof(float)))
-                   : nullptr;
-    a.num_seqs = num_seqs;
-    a.max_blocks = max_blocks_per_seq;
-    a.max_seq_len = max_seq_len;
-    a.num_q_heads = num_q_heads;
-    a.num_kv_heads = cache->num_kv_heads;
-    a.group = group;
-    a.num_blocks = cache->num_blocks;
-    a.block_size = B;
-    a.head_dim = cache->head_dim;
-    a.part_tokens = part;
-    a.max_parts = max_parts;
-    a.scale_log2 = scale * kLog2e;
-    a.sub_groups = fast || mma ? (group + 15) / 16
-                   : tiled     ? (group + kTiledHeads - 1) / kTiledHeads
-                               : 1;
-    if ((int64_t)cache->num_kv_heads * a.sub_groups > 65535) return PA_ERR_UNSUPPORTED;
+int32_t pa_decode_shared_prefix_mode(int32_t num_q_heads, int32_t max_prefix_blocks,
+                                     int32_t mode, const pa_cache_desc* cache) {
+    return shared_mode(num_q_heads, max_prefix_blocks, mode, cache);
+}
 
-    dim3 grid(max_parts, cache->num_kv_heads * a.sub_groups, num_seqs);
-    cudaError_t err;
-    if (fast) {
-        CUtensorMap mk, mv;
-        if (!cached_map(&mk, k_cache, cache, 0) || !cached_map(&mv, v_cache, cache, 1))
-            return PA_ERR_CUDA;
-        err = dispatch_fast(grid, mk, mv, a, st);
-    } else if (mma) {
-        const size_t smem = decode_mma_smem_bytes(cache->head_dim);
-        auto kern = group > 8 ? decode_mma_kernel<true> : decode_mma_kernel<false>;
-        if (!set_smem(kern, smem)) return PA_ERR_UNSUPPORTED;
-        err = launch_pdl(kern, grid, dim3(kMmaThreads), smem, st, a);
-    } else if (tiled) {
-        err = dispatch_tiled(cache, group, grid, a, st);
-        if (err == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
-    } else {
-        const size_t smem = generic_smem_bytes(group, cache->head_dim, part, B);
-        if (cache->dtype == PA_F32) {
-            if (!set_smem(decode_generic_kernel<float>, smem)) return PA_ERR_UNSUPPORTED;
-            err = launch_pdl(decode_generic_kernel<float>, grid, dim3(128), smem, st, a);
-        } else {
-            if (!set_smem(decode_generic_kernel<__nv_bfloat16>, smem)) return PA_ERR_UNSUPPORTED;
-            err = launch_pdl(decode_generic_kernel<__nv_bfloat16>, grid, dim3(128), smem, st, a);
-        }
-    }
-    if (err != cudaSuccess) return PA_ERR_CUDA;
-    if (max_parts > 1) {
-        const cudaError_t merr = cache->dtype == PA_F32 ? launch_merge<float>(a, st)
-                                                        : launch_merge<__nv_bfloat16>(a, st);
-        if (merr != cudaSuccess) return PA_ERR_CUDA;
-    }
-    return PA_OK;
+size_t pa_decode_shared_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                               int32_t max_seq_len, int32_t max_prefix_blocks,
+                                               int32_t partition_tokens,
+                                               const pa_cache_desc* cache) {
+    if (pa_decode_path(num_q_heads, cache) < 0 || num_seqs < 0 || max_seq_len < 0 ||
+        max_prefix_blocks < 0 || partition_tokens < 0)
+        return 0;
+    const int32_t part = partition_tokens > 0
+                             ? partition_tokens
+                             : auto_partition(num_seqs, num_q_heads, max_seq_len, cache);
+    if (part <= 0) return 0;
+    const size_t plain = workspace_bytes(num_seqs, num_q_heads, max_seq_len, part, cache);
+    if (!fast_shape(cache, num_q_heads / cache->num_kv_heads)) return plain;
+    const int64_t slots = cascade_slots(max_seq_len, max_prefix_blocks, part, cache);
+    return std::max(plain, cells_bytes((size_t)num_seqs * num_q_heads * slots, cache));
+}
+
+pa_status pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, int32_t num_seqs,
+                                  int32_t max_seq_len, int32_t num_q_heads, float scale,
+                                  int32_t partition_tokens, const int32_t* seq_group,
+                                  const int32_t* member_start, const int32_t* members,
+                                  const int32_t* prefix_blocks, int32_t num_groups,
+                                  int32_t max_group_size, int32_t max_prefix_blocks,
+                                  int32_t mode, void* out, void* workspace,
+                                  size_t workspace_bytes_given, const pa_cache_desc* cache,
+                                  void* stream) {
+    const CallRange range("pa_decode_shared_prefix");
+    if (num_groups < 0 || max_group_size < 0 || max_prefix_blocks < 0 ||
+        max_prefix_blocks > max_blocks_per_seq || mode < PA_SHARED_AUTO ||
+        mode > PA_SHARED_PLAIN)
+        return PA_ERR_INVALID_ARG;
+    if (num_groups == 0)
+        return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                           num_seqs, max_seq_len, num_q_heads, scale, partition_tokens, out,
+                           workspace, workspace_bytes_given, cache, stream, nullptr);
+    if (!seq_group || !member_start || !members || !prefix_blocks || max_group_size < 1)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(seq_group, 4) || !aligned(member_start, 4) || !aligned(members, 4) ||
+        !aligned(prefix_blocks, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!map_step_arg(seq_group) || !map_step_arg(member_start) || !map_step_arg(members) ||
+        !map_step_arg(prefix_blocks))
+        return PA_ERR_INVALID_ARG;
+    ShareGroups sh;
+    sh.seq_group = seq_group;
+    sh.member_start = member_start;
+    sh.members = members;
+    sh.prefix_blocks = prefix_blocks;
+    sh.num_groups = num_groups;
+    sh.max_group_size = max_group_size;
+    sh.max_prefix_blocks = max_prefix_blocks;
+    sh.mode = mode;
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                       num_seqs, max_seq_len, num_q_heads, scale, partition_tokens, out,
+                       workspace, workspace_bytes_given, cache, stream, &sh);
 }
 
 pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t total_q,

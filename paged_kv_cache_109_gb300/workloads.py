@@ -89,6 +89,9 @@ class Workload:
     steps: list[Step]
     seed: int
     stats: dict = field(default_factory=dict)
+    # groups of sequences sharing leading blocks (member ids, shared blocks),
+    # from the pool's tables and reference counts (BlockPool.shared_prefix_groups)
+    prefix_groups: list = field(default_factory=list)
 
     @property
     def num_seqs(self) -> int:
@@ -232,6 +235,7 @@ def gqa(num_seqs=128, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=1
     wl.stats["shared_seqs"] = sorted(sharers)
     wl.stats["prefix_ref_cnt"] = (pool.ref_cnt[pool.tables[min(sharers)][0]]
                                   if sharers else 0)
+    wl.prefix_groups = pool.shared_prefix_groups(seqs)
     return wl
 
 

@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle
+import paged_kv_cache_109_gb300 as pa
 from paged_kv_cache_109_gb300 import workloads
 from paged_kv_cache_109_gb300.block_pool import BlockPool, SharedTailWrite, slot_of
 from tests.conftest import golden
@@ -268,3 +269,35 @@ def test_positions_give_the_slot_mapping():
             got = oracle.slots_from_positions(st.seq_ids, st.positions, st.block_tables,
                                               wl.block_size)
             assert got.tolist() == st.slot_mapping.tolist()
+
+
+def test_shared_prefix_groups_from_the_pool():
+    """Sequences sharing leading blocks (ref_cnt > 1) group by their first
+    block; the shared count is the run of entries every member agrees on;
+    singletons and unshared sequences are left out."""
+    pool = BlockPool(64, 4)
+    pool.add("a", 10)                               # 3 blocks
+    pool.add("b", 14, prefix_of="a", prefix_tokens=8)
+    pool.add("c", 9, prefix_of="a", prefix_tokens=4)
+    pool.add("d", 5)
+    pool.fork("d", "e")
+    pool.add("f", 3)
+    seqs = ["f", "a", "b", "c", "d", "e"]
+    groups = sorted(pool.shared_prefix_groups(seqs))
+    # a, b, c share block 0 (c only that one); d and e share all of d's blocks
+    assert groups == [([1, 2, 3], 1), ([4, 5], 2)]
+    assert pool.shared_prefix_groups(["f", "a"]) == []
+
+
+def test_prefix_groups_marshal_to_csr():
+    grp = pa.prefix_groups([([4, 1], 3), ([7], 9), ([0, 2, 5], 2)], 8)
+    assert grp.num_groups == 2                      # the one-member group is dropped
+    assert grp.seq_group.tolist() == [1, 0, 1, -1, 0, 1, -1, -1]
+    assert grp.member_start.tolist() == [0, 2, 5]
+    assert grp.members.tolist() == [4, 1, 0, 2, 5]
+    assert grp.prefix_blocks.tolist() == [3, 2]
+    assert (grp.max_group_size, grp.max_prefix_blocks) == (3, 3)
+    assert all(t.dtype == torch.int32 for t in (grp.seq_group, grp.member_start,
+                                                grp.members, grp.prefix_blocks))
+    empty = pa.prefix_groups([], 3)
+    assert empty.num_groups == 0 and empty.seq_group.tolist() == [-1, -1, -1]
