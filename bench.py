@@ -396,7 +396,11 @@ def run_ours(args, rank, world, device):
     # groups sharing leading blocks: the shared-prefix decode reads them once
     shared = bool(wl.prefix_groups) and not args.no_shared_prefix
     groups = pa.prefix_groups(wl.prefix_groups, wl.num_seqs, device) if shared else None
-    bytes_ = [step_bytes(wl, k, shared_prefix=shared) for k in range(nsteps_wl)]
+    # the byte model follows the path the call takes: the shared-prefix
+    # partials only when the shared blocks are read once
+    once = shared and pa.decode_shared_prefix_mode(wl.num_q_heads, groups.max_prefix_blocks,
+                                                   kc) == 1
+    bytes_ = [step_bytes(wl, k, shared_prefix=once) for k in range(nsteps_wl)]
     maxlens = [int(st.seq_lens.max()) for st in wl.steps]
     part = args.partition or 0
     ws_need = max(pa.decode_shared_prefix_workspace_bytes(wl.num_seqs, wl.num_q_heads, m,
@@ -492,8 +496,7 @@ def run_ours(args, rank, world, device):
                             else "slot_mapping",
                    "decode": ("pa_decode_shared_prefix, automatic mode (%s): %d group(s), "
                               "%s shared blocks"
-                              % ("shared blocks read once" if pa.decode_shared_prefix_mode(
-                                     wl.num_q_heads, groups.max_prefix_blocks, kc) == 1
+                              % ("shared blocks read once" if once
                                  else "plain decode: reading them once would not pay here",
                                  len(wl.prefix_groups),
                                  "/".join(str(b) for _, b in wl.prefix_groups))
