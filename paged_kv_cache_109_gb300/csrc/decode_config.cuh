@@ -42,11 +42,15 @@ int device_sm_count() {
 // ---- kernel selection --------------------------------------------------------
 
 // Groups of more than 16 query heads are split into sub-groups of 16, one CTA
-// each, reading the same K/V tiles (the later reads mostly hit L2).
+// each, reading the same K/V tiles (the later reads mostly hit L2).  Head dims
+// 80, 96 and 112 load as two 64-column boxes whose columns past the head dim
+// are zero-filled by the copy (out of the tensor map's bounds).
+bool tma_head_dim(int32_t D) { return D == 64 || D == 80 || D == 96 || D == 112 || D == 128; }
+
 bool fast_shape(const pa_cache_desc* c, int32_t group) {
     if (c->dtype != PA_BF16 || group < 1) return false;
     const int D = c->head_dim, B = c->block_size;
-    if (D != 64 && D != 128) return false;
+    if (!tma_head_dim(D)) return false;
     return B == 8 || (B % 16 == 0 && B <= 256);
 }
 
@@ -63,14 +67,16 @@ bool tiled_shape(const pa_cache_desc* c) {
 #endif
 
 // The mma.sync kernel: bf16 head dims that are multiples of 16 up to 128 the
-// TMA kernel does not take (other head dims, other block sizes), for groups
-// of at least PA_DECODE_MMA_MIN_GROUP query heads.  Smaller groups stay on
-// the tiled CUDA-core kernel: its run copies move a block's rows with one
-// copy each, where this kernel copies every row on its own (to pad it), and
-// at up to four heads the CUDA cores keep up with HBM.  Measured, fraction
-// of the copy peak (tiled / mma.sync): G = 1, D = 96: 0.886 / 0.467;
-// G = 4, D = 96: 0.487 / 0.452; G = 4, B = 4: 0.615 / 0.582; G = 8, D = 64,
-// B = 4: 0.210 / 0.374; G = 16, D = 112: 0.169 / 0.433.
+// TMA kernel does not take (16, 32, 48, and every head dim at block sizes
+// other than 8 or a multiple of 16), for groups of at least
+// PA_DECODE_MMA_MIN_GROUP query heads.  Smaller groups stay on the tiled
+// CUDA-core kernel: its run copies move a block's rows with one copy each,
+// where this kernel copies every row on its own (to pad it), and at up to
+// four heads the CUDA cores keep up with HBM.  Measured, fraction of the copy
+// peak (tiled / mma.sync), before head dims 80-112 moved to the TMA kernel:
+// G = 1, D = 96: 0.886 / 0.467; G = 4, D = 96: 0.487 / 0.452; G = 4, B = 4:
+// 0.615 / 0.582; G = 8, D = 64, B = 4: 0.210 / 0.374; G = 16, D = 112:
+// 0.169 / 0.433.
 bool mma_shape(const pa_cache_desc* c, int32_t group) {
     return c->dtype == PA_BF16 && c->head_dim % 16 == 0 && c->head_dim <= 128 &&
            group >= PA_DECODE_MMA_MIN_GROUP && !fast_shape(c, group);

@@ -55,9 +55,10 @@ struct TmaMmaCfg {
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kChunk = 16;                     // tokens per pipeline stage
     static constexpr int kBoxCols = 64;                   // 64 bf16 = 128 bytes (swizzle span)
-    static constexpr int kBoxes = D / kBoxCols;
+    // head dims 80-112: a second box whose columns past D arrive as zeros
+    static constexpr int kBoxes = (D + kBoxCols - 1) / kBoxCols;
     static constexpr int kBoxBytes = kChunk * 128;        // 16 rows x 128 bytes
-    static constexpr int kTileBytes = kBoxes * kBoxBytes;  // = 16 * D * 2
+    static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 16 rows x kBoxes x 64 columns
     static constexpr int kStageBytes = 2 * kTileBytes;    // K chunk + V chunk
     static constexpr int kStagesRaw = PA_RING_BYTES_PER_WARP / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
@@ -66,7 +67,7 @@ struct TmaMmaCfg {
     static constexpr int kKSteps = D / 16;
     static constexpr int kDTiles = D / 8;
     static constexpr int kMaxTableSlice = 2048;            // block ids per partition
-    static_assert(D % 64 == 0, "tile shape");
+    static_assert(D % 16 == 0 && D <= 128, "tile shape");
     static_assert(kWarps * kRows * (D + 2) * 4 <= kRingBytes, "combine area");
     // dynamic shared bytes for a partition of part_tokens tokens
     static size_t smem_bytes(int32_t part_tokens, int32_t block_size) {

@@ -249,17 +249,33 @@ cudaError_t dispatch_prefill_mma(const pa_cache_desc* c, int32_t group, int32_t 
                               : launch_prefill_mma<256, 32>(c, group, max_q_len, num_seqs, st, a);
 }
 
+template <int D, bool CAS>
+cudaError_t launch_fast_d(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
+                          const DecodeArgs& a, cudaStream_t st) {
+    // 16 rows: any CTA may carry 9-16 heads
+    return a.group > 8 ? launch_fast<D, true, CAS>(grid, mk, mv, a, st)
+                       : launch_fast<D, false, CAS>(grid, mk, mv, a, st);
+}
+
+// The shared-prefix instance exists for head dims 64 and 128 only
+// (shared_mode() never selects it for the others).
 template <bool CAS>
 cudaError_t dispatch_fast_cas(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv,
                               const DecodeArgs& a, cudaStream_t st) {
-    const bool g16 = a.group > 8;                 // 16 rows: any CTA may carry 9-16 heads
     switch (a.head_dim) {
-        case 64: return g16 ? launch_fast<64, true, CAS>(grid, mk, mv, a, st)
-                            : launch_fast<64, false, CAS>(grid, mk, mv, a, st);
-        case 128: return g16 ? launch_fast<128, true, CAS>(grid, mk, mv, a, st)
-                             : launch_fast<128, false, CAS>(grid, mk, mv, a, st);
-        default: return cudaErrorInvalidValue;
+        case 64: return launch_fast_d<64, CAS>(grid, mk, mv, a, st);
+        case 128: return launch_fast_d<128, CAS>(grid, mk, mv, a, st);
+        default: break;
     }
+    if constexpr (!CAS) {
+        switch (a.head_dim) {
+            case 80: return launch_fast_d<80, false>(grid, mk, mv, a, st);
+            case 96: return launch_fast_d<96, false>(grid, mk, mv, a, st);
+            case 112: return launch_fast_d<112, false>(grid, mk, mv, a, st);
+            default: break;
+        }
+    }
+    return cudaErrorInvalidValue;
 }
 
 // cas: the shared-prefix instance (prefix CTAs, members past their shared
@@ -411,7 +427,9 @@ int32_t shared_mode(int32_t num_q_heads, int32_t max_prefix_blocks, int32_t mode
         max_prefix_blocks < 0 || mode < PA_SHARED_AUTO || mode > PA_SHARED_PLAIN)
         return -1;
     const int32_t group = num_q_heads / c->num_kv_heads;
-    if (!fast_shape(c, group) || mode == PA_SHARED_PLAIN) return 0;
+    if (!fast_shape(c, group) || (c->head_dim != 64 && c->head_dim != 128) ||
+        mode == PA_SHARED_PLAIN)
+        return 0;
     if (mode == PA_SHARED_ONCE) return 1;
     const int64_t rows = group > 8 ? 16 : 8;
     const int64_t m = rows / group;                       // members per row tile
@@ -738,7 +756,7 @@ size_t pa_decode_shared_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_h
                              : auto_partition(num_seqs, num_q_heads, max_seq_len, cache);
     if (part <= 0) return 0;
     const size_t plain = workspace_bytes(num_seqs, num_q_heads, max_seq_len, part, cache);
-    if (!fast_shape(cache, num_q_heads / cache->num_kv_heads)) return plain;
+    if (shared_mode(num_q_heads, max_prefix_blocks, PA_SHARED_ONCE, cache) != 1) return plain;
     const int64_t slots = cascade_slots(max_seq_len, max_prefix_blocks, part, cache);
     return std::max(plain, cells_bytes((size_t)num_seqs * num_q_heads * slots, cache));
 }
@@ -840,7 +858,9 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     constexpr int32_t kTilesPerCta = 2;
     a.scale_log2 = scale * kLog2e;
     // the tensor-core kernel takes its row maximum before scaling: scale >= 0
-    const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) && aligned(out, 16) &&
+    // (head dims 64 and 128: the decode kernel's other TMA head dims are not its)
+    const bool fast = path == 1 && (cache->head_dim == 64 || cache->head_dim == 128) &&
+                      a.tokens_per_tile > 0 && aligned(q, 16) && aligned(out, 16) &&
                       aligned(k_cache, 16) && aligned(v_cache, 16) && scale >= 0.f;
     cudaError_t err;
     if (fast) {

@@ -63,8 +63,12 @@ def test_path_selection(lib):
     assert path(32, desc(bs=512)) == 0
     assert path(64, desc(bs=24)) == 2                  # G=8: mma.sync
     assert path(64, desc(bs=4)) == 2
-    assert path(40, desc(d=96)) == 2                   # G=5, bf16 head dim a multiple of 16
-    assert path(32, desc(d=96)) == 0                   # G=4: CUDA cores
+    assert path(40, desc(d=96)) == 1                   # D=96: two 64-column boxes
+    assert path(32, desc(d=80, bs=8)) == 1
+    assert path(128, desc(d=112, bs=32)) == 1
+    assert path(40, desc(d=96, bs=24)) == 2            # G=5 at a block size TMA does not take
+    assert path(64, desc(d=48)) == 2                   # D=48: mma.sync
+    assert path(32, desc(d=96, bs=24)) == 0            # G=4: CUDA cores
     assert path(64, desc(d=40)) == 0                   # not a multiple of 16: CUDA cores
     assert path(64, desc(d=256)) == 0                  # over 128: CUDA cores
     assert path(16, desc(d=64, bs=64, hkv=4)) == 1

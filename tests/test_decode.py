@@ -100,6 +100,11 @@ FAST_CASES = [
     (64, 2, 128, 16, (5, 300, 1000)),                              # G=32: two sub-groups of 16
     (48, 2, 128, 16, (1, 17, 700)),                                # G=24: sub-groups of 16 and 8
     (40, 1, 64, 32, (33, 400)),                                    # G=40: 16, 16 and 8
+    (40, 8, 96, 16, (1, 100, 257, 1500)),                          # D=96: box 2 half zero-filled
+    (64, 8, 80, 32, (1, 31, 32, 33, 900)),                         # D=80, G=8, B=32
+    (32, 8, 112, 16, (17, 400, 2049)),                             # D=112, G=4
+    (128, 8, 96, 16, (5, 700)),                                    # D=96, G=16
+    (8, 8, 96, 8, (1, 9, 130)),                                    # D=96 MHA, B=8
 ]
 
 
@@ -119,8 +124,8 @@ def test_fast_kernel_matches_oracle(cuda_device, hq, hkv, d, bs, lengths, part):
 @pytest.mark.parametrize("hq,hkv,d,bs,lengths,dtype", [
     (8, 2, 8, 4, (10, 7, 1, 33), torch.float32),
     (32, 8, 128, 16, (1, 200, 1000), torch.float32),
-    (64, 2, 96, 16, (5, 300), torch.bfloat16),            # G=32, D=96: portable kernel
-    (6, 2, 96, 8, (1, 8, 9, 100), torch.bfloat16),       # D=96, B=8
+    (64, 2, 96, 24, (5, 300), torch.bfloat16),            # G=32, D=96, B=24: mma.sync
+    (6, 2, 96, 12, (1, 8, 9, 100), torch.bfloat16),      # D=96, B=12: CUDA cores
     (4, 4, 256, 16, (17, 64), torch.bfloat16),           # D=256
 ])
 @pytest.mark.parametrize("part", [0, "B", "5B"])
@@ -144,7 +149,8 @@ def test_portable_kernel_matches_oracle(cuda_device, hq, hkv, d, bs, lengths, dt
     (6, 2, 64, 1, (1100, 3), torch.float32, 1100),          # >512 blocks in one partition
     (6, 3, 12, 16, (30, 70), torch.bfloat16, 0),           # 24-byte rows: the generic kernel
     (6, 3, 12, 16, (30, 70), torch.bfloat16, 32),
-    (40, 8, 96, 16, (1, 100, 257), torch.bfloat16, 0),     # mma.sync, G=5 (lo parts in rows 8-15)
+    (40, 8, 96, 24, (1, 100, 257), torch.bfloat16, 0),     # mma.sync, G=5 (lo parts in rows 8-15)
+    (64, 8, 48, 16, (1, 100, 257), torch.bfloat16, 64),    # mma.sync, D=48
     (96, 8, 80, 5, (700, 33), torch.bfloat16, 35),         # mma.sync, G=12, B=5
     (64, 4, 64, 1, (1100, 3), torch.bfloat16, 1100),       # mma.sync, G=16, >512 blocks a partition
     (256, 8, 112, 24, (500, 1, 90), torch.bfloat16, 0),    # mma.sync, G=32: two sub-groups
@@ -511,8 +517,9 @@ def test_stale_workspace_contents_do_not_matter(cuda_device):
 
 
 @pytest.mark.parametrize("hq,hkv,d,bs,dtype", [(32, 8, 128, 16, torch.bfloat16),   # TMA
-                                              (64, 8, 96, 16, torch.bfloat16),    # mma.sync
-                                              (16, 8, 96, 16, torch.bfloat16),    # tiled
+                                              (64, 8, 96, 4, torch.bfloat16),     # mma.sync
+                                              (16, 8, 96, 4, torch.bfloat16),     # tiled
+                                              (64, 8, 96, 16, torch.bfloat16),    # TMA, D=96
                                               (8, 2, 64, 16, torch.float32)])     # tiled fp32
 @pytest.mark.parametrize("shift", ["q", "out"])
 def test_unaligned_query_or_output(cuda_device, hq, hkv, d, bs, dtype, shift):

@@ -148,13 +148,17 @@ def test_groups_from_the_block_pool(cuda_device):
     assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "block pool groups")
 
 
-@pytest.mark.parametrize("dtype,d,hq,hkv", [(torch.float32, 128, 32, 8),
-                                             (torch.bfloat16, 96, 64, 8),
-                                             (torch.bfloat16, 96, 8, 2)])
-def test_other_shapes_run_the_plain_decode(cuda_device, dtype, d, hq, hkv):
-    q, kc, vc, bt, sl, members = shared_batch(hq, hkv, d, 16, [(4, [100, 70, 65])], [30],
+@pytest.mark.parametrize("dtype,d,hq,hkv,bs", [(torch.float32, 128, 32, 8, 16),
+                                                (torch.bfloat16, 96, 64, 8, 16),
+                                                (torch.bfloat16, 96, 8, 2, 16),
+                                                (torch.bfloat16, 96, 64, 8, 4)])
+def test_other_shapes_run_the_plain_decode(cuda_device, dtype, d, hq, hkv, bs):
+    """Shapes whose decode kernel has no shared-prefix instance (fp32, the
+    CUDA-core and mma.sync kernels, the TMA kernel at head dims other than 64
+    and 128) run the plain decode in every mode."""
+    q, kc, vc, bt, sl, members = shared_batch(hq, hkv, d, bs, [(4, [100, 70, 65])], [30],
                                               dtype=dtype, seed=3)
-    assert pa.decode_path(hq, kc) != 1
+    assert pa.decode_shared_prefix_mode(hq, 4, kc, pa.SHARED_ONCE) == 0
     scale = 1 / math.sqrt(d)
     out = run_shared(cuda_device, q, kc, vc, bt, sl, members, scale, partition_tokens=32)
     atol, rtol = tolerance(dtype)
