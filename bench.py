@@ -361,11 +361,15 @@ def time_oracle_prefill(wl, budget_s: float, piece: int = 256) -> dict:
                       f"oracle with OpenMP, {elapsed:.1f} s"}
 
 
-def time_oracle_copy(args) -> dict:
-    """The oracle's block copy on the host, repeated for ~cpu_seconds."""
+def time_oracle_copy(args):
+    """The oracle's block copy on the host, repeated for ~cpu_seconds; returns
+    the timing and the workload it copied."""
     import oracle
-    wl = workloads.copy_pairs() if args.workload == "copy" else \
-        workloads.copy_pairs(num_blocks=8192, num_pairs=2048)
+    if args.workload == "copy":
+        wl = (workloads.copy_pairs(num_blocks=args.num_blocks, num_pairs=args.num_blocks // 4)
+              if args.num_blocks else workloads.copy_pairs())
+    else:
+        wl = workloads.copy_pairs(num_blocks=8192, num_pairs=2048)
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle.copy_blocks(wl.k_cache, wl.v_cache, wl.k_cache, wl.v_cache, wl.pairs)
@@ -376,7 +380,46 @@ def time_oracle_copy(args) -> dict:
     return {"value": reps * wl.copy_bytes() / el / 1e9, "unit": "GB/s", "cores": 1,
             "kind": "oracle", "seconds": round(el, 3), "steps": reps,
             "sample": f"{reps} oracle block-copy call(s) of {wl.pairs.shape[0]} pairs "
-                      "(sequential memcpy), 1 thread"}
+                      "(sequential memcpy), 1 thread"}, wl
+
+
+# ---- the workload's description (shared by both arms' JSON lines) -------------------
+
+def parallelism(world: int) -> str:
+    return f"replicas x{world}" if world > 1 else "single GPU"
+
+
+def decode_config(args, wl, world: int) -> dict:
+    """The decode line's workload, identical in the GPU and reference arms."""
+    b0 = step_bytes(wl, 0, split_traffic=False)
+    return {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+            "overrides": overrides_json(args) or None,
+            "write": "device slots from (seq, position)" if args.positions else "slot_mapping",
+            "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+            "block_size": wl.block_size, "max_seq_len": wl.max_seq_len, "seed": wl.seed,
+            "block_utilization": wl.stats.get("block_utilization"),
+            "shared_prefix_groups": len(wl.prefix_groups),
+            "l2": f"inputs larger than L2: {b0['unique_kv'] / 2**20:.0f} MiB of K/V "
+                  f"per step vs {L2_BYTES / 2**20:.0f} MiB L2",
+            "parallelism": parallelism(world)}
+
+
+def prefill_config(args, wl, world: int) -> dict:
+    st = wl.steps[0]
+    by = step_bytes(wl, 0, split_traffic=False)
+    return {"workload": WORKLOAD_TEXT["prefill"], "name": "prefill",
+            "overrides": overrides_json(args) or None, "num_seqs": wl.num_seqs,
+            "query_rows": int(st.query_start[-1]), "max_seq_len": int(st.seq_lens.max()),
+            "l2": f"inputs larger than L2: {by['unique_kv'] / 2**20:.0f} MiB of K/V",
+            "parallelism": parallelism(world)}
+
+
+def copy_config(args, wl, pairs_per_call: int, step_bytes_: int, world: int) -> dict:
+    return {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+            "pairs_per_call": pairs_per_call,
+            "l2": f"inputs larger than L2: {step_bytes_ / 2 / 2**20:.0f} MiB read per step",
+            "parallelism": parallelism(world)}
 
 
 # ---- GPU arm ------------------------------------------------------------------------
@@ -431,19 +474,20 @@ def run_ours(args, rank, world, device):
             pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
         decode(k)
 
-    for w in range(args.warmup):
-        step(w % nsteps_wl)
-    torch.cuda.synchronize(device)
-    if pa.last_device_error() != 0:
-        raise RuntimeError("device error flag raised during warm-up")
-
     # The step loop: nothing between the steps' kernels, exactly as a user's
     # loop would issue them (an event between two kernels would stop the
-    # programmatic-launch overlap).
+    # programmatic-launch overlap).  The warm-up steps run inside the clock
+    # sampler's window, right before the timed ones, so the GPU does not sit
+    # idle (and ramp down) between them.
     K = args.steps
-    rank_barrier()
-    torch.cuda.synchronize(device)
     with ClockSampler(device.index or 0) as clocks:
+        for w in range(args.warmup):
+            step(w % nsteps_wl)
+        torch.cuda.synchronize(device)
+        if pa.last_device_error() != 0:
+            raise RuntimeError("device error flag raised during warm-up")
+        rank_barrier()
+        torch.cuda.synchronize(device)
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
@@ -490,25 +534,15 @@ def run_ours(args, rank, world, device):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_name(wl.dtype),
         "data": "synthetic (seeded N(0,1) K/V/q; tables from a shuffled block pool)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
-                   "overrides": overrides_json(args) or None,
-                   "write": "device slots from (seq, position)" if args.positions
-                            else "slot_mapping",
-                   "decode": ("pa_decode_shared_prefix, automatic mode (%s): %d group(s), "
-                              "%s shared blocks"
-                              % ("shared blocks read once" if once
-                                 else "plain decode: reading them once would not pay here",
-                                 len(wl.prefix_groups),
-                                 "/".join(str(b) for _, b in wl.prefix_groups))
-                              if shared else "pa_decode"),
-                   "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
-                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
-                   "block_size": wl.block_size, "max_seq_len": max(maxlens),
-                   "partition_tokens": b0["partition"], "seed": wl.seed,
-                   "block_utilization": wl.stats.get("block_utilization"),
-                   "l2": f"inputs larger than L2: {b0['unique_kv'] / 2**20:.0f} MiB of K/V "
-                         f"per step vs {L2_BYTES / 2**20:.0f} MiB L2",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": decode_config(args, wl, world),
+        "kernel_config": {
+            "partition_tokens": b0["partition"],
+            "decode": ("pa_decode_shared_prefix, automatic mode (%s): %d group(s), "
+                       "%s shared blocks"
+                       % ("shared blocks read once" if once
+                          else "plain decode: reading them once would not pay here",
+                          len(wl.prefix_groups), "/".join(str(b) for _, b in wl.prefix_groups))
+                       if shared else "pa_decode")},
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "decode_tokens_per_s_per_layer": round(world * seqs / (total_ms / 1e3), 1),
@@ -551,9 +585,11 @@ def time_decode_calls(decode, nsteps, bytes_, device, stream, peak, peak_kind,
     calls = max(ROOF_MIN_CALLS, math.ceil(ROOF_MIN_MS / max(est, 1e-3)))
     calls = max_over_ranks(float(calls), device)      # every rank issues the same block
     calls = int(calls)
-    rank_barrier()
-    torch.cuda.synchronize(device)
     with ClockSampler(device.index or 0) as clocks:
+        for c in range(10):                           # busy again after the sampler's start
+            decode(c % nsteps)
+        rank_barrier()
+        torch.cuda.synchronize(device)
         a.record(stream)
         for c in range(calls):
             decode(c % nsteps)
@@ -688,11 +724,7 @@ def run_prefill(args, rank, world, device):
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(wl.dtype),
         "data": "synthetic (seeded N(0,1) K/V/q; tables from a shuffled block pool)",
-        "config": {"workload": WORKLOAD_TEXT["prefill"], "name": "prefill",
-                   "overrides": overrides_json(args) or None, "num_seqs": wl.num_seqs,
-                   "query_rows": int(st.query_start[-1]), "max_seq_len": max_len,
-                   "l2": f"inputs larger than L2: {by['unique_kv'] / 2**20:.0f} MiB of K/V",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": prefill_config(args, wl, world),
         "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2),
         "prefill_tflops": round(tflops, 1),
         "roofline": {"bound": "tensor", "kernel": "pa_prefill call (tcgen05 bf16)",
@@ -797,10 +829,7 @@ def run_copy(args, rank, world, device):
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) blocks, shuffled pool)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
-                   "pairs_per_call": int(calls[0][4].shape[0]),
-                   "l2": f"inputs larger than L2: {step_bytes_ / 2 / 2**20:.0f} MiB read per step",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": copy_config(args, wl, int(calls[0][4].shape[0]), step_bytes_, world),
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "bytes_per_step": step_bytes_,
@@ -973,18 +1002,21 @@ def dtype_name(dt) -> str:
     return "f32" if dt == torch.float32 else "bf16"
 
 
-def run_reference(args, rank):
-    """The oracle as the reference arm: bounded full steps on the host cores."""
+def run_reference(args, rank, world=1):
+    """The oracle as the reference arm: bounded full steps on the host cores.
+    Its config is the GPU arm's (the same workload description)."""
     if rank != 0:
         return None
     if args.workload in ("copy", "swap"):
-        cpu = time_oracle_copy(args)
+        cpu, wl = time_oracle_copy(args)
+        n_pairs = int(wl.pairs.shape[0])
+        sb = wl.copy_bytes() if args.workload == "copy" else 2 * wl.copy_bytes()
         return {"impl": "reference", "metric": METRIC, "value": round(cpu["value"], 4),
                 "unit": "GB/s", "n_gpus": 0, "steps": cpu["steps"], "warmup": 0,
                 "ms_per_step": round(1e3 * cpu["seconds"] / cpu["steps"], 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+                "config": copy_config(args, wl, n_pairs, sb, world),
                 "cpu_baseline": cpu,
                 "e2e": {"value": round(cpu["value"], 4), "unit": "GB/s",
                         "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -996,9 +1028,9 @@ def run_reference(args, rank):
             "unit": "GB/s", "n_gpus": 0, "steps": cpu["steps"], "warmup": 0,
             "ms_per_step": round(1e3 * cpu["seconds"] / cpu["steps"], 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload],
-                                            "name": args.workload,
-                                            "overrides": overrides_json(args) or None},
+            "data": "synthetic",
+            "config": (prefill_config(args, wl, world) if args.workload == "prefill"
+                       else decode_config(args, wl, world)),
             "cpu_baseline": cpu,
             "e2e": {"value": round(cpu["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -1045,7 +1077,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
-        res = run_reference(args, rank)
+        res = run_reference(args, rank, world)
         if res is not None:
             print(json.dumps(res), flush=True)
         return

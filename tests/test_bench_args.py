@@ -50,3 +50,20 @@ def test_default_line_is_the_long_context_decode():
     assert "131072" in bench.WORKLOAD_TEXT[args.workload]
     # the roofline block is long enough to be a per-call mean, not a sample
     assert bench.ROOF_MIN_CALLS >= 200 and bench.ROOF_SAMPLED >= 20
+
+
+def test_reference_arm_describes_the_same_workload():
+    """The reference arm's config is built by the GPU arm's own function, so
+    the two lines of one command name the same workload."""
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "mha",
+                        "--num-seqs", "2", "--num-blocks", "512", "--steps", "1",
+                        "--cpu-seconds", "0.2"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
+    from paged_kv_cache_109_gb300 import workloads
+    args = bench.make_parser().parse_args(["--workload", "mha", "--num-seqs", "2",
+                                           "--num-blocks", "512"])
+    wl = workloads.make("mha", **bench.overrides(args))
+    assert line["config"] == json.loads(json.dumps(bench.decode_config(args, wl, 1)))
+    assert line["impl"] == "reference" and line["config"]["num_seqs"] == 2
