@@ -67,7 +67,7 @@ def test_reference_arm_under_torchrun_two_ranks():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr=127.0.0.1", f"--master-port={_free_port()}", "bench.py",
            "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
-           "--workload", "mha", "--cpu-seconds", "1"]
+           "--workload", "mha", "--num-seqs", "4", "--num-blocks", "512", "--cpu-seconds", "1"]
     res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert res.returncode == 0, res.stderr[-2000:]
     lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
