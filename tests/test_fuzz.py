@@ -209,3 +209,33 @@ def test_fuzz_portable_shapes(cuda_device, seed):
     assert_close(outp.cpu().double().numpy(), oracle.prefill(qp, qs, kc, vc, bt, sl, scale),
                  atol, rtol, "prefill " + what)
     assert pa.last_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_fuzz_shared_prefix_decode(cuda_device, seed):
+    """Random groups sharing leading blocks (sizes, shared block counts,
+    members shorter than the shared blocks, sequences in no group), group
+    sizes, head dims, block sizes and partitions: the shared-prefix decode
+    with the shared blocks read once against the oracle's plain decode."""
+    from tests.test_shared_prefix import run_shared, shared_batch
+    rng = np.random.default_rng(5000 + seed)
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    g = int(rng.choice([1, 2, 4, 8, 16, 32]))
+    d = int(rng.choice([64, 128]))
+    bs = int(rng.choice([8, 16, 32, 64]))
+    groups = []
+    for _ in range(int(rng.integers(1, 4))):
+        blocks = int(rng.integers(0, 11))
+        lens = [int(rng.integers(0, blocks * bs + 300)) for _ in range(int(rng.integers(1, 7)))]
+        groups.append((blocks, lens))
+    singles = [int(rng.integers(1, 700)) for _ in range(int(rng.integers(0, 5)))]
+    if max(max(lens) for _, lens in groups) == 0 and not singles:
+        singles = [5]
+    q, kc, vc, bt, sl, members = shared_batch(hkv * g, hkv, d, bs, groups, singles, seed=seed)
+    part = 0 if rng.random() < 0.5 else bs * int(rng.integers(1, 9))
+    scale = float(rng.uniform(0.5, 1.5)) / math.sqrt(d)
+    out = run_shared(cuda_device, q, kc, vc, bt, sl, members, scale, partition_tokens=part)
+    what = f"hq={hkv * g} hkv={hkv} d={d} B={bs} groups={groups} singles={singles} part={part}"
+    assert_close(out.double().numpy(), oracle.decode(q, kc, vc, bt, sl, scale), BF16_ATOL,
+                 BF16_RTOL, what)
+    assert pa.last_device_error() == 0

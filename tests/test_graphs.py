@@ -142,3 +142,44 @@ def test_back_to_back_steps_without_synchronising(cuda_device):
                              f"step {i // 2} partition {part}")
                 i += 1
     assert torch.equal(kd.cpu(), kh) and torch.equal(vd.cpu(), vh)
+
+
+def test_shared_prefix_decode_replays_in_a_graph(cuda_device):
+    """pa_decode_shared_prefix (shared blocks read once) captured on static
+    buffers: each replay decodes whatever q and lengths hold at that time,
+    with the groups' arrays fixed."""
+    from tests.test_shared_prefix import shared_batch
+    dev = cuda_device
+    q, kc, vc, bt, sl, members = shared_batch(32, 8, 128, 16, [(6, [200, 150, 300, 97])],
+                                              [60, 400], seed=11)
+    kd, vd = kc.to(dev), vc.to(dev)
+    max_len = bt.shape[1] * 16                     # the tables' reach: a host bound
+    grp = pa.prefix_groups(members, q.shape[0], dev)
+    need = pa.decode_shared_prefix_workspace_bytes(q.shape[0], 32, max_len, 6, kd, 64)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    q_s, lens_s, bt_s = q.to(dev), sl.to(dev), bt.to(dev)
+    scale = 1 / math.sqrt(128)
+
+    def call():
+        return pa.decode_shared_prefix(q_s, kd, vd, bt_s, lens_s, max_len, grp, scale,
+                                       workspace=ws, partition_tokens=64, mode=pa.SHARED_ONCE)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        call()                                     # warm-up outside the capture
+    torch.cuda.current_stream(dev).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out_s = call()
+    g = torch.Generator().manual_seed(12)
+    for s in range(3):
+        q2 = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+        lens = torch.clamp(sl - s, min=0)          # the tables cover every length up to sl
+        q_s.copy_(q2)
+        lens_s.copy_(lens)
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = oracle.decode(q2, kc, vc, bt, lens, scale)
+        assert_close(out_s.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, f"replay {s}")
+    assert pa.last_device_error() == 0
