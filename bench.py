@@ -37,7 +37,6 @@ from paged_kv_cache_109_gb300 import workloads  # noqa: E402
 
 METRIC = "paged decode KV GB/s and % of GB300 HBM peak; decode tokens/s per layer"
 L2_BYTES = 129 * 1024 * 1024
-DEC_SAMPLE = 8          # prefill / copy calls bracketed by events: every 8th step
 ROOF_MIN_CALLS = 200    # the roofline block: at least this many back-to-back decode calls
 ROOF_MIN_MS = 250.0     # ... and at least this long (several clock samples)
 ROOF_SAMPLED = 50       # isolated decode calls, each between its own events (quantiles)
@@ -558,72 +557,84 @@ def run_ours(args, rank, world, device):
     return result
 
 
-def time_decode_calls(decode, nsteps, bytes_, device, stream, peak, peak_kind,
-                      ms_per_step) -> dict:
-    """The roofline figure of the pa_decode call (partition kernel + merge).
+def time_calls(call, n_distinct, device, stream) -> dict:
+    """A library call's time, the way every line's roofline takes it.
 
     Block: at least ROOF_MIN_CALLS calls and ROOF_MIN_MS milliseconds issued
     back to back on the caller's stream between one pair of CUDA events, with
-    nothing between the calls (programmatic-launch overlap intact); achieved =
-    the calls' algorithmic bytes / the block's time, so the mean call.  Clocks
-    are sampled over the block.  Then ROOF_SAMPLED isolated calls, each
-    between its own pair of events, give the median and p10/p90 of one call
-    (an event between calls stops the overlap, so these include the launch).
-    Self-check: the block's mean call must not be longer than a whole step
-    (write + decode) of the step loop, within ROOF_STEP_SLACK."""
-    # one call's time, to size the block
+    nothing between the calls (programmatic-launch overlap intact), so the
+    block's time / calls is the mean call.  Clocks are sampled over the block.
+    Then ROOF_SAMPLED isolated calls, each between its own pair of events,
+    give the median and p10/p90 of one call (an event between calls stops the
+    overlap, so these include the launch).  call(c) issues call number c
+    (c % n_distinct picks the inputs)."""
     for c in range(3):
-        decode(c % nsteps)
+        call(c % n_distinct)
     torch.cuda.synchronize(device)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for c in range(10):
-        decode(c % nsteps)
+        call(c % n_distinct)
     b.record(stream)
     torch.cuda.synchronize(device)
-    est = a.elapsed_time(b) / 10
+    est = a.elapsed_time(b) / 10                       # one call's time, to size the block
     calls = max(ROOF_MIN_CALLS, math.ceil(ROOF_MIN_MS / max(est, 1e-3)))
-    calls = max_over_ranks(float(calls), device)      # every rank issues the same block
-    calls = int(calls)
+    calls = int(max_over_ranks(float(calls), device))  # every rank issues the same block
     with ClockSampler(device.index or 0) as clocks:
         for c in range(10):                           # busy again after the sampler's start
-            decode(c % nsteps)
+            call(c % n_distinct)
         rank_barrier()
         torch.cuda.synchronize(device)
         a.record(stream)
         for c in range(calls):
-            decode(c % nsteps)
+            call(c % n_distinct)
         b.record(stream)
         torch.cuda.synchronize(device)
     rank_barrier()
     block_ms = max_over_ranks(a.elapsed_time(b), device)
-    block_bytes = sum(bytes_[c % nsteps]["decode"] for c in range(calls))
-    achieved = block_bytes / (block_ms / 1e3) / 1e9
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(ROOF_SAMPLED)]
     for c, (e0, e1) in enumerate(evs):
         e0.record(stream)
-        decode(c % nsteps)
+        call(c % n_distinct)
         e1.record(stream)
     torch.cuda.synchronize(device)
     one = [e0.elapsed_time(e1) for e0, e1 in evs]
     q = statistics.quantiles(one, n=10)
-    mean_ms = block_ms / calls
+    return {"calls": calls, "block_ms": block_ms, "mean_ms": block_ms / calls,
+            "median_ms": statistics.median(one), "p10_ms": q[0], "p90_ms": q[-1],
+            "sampled": len(one), "clocks": clocks.summary()}
+
+
+def roofline_fields(t: dict, what: str, prefix: str, ms_per_step: float) -> dict:
+    """The block timing's keys of a line's roofline object."""
+    return {"timed_launches": t["calls"], "block_ms": round(t["block_ms"], 3),
+            f"{prefix}_ms_mean": round(t["mean_ms"], 5),
+            f"{prefix}_ms_median": round(t["median_ms"], 5),
+            f"{prefix}_ms_p10": round(t["p10_ms"], 5), f"{prefix}_ms_p90": round(t["p90_ms"], 5),
+            "sampled_calls": t["sampled"],
+            "per_call_le_step": bool(t["mean_ms"] <= ms_per_step * ROOF_STEP_SLACK),
+            "clocks": t["clocks"],
+            "how": f"{t['calls']} {what} back to back on the caller's stream between one pair "
+                   f"of CUDA events (achieved = their algorithmic work / that time); median "
+                   f"and p10/p90 from {t['sampled']} isolated calls, each between its own "
+                   f"events"}
+
+
+def time_decode_calls(decode, nsteps, bytes_, device, stream, peak, peak_kind,
+                      ms_per_step) -> dict:
+    """The roofline figure of the pa_decode call (partition kernel + merge):
+    time_calls' block, achieved = the calls' algorithmic bytes / its time.
+    Self-check: the block's mean call must not be longer than a whole step
+    (write + decode) of the step loop, within ROOF_STEP_SLACK."""
+    t = time_calls(decode, nsteps, device, stream)
+    block_bytes = sum(bytes_[c % nsteps]["decode"] for c in range(t["calls"]))
+    achieved = block_bytes / (t["block_ms"] / 1e3) / 1e9
     return {"bound": "hbm", "kernel": "pa_decode call (partition kernel + merge)",
             "achieved": round(achieved, 2), "peak": peak,
             "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "timed_launches": calls, "block_ms": round(block_ms, 3),
-            "decode_ms_mean": round(mean_ms, 5),
-            "decode_ms_median": round(statistics.median(one), 5),
-            "decode_ms_p10": round(q[0], 5), "decode_ms_p90": round(q[-1], 5),
-            "sampled_calls": len(one),
-            "per_call_le_step": bool(mean_ms <= ms_per_step * ROOF_STEP_SLACK),
-            "clocks": clocks.summary(),
-            "how": f"{calls} pa_decode calls back to back on the caller's stream between "
-                   f"one pair of CUDA events (achieved = their algorithmic bytes / that "
-                   f"time); median and p10/p90 from {len(one)} isolated calls, each between "
-                   f"its own events"}
+            **roofline_fields(t, "pa_decode calls", "decode", ms_per_step)}
 
 
 def prefill_flops(wl) -> int:
@@ -652,40 +663,36 @@ def run_prefill(args, rank, world, device):
     max_len = int(st.seq_lens.max())
     stream = torch.cuda.current_stream(device)
 
-    def step(ev=None):
-        pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
-        if ev is not None:
-            ev[0].record(stream)
+    def prefill_call(_=0):
         pa.prefill(d["q"], d["query_start"], kc, vc, d["block_tables"], d["seq_lens"], max_q,
                    max_len, wl.scale, out=out)
-        if ev is not None:
-            ev[1].record(stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(device)
+    def step():
+        pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
+        prefill_call()
+
     K = args.steps
-    sampled = list(range(0, K, DEC_SAMPLE))
-    evs = {it: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for it in sampled}
-    rank_barrier()
-    torch.cuda.synchronize(device)
     with ClockSampler(device.index or 0) as clocks:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(device)
+        rank_barrier()
+        torch.cuda.synchronize(device)
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for it in range(K):
-            step(evs.get(it))
+            step()
         end.record(stream)
         torch.cuda.synchronize(device)
     rank_barrier()
     total_ms = max_over_ranks(start.elapsed_time(end), device)
     if pa.last_device_error() != 0:
         raise RuntimeError("device error flag raised in the timed region")
-    pre_ms = [evs[it][0].elapsed_time(evs[it][1]) for it in sampled]
+    tcalls = time_calls(prefill_call, 1, device, stream)
     flops = prefill_flops(wl)
     by = step_bytes(wl, 0, split_traffic=False)
     step_b = by["decode"] + by["write"]
-    tflops = flops / (statistics.mean(pre_ms) / 1e3) / 1e12
+    tflops = flops * tcalls["calls"] / (tcalls["block_ms"] / 1e3) / 1e12
     peak_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         peak = float(json.load(open(peak_path))["bf16_tflops_sustained"])
@@ -731,7 +738,8 @@ def run_prefill(args, rank, world, device):
                      "achieved": round(tflops, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                      "traffic": None if overrides(args) else measured_traffic("prefill"),
-                     "flops_per_call": flops, "prefill_ms_mean": round(statistics.mean(pre_ms), 4)},
+                     "flops_per_call": flops,
+                     **roofline_fields(tcalls, "pa_prefill calls", "prefill", total_ms / K)},
         "e2e": e2e,
         "gpu_launches": 2 * K,
         "clocks": clocks.summary(),
@@ -765,47 +773,42 @@ def run_copy(args, rank, world, device):
         calls = [(kc, vc, host_k, host_v, to_host), (host_k, host_v, kc, vc, from_host)]
         step_bytes_ = 2 * wl.copy_bytes()
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def step(_=0):
         for c in calls:
             pa.copy_blocks(*c)
-        if ev is not None:
-            ev[1].record(stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(device)
     K = args.steps
-    sampled = list(range(0, K, DEC_SAMPLE))
-    evs = {it: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for it in sampled}
-    rank_barrier()
-    torch.cuda.synchronize(device)
     with ClockSampler(device.index or 0) as clocks:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(device)
+        rank_barrier()
+        torch.cuda.synchronize(device)
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for it in range(K):
-            step(evs.get(it))
+            step()
         end.record(stream)
         torch.cuda.synchronize(device)
     rank_barrier()
     total_ms = max_over_ranks(start.elapsed_time(end), device)
     if pa.last_device_error() != 0:
         raise RuntimeError("device error flag raised in the timed region")
-    call_ms = [evs[it][0].elapsed_time(evs[it][1]) for it in sampled]
-    achieved = step_bytes_ / (statistics.mean(call_ms) / 1e3) / 1e9
+    tcalls = time_calls(step, 1, device, stream)
+    achieved = step_bytes_ * tcalls["calls"] / (tcalls["block_ms"] / 1e3) / 1e9
     value = world * K * step_bytes_ / (total_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
     if args.workload == "copy":
         roof = {"bound": "hbm", "kernel": "pa_copy_blocks call", "achieved": round(achieved, 2),
                 "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind} (a copy, like this kernel)",
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": None if args.num_blocks else measured_traffic("copy")}
+                "traffic": None if args.num_blocks else measured_traffic("copy"),
+                **roofline_fields(tcalls, "pa_copy_blocks calls", "copy", total_ms / K)}
     else:
         roof = {"bound": "host link", "kernel": "pa_copy_blocks calls (out + in)",
                 "achieved": round(achieved, 2), "peak": None, "unit": "GB/s", "frac": None,
-                "traffic": None, "note": "device <-> page-locked host copies; no HBM roofline"}
+                "traffic": None, "note": "device <-> page-locked host copies; no HBM roofline",
+                **roofline_fields(tcalls, "swap steps (out + in)", "swap", total_ms / K)}
     # end to end: pairs from pinned host memory each step, one block read back
     host_pairs = [c[4].cpu().pin_memory() for c in calls]
     dev_pairs = [torch.empty_like(c[4]) for c in calls]
