@@ -236,7 +236,10 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * may be shorter than the shared blocks: it sees only its own T_i keys.
  *
  * seq_group      device or pinned int32 [num_seqs]: k for a member of group k,
- *                -1 for a sequence in no group.
+ *                -1 (or any negative value) for a sequence in no group.  It must
+ *                agree with the member lists: a sequence listed in a group but
+ *                not marked here, or the reverse, gets an undefined output
+ *                (refused under PA_DEBUG).
  * member_start   device or pinned int32 [num_groups + 1], from 0, non-decreasing.
  * members        device or pinned int32 [member_start[num_groups]], sequence ids.
  * prefix_blocks  device or pinned int32 [num_groups], each in [0, max_prefix_blocks].
