@@ -262,3 +262,24 @@ def test_automatic_mode_reads_once_only_where_it_pays(cuda_device):
     f32 = torch.empty(1, 8, 16, 128, dtype=torch.float32)
     assert pa.decode_shared_prefix_mode(32, 1024, f32, pa.SHARED_ONCE) == 0   # plain kernel
     assert mode(32, 32, 7) < 0
+
+
+def test_debug_pass_refuses_seq_group_that_disagrees_with_members(cuda_device, monkeypatch):
+    """A member not marked in seq_group, and a sequence marked but not listed,
+    are refused under PA_DEBUG before launch (without it the output would be
+    undefined)."""
+    q, kc, vc, bt, sl, members = shared_batch(32, 8, 128, 16, [(4, [100, 90, 80])], [50],
+                                              seed=13)
+    dev = cuda_device
+    monkeypatch.setenv("PA_DEBUG", "1")
+    for bad in ("unmarked member", "marked outsider"):
+        grp = pa.prefix_groups(members, q.shape[0], dev)
+        if bad == "unmarked member":
+            grp.seq_group[members[0][0][1]] = -1
+        else:
+            grp.seq_group[int((grp.seq_group == -1).nonzero()[0])] = 0
+        with pytest.raises(pa.PaError) as e:
+            pa.decode_shared_prefix(q.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), sl.to(dev),
+                                    int(sl.max()), grp, 0.1, mode=pa.SHARED_ONCE)
+        assert e.value.status == pa.PA_ERR_INVALID_ARG, bad
+    assert pa.last_device_error() == 0                 # nothing was launched
