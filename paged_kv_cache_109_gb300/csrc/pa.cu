@@ -858,9 +858,9 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     constexpr int32_t kTilesPerCta = 2;
     a.scale_log2 = scale * kLog2e;
     // the tensor-core kernel takes its row maximum before scaling: scale >= 0
-    // (head dims 64 and 128: the decode kernel's other TMA head dims are not its)
-    const bool fast = path == 1 && (cache->head_dim == 64 || cache->head_dim == 128) &&
-                      a.tokens_per_tile > 0 && aligned(q, 16) && aligned(out, 16) &&
+    // (head dims 80-112 run in a 128-column tile whose columns past the head
+    // dim are zeros)
+    const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) && aligned(out, 16) &&
                       aligned(k_cache, 16) && aligned(v_cache, 16) && scale >= 0.f;
     cudaError_t err;
     if (fast) {
@@ -870,7 +870,7 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
         const int32_t per_cta = kTilesPerCta * a.tokens_per_tile;
         const int32_t tiles = std::max(1, (max_q_len + per_cta - 1) / per_cta);
         dim3 grid(tiles, cache->num_kv_heads, num_seqs);
-        if (cache->head_dim == 128) {
+        if (cache->head_dim > 64) {
             using Cfg = PrefillWsCfg<128, PA_PREFILL_KEYS>;
             auto kern = prefill_ws_kernel<128, PA_PREFILL_KEYS>;
             if (!set_smem(kern, Cfg::smem_bytes())) return PA_ERR_UNSUPPORTED;

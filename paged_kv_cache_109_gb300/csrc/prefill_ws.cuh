@@ -80,7 +80,7 @@ struct PrefillWsCfg {
     static constexpr uint32_t kTmemCols = 512;            // per tile: S (and P) at +0, O at +128
     static constexpr uint32_t kTileCols = 256;
     static constexpr uint32_t kOCol = 128;
-    static_assert(D == 64 || D == 128, "head_dim");
+    static_assert(D == 64 || D == 128, "tile width");
     static_assert(KEYS == 128, "key block: two 64-key halves");
     static_assert(kSlots >= 4, "ring");
 };
@@ -154,14 +154,17 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // rows past tpt * G (G not dividing 128) carry nothing: no Q, no output
     const bool row_ok = softmax && r < tpt * G && tok < ntok;
     const int32_t pos = pos0 + min(tok, ntok - 1);
-    const int64_t row_elem = ((int64_t)(q0 + tok0 + tok) * a.num_q_heads + g * G + head) * D;
+    // the head dim; the tile is D columns (head dims 80-112 in a 128-column
+    // tile: the columns past hd are zeros in Q, K and V and never stored)
+    const int32_t hd = a.head_dim;
+    const int64_t row_elem = ((int64_t)(q0 + tok0 + tok) * a.num_q_heads + g * G + head) * hd;
     if (softmax) {
         // Q row -> shared memory, 128-byte swizzle per 64-column slice
         const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
 #pragma unroll
         for (int32_t c = 0; c < D / 8; ++c) {
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (row_ok) v = *reinterpret_cast<const uint4*>(q + row_elem + c * 8);
+            if (row_ok && c * 8 < hd) v = *reinterpret_cast<const uint4*>(q + row_elem + c * 8);
             const int32_t h = c >> 3, cc = c & 7;
             *reinterpret_cast<uint4*>(sm + C::kQOff + w * C::kQTile + h * C::kQSlice + r * 128 +
                                       ((cc ^ (r & 7)) << 4)) = v;
@@ -329,12 +332,16 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     if (!ok) break;
                 }
                 if (kb < nb && leader) {
-                    // S_t(kb) = Q_t K(kb)^T over the columns P_t(kb - 1) occupied
+                    // S_t(kb) = Q_t K(kb)^T over the columns P_t(kb - 1) occupied,
+                    // k-steps of the head dim only
 #pragma unroll
-                    for (int32_t k = 0; k < D / 16; ++k)
-                        umma_bf16(s_t, qdesc[t] + (uint64_t)((k >> 2) * (C::kQSlice >> 4) + (k & 3) * 2),
-                                  kdesc + (uint64_t)((k >> 2) * (C::kSlice >> 4) + (k & 3) * 2), kIdS,
-                                  k > 0 ? 1u : 0u);
+                    for (int32_t k = 0; k < D / 16; ++k) {
+                        if (k < hd / 16)
+                            umma_bf16(s_t,
+                                      qdesc[t] + (uint64_t)((k >> 2) * (C::kQSlice >> 4) + (k & 3) * 2),
+                                      kdesc + (uint64_t)((k >> 2) * (C::kSlice >> 4) + (k & 3) * 2),
+                                      kIdS, k > 0 ? 1u : 0u);
+                    }
                     umma_commit(s_full(t));
                 }
                 __syncwarp();
@@ -478,6 +485,7 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 if (row_ok) {
 #pragma unroll
                     for (int32_t q4 = 0; q4 < 4; ++q4) {
+                        if (cc * 32 + q4 * 8 >= hd) break;   // past the head dim
                         uint4 v;
                         v.x = pack_bf16x2(ov[q4 * 8 + 0] * inv, ov[q4 * 8 + 1] * inv);
                         v.y = pack_bf16x2(ov[q4 * 8 + 2] * inv, ov[q4 * 8 + 3] * inv);

@@ -66,6 +66,10 @@ FAST = [
     (28, 4, 128, 16, (300, 77), (200, 77)),                       # G=7: 18 tokens, 2 rows idle
     (40, 8, 128, 16, (150,), (150,)),                             # G=5: 25 tokens, 3 rows idle
     (24, 2, 64, 16, (61, 130), (61, 40)),                         # G=12: 10 tokens, 8 rows idle
+    (32, 8, 96, 16, (300, 17, 1000), (300, 5, 100)),              # D=96 in a 128-column tile
+    (32, 32, 80, 16, (70, 129), (70, 33)),                        # D=80, MHA
+    (64, 8, 112, 32, (257, 40), (100, 40)),                       # D=112, G=8, B=32
+    (40, 8, 96, 8, (150, 3), (150, 3)),                           # D=96, G=5, B=8
 ]
 
 
