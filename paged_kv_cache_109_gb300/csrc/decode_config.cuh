@@ -21,6 +21,9 @@
 #ifndef PA_MAX_PARTITION_TOKENS
 #define PA_MAX_PARTITION_TOKENS 1024
 #endif
+#ifndef PA_LONG_PARTITIONS
+#define PA_LONG_PARTITIONS 32   // TMA kernel: the cap rises to max_seq_len / this
+#endif
 
 namespace pa {
 namespace {
@@ -112,7 +115,14 @@ int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_le
     // chunk for each of their four warps, rounded up to whole blocks.  Aim for about
     // PA_TARGET_CTAS_PER_SM CTAs per SM over the batch (counted at
     // max_seq_len, sub-groups included), between one unit and
-    // PA_MAX_PARTITION_TOKENS tokens
+    // PA_MAX_PARTITION_TOKENS tokens.  On the TMA kernel the cap rises to
+    // max_seq_len / PA_LONG_PARTITIONS for sequences long enough that it
+    // binds: there the batch's CTA count never runs short, and fewer, longer
+    // partitions cost fewer partials to write and merge.  Measured on the
+    // long-context batch (4 x 131072, Hkv = 8, 1216 CTAs at the target): 1024
+    // tokens 1.034-1.037 of the copy peak per call, 2048 1.057, 3456 (the
+    // target) 1.070; the batches whose longest sequence is under 32768 tokens
+    // keep 1024, which measured best or within 1% for them.
     const int64_t chunks = mma ? 4 * 16
                                : (int64_t)kTiledWarps *
                                      tiled_chunk(c->head_dim, c->dtype == PA_F32 ? 4 : 2);
@@ -125,7 +135,8 @@ int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_le
     const int64_t target = (int64_t)PA_TARGET_CTAS_PER_SM * sms;
     int64_t p = (work + target - 1) / target;
     p = (p + unit - 1) / unit * unit;
-    const int64_t cap = std::max<int64_t>(unit, PA_MAX_PARTITION_TOKENS / unit * unit);
+    int64_t cap = std::max<int64_t>(unit, PA_MAX_PARTITION_TOKENS / unit * unit);
+    if (fast) cap = std::max<int64_t>(cap, (int64_t)max_seq_len / PA_LONG_PARTITIONS / unit * unit);
     p = std::min(std::max(p, unit), cap);
     if (fast) p = std::min<int64_t>(p, fast_max_partition(c));
     return (int32_t)p;
