@@ -350,11 +350,12 @@ pa_status launch_write(const void* k, const void* v, SlotFn slot_of, int32_t num
     if (row % vec || !aligned(k, vec) || !aligned(v, vec) || !aligned(k_cache, vec) ||
         !aligned(v_cache, vec))
         return PA_ERR_INVALID_ARG;
-    const int64_t total = (int64_t)num_tokens * 2 * cache->num_kv_heads * (row / vec);
-    const int threads = 256;
+    // one warp per token (kWriteWarps tokens a CTA), at most 16 CTAs per SM
+    // with a grid-stride loop past that
+    const int threads = 32 * kWriteWarps;
     const int64_t sms = std::max(1, device_sm_count());
     const unsigned blocks = (unsigned)std::max<int64_t>(
-        1, std::min<int64_t>((total + threads - 1) / threads, sms * 16));
+        1, std::min<int64_t>(((int64_t)num_tokens + kWriteWarps - 1) / kWriteWarps, sms * 16));
     const int64_t num_slots = (int64_t)cache->num_blocks * cache->block_size;
     auto go = [&](auto kern) {
         return launch_pdl(kern, dim3(blocks), dim3(threads), 0, st,

@@ -3,9 +3,9 @@
 // Token j with slot s = slot_mapping[j] >= 0 lands in block s / B, row s % B
 // of every kv head ("vLLM PagedAttention: from memory fragmentation to slot
 // mapping" §6; paper notes' block lifecycle: decode fills the next slot of the
-// last block).  Each thread moves one VEC-byte vector; consecutive threads
-// cover one (token, head) row, then the next head, then V, then the next
-// token, so both the read of k/v and the write of each cache row coalesce.
+// last block).  A warp moves one token's rows in VEC-byte vectors; consecutive
+// lanes cover one (token, head) row, then the next head, then V, so both the
+// read of k/v and the write of each cache row coalesce.
 #pragma once
 
 #include "common.cuh"
@@ -59,8 +59,17 @@ struct SlotFromPosition {
     }
 };
 
+// One warp per token (a grid-stride loop over tokens): every lane reads the
+// token's slot (one broadcast load), then the warp moves the token's
+// 2 * Hkv * row_bytes bytes, each lane issuing up to kWriteUnroll vector
+// loads before its stores, so a warp keeps 32 * kWriteUnroll vectors in
+// flight.  Vector x of a token is (K or V, head, piece): K rows first, head
+// by head, so consecutive lanes read and write consecutive bytes.
+constexpr int kWriteUnroll = 8;
+constexpr int kWriteWarps = 8;                  // warps per CTA
+
 template <int VEC, typename SlotFn>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(32 * kWriteWarps, 2)
 write_kv_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v, SlotFn slot_of,
                 int64_t num_tokens, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
                 int32_t num_kv_heads, int32_t block_size, int64_t num_slots,
@@ -68,30 +77,48 @@ write_kv_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v, Sl
     using V = typename VecType<VEC>::T;
     griddep_wait();                 // inputs may come from the previous kernel
     griddep_launch_dependents();    // the next kernel may start its prologue
-    const int64_t vecs_per_row = row_bytes / VEC;
-    const int64_t per_token = 2LL * num_kv_heads * vecs_per_row;
-    const int64_t total = num_tokens * per_token;
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t j = idx / per_token;
-        int64_t rem = idx - j * per_token;
-        const int which = rem >= num_kv_heads * vecs_per_row;   // 0 = K, 1 = V
-        rem -= which * num_kv_heads * vecs_per_row;
-        const int64_t h = rem / vecs_per_row;
-        const int64_t c = rem - h * vecs_per_row;
-        const bool first = which == 0 && h == 0 && c == 0;    // one report per token
-        const int64_t s = slot_of(j, first);
+    const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t vpr = row_bytes / VEC;                  // vectors per (token, head) row
+    const int32_t per_kind = num_kv_heads * vpr;           // vectors of K (or V) of a token
+    const int32_t per_token = 2 * per_kind;
+    for (int64_t j = (int64_t)blockIdx.x * kWriteWarps + warp; j < num_tokens;
+         j += (int64_t)gridDim.x * kWriteWarps) {
+        const int64_t s = slot_of(j, lane == 0);          // one report per token
         if (s < 0) continue;
         if (s >= num_slots) {
-            if (first) raise_error(PA_DEVERR_SLOT);
+            if (lane == 0) raise_error(PA_DEVERR_SLOT);
             continue;
         }
         const int64_t blk = s / block_size;
         const int64_t row = s - blk * block_size;
-        const uint8_t* src = (which ? v : k) + (j * num_kv_heads + h) * row_bytes + c * VEC;
-        uint8_t* dst = (which ? v_cache : k_cache) +
-                       ((blk * num_kv_heads + h) * block_size + row) * row_bytes + c * VEC;
-        *reinterpret_cast<V*>(dst) = *reinterpret_cast<const V*>(src);
+        const int64_t src0 = j * num_kv_heads * (int64_t)row_bytes;
+        // cache row of head h: ((blk * Hkv + h) * B + row) * row_bytes
+        const int64_t dst0 = (blk * num_kv_heads * block_size + row) * (int64_t)row_bytes;
+        const int64_t head_stride = (int64_t)block_size * row_bytes;
+        for (int32_t x0 = 0; x0 < per_token; x0 += 32 * kWriteUnroll) {
+            V buf[kWriteUnroll];
+#pragma unroll
+            for (int u = 0; u < kWriteUnroll; ++u) {
+                const int32_t x = x0 + u * 32 + lane;
+                if (x < per_token) {
+                    const int32_t which = x >= per_kind;      // 0 = K, 1 = V
+                    const int32_t y = x - which * per_kind;   // head * vpr + piece
+                    buf[u] = *reinterpret_cast<const V*>((which ? v : k) + src0 +
+                                                         (int64_t)y * VEC);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kWriteUnroll; ++u) {
+                const int32_t x = x0 + u * 32 + lane;
+                if (x < per_token) {
+                    const int32_t which = x >= per_kind;
+                    const int32_t y = x - which * per_kind;
+                    const int32_t h = y / vpr, c = y - h * vpr;
+                    *reinterpret_cast<V*>((which ? v_cache : k_cache) + dst0 +
+                                          h * head_stride + (int64_t)c * VEC) = buf[u];
+                }
+            }
+        }
     }
 }
 
