@@ -546,3 +546,22 @@ def test_unaligned_query_or_output(cuda_device, hq, hkv, d, bs, dtype, shift):
         assert_close(got.cpu().double().numpy(), oracle.decode(q, kc, vc, bt, sl, scale), atol,
                      rtol, f"shifted {shift}, partition {part}")
     assert pa.last_device_error() == 0
+
+
+@pytest.mark.slow
+def test_million_token_sequences(cuda_device):
+    """Two sequences of 2^20 tokens (1 GiB of K/V): the automatic partition
+    for very long sequences (its cap rises with the length: about 300
+    partitions a sequence, the merge's many-partition path) and an explicit
+    partition at the largest whole-table slice, against the oracle on every
+    (sequence, head)."""
+    T, bs, hkv, g, d = 1 << 20, 16, 2, 4, 64
+    q, kc, vc, bt, sl = synthetic(hkv * g, hkv, d, bs, (T, T - 5), seed=77)
+    scale = 1 / math.sqrt(d)
+    part = pa.decode_partition_tokens(2, hkv * g, T, kc)
+    assert part > 1024                                  # the long-sequence cap
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    for p in (0, 2048 * bs):
+        out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=p)
+        assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, f"million tokens, {p}")
+    assert pa.last_device_error() == 0
