@@ -259,8 +259,10 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  *                when enough reads are saved (measured: a 512-token prefix at
  *                4 query heads per kv head is 1.5% faster plain, a 4096-token
  *                one 16% faster once; one member per tile is 13% faster plain).
- * Other arguments as pa_decode.  A group id, member id or shared-block count
- * out of range on the device is skipped and reported (PA_DEVERR_GROUP).
+ * Other arguments as pa_decode.  A group id, member id, member list (offsets
+ * outside [0, member_start[num_groups]] or longer than max_group_size) or
+ * shared-block count out of range on the device is skipped and reported
+ * (PA_DEVERR_GROUP); the affected members' outputs are then undefined.
  * Shapes that pa_decode_path does not send to kernel 1, and num_groups == 0,
  * run the plain pa_decode over the same tables in every mode: same result.
  */

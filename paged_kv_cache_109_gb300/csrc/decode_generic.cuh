@@ -46,6 +46,7 @@ struct DecodeArgs {
     const int32_t* members;
     const int32_t* prefix_blocks;
     int32_t num_groups;
+    int32_t max_group_size;
     int32_t max_prefix_blocks;
     int32_t prefix_ztiles;   // grid z per group taken by its prefix CTAs
     int32_t prefix_z;        // num_groups * prefix_ztiles: z below this is a prefix CTA

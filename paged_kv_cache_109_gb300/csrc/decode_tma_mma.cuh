@@ -148,9 +148,16 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         direct = false;
         const int32_t z = blockIdx.z, k = z / a.prefix_ztiles;
         const int32_t rt = (z - k * a.prefix_ztiles) * a.sub_groups + sg;   // row tile
+        // member list [ms, ms + mc) inside members[0 .. member_start[num_groups])
+        // and within the host bound; anything else is reported and skipped
+        const int32_t total = a.member_start[a.num_groups];
         const int32_t ms = a.member_start[k], mc = a.member_start[k + 1] - ms;
+        if (ms < 0 || mc < 0 || ms + mc > total || mc > a.max_group_size) {
+            if (tid == 0) raise_error(PA_DEVERR_GROUP);
+            return;
+        }
         const int32_t pk = group_prefix_blocks(a, k) * BS;
-        if (mc <= 0 || t0 >= pk) return;
+        if (mc == 0 || t0 >= pk) return;
         if (tid < C::kRows) {
             // MMA row tid = pair rt * kRows + tid of the group's (member, head)
             // pairs, head fastest

@@ -563,6 +563,7 @@ pa_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
         a.members = sh->members;
         a.prefix_blocks = sh->prefix_blocks;
         a.num_groups = sh->num_groups;
+        a.max_group_size = sh->max_group_size;
         a.max_prefix_blocks = sh->max_prefix_blocks;
         a.prefix_ztiles = (int32_t)zt;
         a.prefix_z = (int32_t)pz;

@@ -283,3 +283,25 @@ def test_debug_pass_refuses_seq_group_that_disagrees_with_members(cuda_device, m
                                     int(sl.max()), grp, 0.1, mode=pa.SHARED_ONCE)
         assert e.value.status == pa.PA_ERR_INVALID_ARG, bad
     assert pa.last_device_error() == 0                 # nothing was launched
+
+
+def test_inconsistent_member_offsets_are_reported(cuda_device):
+    """member_start entries that leave [0, member_start[num_groups]] or run
+    backwards: the prefix CTAs read no member and report PA_DEVERR_GROUP;
+    the sequences in no group are still exact."""
+    q, kc, vc, bt, sl, members = shared_batch(32, 8, 128, 16, [(4, [100, 90]), (2, [70])], [50],
+                                              seed=14)
+    dev = cuda_device
+    grp = pa.prefix_groups(members, q.shape[0], dev)          # one group: the [70] one is dropped
+    bad = pa.PrefixGroups(grp.seq_group, torch.tensor([0, 3], dtype=torch.int32, device=dev),
+                          grp.members, grp.prefix_blocks, grp.max_group_size,
+                          grp.max_prefix_blocks)
+    # the group claims 3 members, more than max_group_size (2): refused before
+    # any member is read (members holds only 2)
+    out = pa.decode_shared_prefix(q.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), sl.to(dev),
+                                  int(sl.max()), bad, 0.1, partition_tokens=32,
+                                  mode=pa.SHARED_ONCE).cpu()
+    assert pa.last_device_error() & pa.DEVERR_GROUP
+    ref = oracle.decode(q, kc, vc, bt, sl, 0.1)
+    alone = (grp.seq_group == -1).cpu().numpy()
+    assert_close(out.double().numpy()[alone], ref[alone], BF16_ATOL, BF16_RTOL, "no-group rows")
