@@ -388,12 +388,44 @@ def parallelism(world: int) -> str:
     return f"replicas x{world}" if world > 1 else "single GPU"
 
 
+def appends_only(wl) -> bool:
+    """Whether every step writes exactly one token per sequence, at its last
+    position (a decode step): then the write can go inside the decode call."""
+    for st in wl.steps:
+        n = st.seq_lens.numel()
+        if st.seq_ids is None or st.seq_ids.numel() != n:
+            return False
+        if not torch.equal(st.seq_ids, torch.arange(n, dtype=torch.int32)):
+            return False
+        if not torch.equal(st.positions, st.seq_lens - 1):
+            return False
+    return True
+
+
+WRITE_TEXT = {"append": "each sequence's new token at position seq_lens - 1, written by the "
+                        "decode call itself (pa_decode_append)",
+              "positions": "device slots from (seq, position) (pa_write_kv_positions)",
+              "slot_mapping": "slot_mapping (pa_write_kv)"}
+
+
+def write_mode(args, wl) -> str:
+    """How a decode step writes its new tokens: fused into the decode call
+    where the steps are pure appends (automatic), else a cache-write call."""
+    mode = "positions" if args.positions else args.write
+    if mode == "auto":
+        return "append" if appends_only(wl) else "slot_mapping"
+    if mode == "append" and not appends_only(wl):
+        raise SystemExit(f"--write append: the {args.workload} steps write other tokens than "
+                         f"each sequence's last position")
+    return mode
+
+
 def decode_config(args, wl, world: int) -> dict:
     """The decode line's workload, identical in the GPU and reference arms."""
     b0 = step_bytes(wl, 0, split_traffic=False)
     return {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
             "overrides": overrides_json(args) or None,
-            "write": "device slots from (seq, position)" if args.positions else "slot_mapping",
+            "write": WRITE_TEXT[write_mode(args, wl)],
             "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
             "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
             "block_size": wl.block_size, "max_seq_len": wl.max_seq_len, "seed": wl.seed,
@@ -442,6 +474,14 @@ def run_ours(args, rank, world, device):
     # partials only when the shared blocks are read once
     once = shared and pa.decode_shared_prefix_mode(wl.num_q_heads, groups.max_prefix_blocks,
                                                    kc) == 1
+    mode = write_mode(args, wl)
+    if mode == "append" and once:
+        raise SystemExit("--write append: this batch's shared blocks are read once, which "
+                         "the fused call does not do; use --write slot_mapping")
+    # where the shared-prefix decode would run the plain decode anyway, the
+    # step's fused call is that same plain decode
+    if mode == "append":
+        shared = False
     bytes_ = [step_bytes(wl, k, shared_prefix=once) for k in range(nsteps_wl)]
     maxlens = [int(st.seq_lens.max()) for st in wl.steps]
     part = args.partition or 0
@@ -464,9 +504,18 @@ def run_ours(args, rank, world, device):
             pa.decode(d["q"], kc, vc, d["block_tables"], d["seq_lens"], maxlens[k], wl.scale,
                       out=outs[k], workspace=ws, partition_tokens=part)
 
+    def append(k):
+        d = dsteps[k]
+        pa.decode_append(d["q"], d["k_new"], d["v_new"], kc, vc, d["block_tables"],
+                         d["seq_lens"], maxlens[k], wl.scale, out=outs[k], workspace=ws,
+                         partition_tokens=part)
+
     def step(k):
         d = dsteps[k]
-        if args.positions:
+        if mode == "append":
+            append(k)
+            return
+        if mode == "positions":
             pa.write_kv_positions(d["k_new"], d["v_new"], d["seq_ids"], d["positions"],
                                   d["block_tables"], kc, vc)
         else:
@@ -505,18 +554,18 @@ def run_ours(args, rank, world, device):
     if err != 0:
         raise RuntimeError(f"device error flag {err} raised in the timed region")
 
-    roof = time_decode_calls(decode, nsteps_wl, bytes_, device, stream, peak, peak_kind,
-                             total_ms / K)
+    roof = time_decode_calls(append if mode == "append" else decode, nsteps_wl, bytes_, device,
+                             stream, peak, peak_kind, total_ms / K, fused=mode == "append")
     if pa.last_device_error() != 0:
         raise RuntimeError("device error flag raised in the roofline block")
 
     # end to end: host buffers, H2D of the step inputs and D2H of the output
     e2e = run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, world,
-                  shared)
+                  shared, fused=mode == "append")
 
     launches_per_step = []
     for k in range(nsteps_wl):
-        n = 1 if wl.steps[k].slot_mapping.numel() else 0
+        n = 1 if wl.steps[k].slot_mapping.numel() and mode != "append" else 0
         n += 1
         need = pa.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, maxlens[k], kc, part)
         n += 1 if need or shared else 0                # the merge
@@ -541,7 +590,14 @@ def run_ours(args, rank, world, device):
                        % ("shared blocks read once" if once
                           else "plain decode: reading them once would not pay here",
                           len(wl.prefix_groups), "/".join(str(b) for _, b in wl.prefix_groups))
-                       if shared else "pa_decode")},
+                       if shared else
+                       ("pa_decode_append (the write inside the decode kernel)%s"
+                        % ("; %d shared-prefix group(s): the shared-prefix decode's automatic "
+                           "mode runs the plain decode on this batch (reading the shared "
+                           "blocks once would not pay), which this call is"
+                           % len(wl.prefix_groups) if wl.prefix_groups and
+                           not args.no_shared_prefix else ""))
+                       if mode == "append" else "pa_decode")},
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "decode_tokens_per_s_per_layer": round(world * seqs / (total_ms / 1e3), 1),
@@ -622,19 +678,25 @@ def roofline_fields(t: dict, what: str, prefix: str, ms_per_step: float) -> dict
 
 
 def time_decode_calls(decode, nsteps, bytes_, device, stream, peak, peak_kind,
-                      ms_per_step) -> dict:
-    """The roofline figure of the pa_decode call (partition kernel + merge):
+                      ms_per_step, fused: bool = False) -> dict:
+    """The roofline figure of the decode call (partition kernel + merge):
     time_calls' block, achieved = the calls' algorithmic bytes / its time.
-    Self-check: the block's mean call must not be longer than a whole step
-    (write + decode) of the step loop, within ROOF_STEP_SLACK."""
+    With `fused` the call is pa_decode_append, whose bytes include the
+    append's (new rows read, cache rows written).  Self-check: the block's
+    mean call must not be longer than a whole step of the step loop, within
+    ROOF_STEP_SLACK."""
     t = time_calls(decode, nsteps, device, stream)
-    block_bytes = sum(bytes_[c % nsteps]["decode"] for c in range(t["calls"]))
+    keys = ("decode", "write") if fused else ("decode",)
+    block_bytes = sum(bytes_[c % nsteps][k] for c in range(t["calls"]) for k in keys)
     achieved = block_bytes / (t["block_ms"] / 1e3) / 1e9
-    return {"bound": "hbm", "kernel": "pa_decode call (partition kernel + merge)",
+    name = "pa_decode_append" if fused else "pa_decode"
+    what = ("partition kernel with the append + merge" if fused
+            else "partition kernel + merge")
+    return {"bound": "hbm", "kernel": f"{name} call ({what})",
             "achieved": round(achieved, 2), "peak": peak,
             "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            **roofline_fields(t, "pa_decode calls", "decode", ms_per_step)}
+            **roofline_fields(t, f"{name} calls", "decode", ms_per_step)}
 
 
 def prefill_flops(wl) -> int:
@@ -926,13 +988,14 @@ def pipelined_steps(host, outs_like, launch, K, device, stream):
 
 
 def run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, world=1,
-            shared=False):
+            shared=False, fused=False):
     """Same step through the public API from pinned host buffers: the step's
-    inputs (q, new K/V, slots, tables, lengths, and the shared-prefix groups
-    when used) packed in one page-locked buffer cross in one H2D copy; write +
-    decode; the output returns in one D2H copy (pipelined as in
-    pipelined_steps)."""
-    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens")
+    inputs (q, new K/V, slots unless the write is fused, tables, lengths, and
+    the shared-prefix groups when used) packed in one page-locked buffer cross
+    in one H2D copy; write + decode (one pa_decode_append call when fused);
+    the output returns in one D2H copy (pipelined as in pipelined_steps)."""
+    names = ("q", "k_new", "v_new", "block_tables", "seq_lens") if fused else \
+        ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens")
     gnames = ("seq_group", "member_start", "members", "prefix_blocks")
     hgroups = pa.prefix_groups(wl.prefix_groups, wl.num_seqs) if shared else None
     host = []
@@ -948,6 +1011,11 @@ def run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, wor
     K = max(1, min(args.steps, 200))
 
     def launch(k, d, out):
+        if fused:
+            pa.decode_append(d["q"], d["k_new"], d["v_new"], kc, vc, d["block_tables"],
+                             d["seq_lens"], maxlens[k], wl.scale, out=out, workspace=ws,
+                             partition_tokens=part)
+            return
         pa.write_kv(d["k_new"], d["v_new"], d["slot_mapping"], kc, vc)
         if shared:
             grp = pa.PrefixGroups(d["seq_group"], d["member_start"], d["members"],
@@ -967,9 +1035,11 @@ def run_e2e(args, wl, pa, kc, vc, ws, maxlens, part, device, stream, bytes_, wor
     return {"value": round(total / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
             "ms_per_step": round(ms / K, 5),
-            "how": "per step: one H2D copy of the packed inputs from pinned memory, write + "
-                   "decode, one D2H copy of the output to pinned memory; copies on their own "
-                   "streams, double-buffered, overlapping the neighbouring steps' kernels"}
+            "how": "per step: one H2D copy of the packed inputs from pinned memory, %s, one "
+                   "D2H copy of the output to pinned memory; copies on their own streams, "
+                   "double-buffered, overlapping the neighbouring steps' kernels"
+                   % ("pa_decode_append (write inside the decode)" if fused
+                      else "write + decode")}
 
 
 def overrides(args) -> dict:
@@ -1057,8 +1127,14 @@ def make_parser() -> argparse.ArgumentParser:
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="decode a workload with shared-prefix groups (gqa) with the plain "
                          "pa_decode instead of pa_decode_shared_prefix")
+    ap.add_argument("--write", choices=["auto", "append", "slot_mapping", "positions"],
+                    default="auto",
+                    help="how a decode step writes its new tokens: inside the decode call "
+                         "(append: steps that add one token per sequence at its last "
+                         "position), pa_write_kv with a slot mapping, or "
+                         "pa_write_kv_positions; auto = append where the steps allow it")
     ap.add_argument("--positions", action="store_true",
-                    help="write with slots computed on the device from (seq, position)")
+                    help="same as --write positions")
     ap.add_argument("--dtype", choices=["bf16", "f32"], default="bf16",
                     help="cache and q dtype of a decode workload (f32 runs the CUDA-core "
                          "decode kernel)")

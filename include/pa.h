@@ -214,6 +214,43 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     const pa_cache_desc* cache, void* stream);
 
 /*
+ * pa_decode_append -- one decode step in one call: each sequence's newest
+ * token is written to the caches, then pa_decode runs over the same
+ * arguments.  Sequence i's newest token is position T_i - 1 (T_i =
+ * seq_lens[i] counts it; "PagedAttention" glossary, upstream and downstream:
+ * decode appends one slot per step; "PagedAttention engineering notes"
+ * (nxmr.cn) §3.1: each generated token's K/V goes to the next slot of the
+ * sequence's current block), and its rows k_new[i], v_new[i] go to slot
+ * table[i][(T_i - 1) / B] * B + (T_i - 1) % B of both caches.  The caches and
+ * the output are bit for bit those of pa_write_kv_positions(k_new, v_new,
+ * seq_ids = 0 .. num_seqs - 1, positions = T_i - 1) followed by pa_decode.
+ *
+ * On the TMA decode kernel (pa_decode_path 1, k_new and v_new 16-byte
+ * aligned) the write is fused into the decode: the CTA whose partition holds
+ * position T_i - 1 attends to the new rows in place of the slot's old
+ * contents and stores them, so the step is one launch shorter.  Otherwise
+ * the cache write (slots from the lengths and tables) runs first, then the
+ * decode.
+ *
+ * k_new, v_new   device or pinned [num_seqs][num_kv_heads][head_dim], cache dtype.
+ * k_cache, v_cache  written at the appended slots.
+ * T_i == 0 appends nothing.  A length outside [0, min(max_seq_len,
+ * max_blocks_per_seq * B)] or a bad table entry at the appended position
+ * appends nothing and is reported (PA_DEVERR_SEQ_LEN, PA_DEVERR_TABLE_ENTRY),
+ * as pa_decode reports it.  The appended slot must belong to this sequence
+ * alone (a block shared with another table is copied first: pa_copy_blocks);
+ * two sequences appending to one slot is undefined.
+ * Other arguments, the workspace and the errors as pa_decode.
+ */
+pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
+                           void* k_cache, void* v_cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                           int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads,
+                           float scale, int32_t partition_tokens, void* out,
+                           void* workspace, size_t workspace_bytes,
+                           const pa_cache_desc* cache, void* stream);
+
+/*
  * pa_decode_shared_prefix -- pa_decode for a batch in which groups of
  * sequences share their leading blocks: a common prompt prefix held once and
  * referenced by several block tables ("vLLM source walkthrough: PagedAttention

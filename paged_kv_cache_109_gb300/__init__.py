@@ -21,8 +21,8 @@ from ._build import LIB as LIBRARY_PATH
 from ._build import build
 from .block_pool import BlockPool, SharedTailWrite
 
-__all__ = ["write_kv", "write_kv_positions", "copy_blocks", "decode", "decode_shared_prefix",
-           "prefix_groups", "PrefixGroups", "decode_shared_prefix_workspace_bytes",
+__all__ = ["write_kv", "write_kv_positions", "copy_blocks", "decode", "decode_append",
+           "decode_shared_prefix", "prefix_groups", "PrefixGroups", "decode_shared_prefix_workspace_bytes",
            "decode_shared_prefix_mode", "prefill",
            "decode_workspace_bytes", "decode_partition_tokens",
            "decode_path", "last_device_error", "PaError", "build", "BlockPool",
@@ -77,6 +77,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.pa_decode.argtypes = [P, P, P, P, I32, P, I32, I32, I32, ctypes.c_float, I32, P, P, SZ,
                               DP, P]
     lib.pa_decode.restype = ctypes.c_int
+    lib.pa_decode_append.argtypes = [P, P, P, P, P, P, I32, P, I32, I32, I32, ctypes.c_float,
+                                     I32, P, P, SZ, DP, P]
+    lib.pa_decode_append.restype = ctypes.c_int
     lib.pa_decode_shared_prefix_workspace_bytes.argtypes = [I32, I32, I32, I32, I32, DP]
     lib.pa_decode_shared_prefix_workspace_bytes.restype = SZ
     lib.pa_decode_shared_prefix.argtypes = [P, P, P, P, I32, P, I32, I32, I32, ctypes.c_float,
@@ -265,6 +268,45 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int,
         _ptr(seq_lens), n, max_seq_len, hq, float(scale), partition_tokens, _ptr(out),
         _ptr(workspace), ws_bytes, ctypes.byref(desc), _stream(stream))
     _check(st, "pa_decode")
+    return out
+
+
+def decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                  max_seq_len: int, scale: float | None = None, out=None, workspace=None,
+                  partition_tokens: int = 0, stream=None) -> torch.Tensor:
+    """One decode step in one call: sequence i's newest token, at position
+    seq_lens[i] - 1, takes the rows k_new[i], v_new[i] ([N, Hkv, D]) in both
+    caches, then the decode runs as ``decode`` does.  Caches and output equal
+    ``write_kv_positions`` (positions seq_lens - 1) followed by ``decode``,
+    bit for bit; on the TMA decode kernel the write is fused into it."""
+    _dev(k_cache, v_cache)
+    _dev_or_pinned(q, k_new, v_new, block_tables, seq_lens)
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_tables and seq_lens must be int32")
+    if k_new.dtype != k_cache.dtype or v_new.dtype != k_cache.dtype \
+            or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_new, v_new and caches must share one dtype")
+    desc = cache_desc(k_cache)
+    n, hq, d = q.shape
+    if k_new.shape != (n, desc.num_kv_heads, desc.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError(f"k_new, v_new must be [{n}, {desc.num_kv_heads}, {desc.head_dim}]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q, device=k_cache.device)
+    _dev_or_pinned(out)
+    need = decode_workspace_bytes(n, hq, max_seq_len, desc, partition_tokens)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=k_cache.device)
+    if workspace is not None:
+        _dev(workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().pa_decode_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), n, max_seq_len, hq, float(scale),
+        partition_tokens, _ptr(out), _ptr(workspace), ws_bytes, ctypes.byref(desc),
+        _stream(stream))
+    _check(st, "pa_decode_append")
     return out
 
 

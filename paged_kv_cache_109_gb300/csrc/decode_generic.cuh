@@ -50,6 +50,13 @@ struct DecodeArgs {
     int32_t max_prefix_blocks;
     int32_t prefix_ztiles;   // grid z per group taken by its prefix CTAs
     int32_t prefix_z;        // num_groups * prefix_ztiles: z below this is a prefix CTA
+    // Decode with the append fused in (TMA kernel only; nullptr otherwise):
+    // sequence i's newest token, at position seq_lens[i] - 1, has K and V rows
+    // k_new[i], v_new[i] ([num_seqs, Hkv, head_dim]); the kernel attends to
+    // them in place of the cache's old contents of that slot and stores them
+    // to the caches.
+    const void* k_new;
+    const void* v_new;
 };
 
 // Shared leading blocks of group k, clamped to the host bound (an entry past

@@ -253,6 +253,25 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     const int32_t nblk = (n + BS - 1) / BS;
     const int32_t nchunk = (n + C::kChunk - 1) / C::kChunk;
+    // Fused append: the CTA whose partition holds position T - 1 takes that
+    // token's K and V rows from k_new / v_new.  Lane l of the warp that owns
+    // its chunk holds 16 bytes (lanes 0-15 K, 16-31 V, eight columns each),
+    // loaded here so the load overlaps the first tile copies; they replace
+    // row rnew of the chunk's tile once its copy has landed.  A clamped
+    // (reported) length appends nothing.
+    int32_t cnew = -1, rnew = 0;
+    uint4 nrow = make_uint4(0u, 0u, 0u, 0u);
+    const bool npiece = (lane & 15) * 8 < D;
+    if (!CAS && a.k_new != nullptr && T == T_raw && T - 1 >= t0 && T - 1 < t0 + n) {
+        cnew = (T - 1 - t0) / C::kChunk;
+        rnew = T - 1 - t0 - cnew * C::kChunk;
+        if (cnew % C::kWarps == warp && npiece) {
+            const __nv_bfloat16* src =
+                static_cast<const __nv_bfloat16*>(lane < 16 ? a.k_new : a.v_new);
+            nrow = *reinterpret_cast<const uint4*>(src + ((int64_t)i * a.num_kv_heads + g) * D +
+                                                   (lane & 15) * 8);
+        }
+    }
 #pragma unroll
     for (int r = 0; r < kIdsPerThread; ++r) {
         const int32_t b = tid + r * C::kThreads;
@@ -356,6 +375,26 @@ decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const int32_t b = x / chunks, r = x - b * chunks;
                     *reinterpret_cast<uint4*>(vt + b * C::kBoxBytes + nvalid * 128 + r * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            if (!CAS && c == cnew) {
+                // the appended token: its rows replace row rnew of the K and
+                // V tiles (same 128-byte swizzle as the copy), and sub-group 0
+                // stores them to the caches for later calls
+                if (npiece) {
+                    const int32_t pc = lane & 15;
+                    uint8_t* tile = sm + warp * C::kStages * C::kStageBytes + st * C::kStageBytes +
+                                    (lane < 16 ? 0 : C::kTileBytes);
+                    *reinterpret_cast<uint4*>(tile + (pc >> 3) * C::kBoxBytes + rnew * 128 +
+                                              (((pc & 7) ^ (rnew & 7)) << 4)) = nrow;
+                    if (sg == 0) {
+                        const int32_t off = T - 1 - t0, pos = T - 1 - (T - 1) / BS * BS;
+                        const int64_t crow = ((int64_t)ids[off / BS] * hkv + g) * BS + pos;
+                        void* cache = const_cast<void*>(lane < 16 ? a.k_cache : a.v_cache);
+                        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(cache) +
+                                                  crow * D + pc * 8) = nrow;
+                    }
                 }
                 __syncwarp();
             }

@@ -449,12 +449,19 @@ size_t cells_bytes(size_t cells, const pa_cache_desc* c) {
 // for all its members' query heads, members' own CTAs start past them, and
 // the merge combines both.  Other kernels run the plain decode over the same
 // tables (same result).
+//
+// With k_new / v_new (a decode step's append, never with `sh`), sequence i's
+// token at position seq_lens[i] - 1 is first written to the caches: inside
+// the TMA kernel (the CTA holding that position uses the new rows in place of
+// the slot's old contents and stores them), else by the cache-write kernel
+// with slots from the lengths, launched before the decode.
 pa_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, int32_t max_blocks_per_seq,
                       const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
                       int32_t num_q_heads, float scale, int32_t partition_tokens, void* out,
                       void* workspace, size_t workspace_bytes_given, const pa_cache_desc* cache,
-                      void* stream, const ShareGroups* sh) {
+                      void* stream, const ShareGroups* sh, const void* k_new = nullptr,
+                      const void* v_new = nullptr) {
     const int32_t path = !desc_ok(cache) || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads
                              ? -1
                              : fast_shape(cache, num_q_heads / cache->num_kv_heads) ? 1
@@ -492,6 +499,14 @@ pa_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
         !map_step_arg(out) || !device_memory(k_cache) || !device_memory(v_cache))
         return PA_ERR_INVALID_ARG;
     if (num_parts(max_seq_len, part) > 65535) return PA_ERR_UNSUPPORTED;
+    // the append: fused into the TMA kernel when its 16-byte row pieces are
+    // aligned, else a separate cache write first
+    const bool append = k_new != nullptr || v_new != nullptr;
+    if (append && (!k_new || !v_new || sh || !aligned(k_new, elem_bytes(cache)) ||
+                   !aligned(v_new, elem_bytes(cache)) || !map_step_arg(k_new) ||
+                   !map_step_arg(v_new)))
+        return PA_ERR_INVALID_ARG;
+    const bool fused = append && fast && aligned(k_new, 16) && aligned(v_new, 16);
     // shared-prefix decode on the TMA kernel: workspace slots for the
     // groups' prefix partitions in front of each member's own
     const bool cas = sh != nullptr && fast &&
@@ -571,6 +586,16 @@ pa_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
         const int64_t pre = ((int64_t)sh->max_prefix_blocks * B + part - 1) / part;
         grid = dim3((unsigned)std::max(own, pre), cache->num_kv_heads * a.sub_groups,
                     (unsigned)(pz + num_seqs));
+    }
+    if (fused) {
+        a.k_new = k_new;
+        a.v_new = v_new;
+    } else if (append) {
+        const SlotFromAppend slots{seq_lens, block_tables, max_blocks_per_seq, B,
+                                   cache->num_blocks, max_seq_len};
+        const pa_status w = launch_write(k_new, v_new, slots, num_seqs, const_cast<void*>(k_cache),
+                                         const_cast<void*>(v_cache), cache, st);
+        if (w != PA_OK) return w;
     }
     cudaError_t err;
     if (fast) {
@@ -739,6 +764,19 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
     return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                        num_seqs, max_seq_len, num_q_heads, scale, partition_tokens, out,
                        workspace, workspace_bytes_given, cache, stream, nullptr);
+}
+
+pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                           void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                           int32_t num_q_heads, float scale, int32_t partition_tokens, void* out,
+                           void* workspace, size_t workspace_bytes_given,
+                           const pa_cache_desc* cache, void* stream) {
+    const CallRange range("pa_decode_append");
+    if (!k_new || !v_new) return PA_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                       num_seqs, max_seq_len, num_q_heads, scale, partition_tokens, out,
+                       workspace, workspace_bytes_given, cache, stream, nullptr, k_new, v_new);
 }
 
 int32_t pa_decode_shared_prefix_mode(int32_t num_q_heads, int32_t max_prefix_blocks,

@@ -59,6 +59,34 @@ struct SlotFromPosition {
     }
 };
 
+// Slot of sequence j's newest token in a decode step: position
+// seq_lens[j] - 1 (lengths count the new token; paper notes' block
+// lifecycle: decode fills the next slot of the last block), through the same
+// table formula.  A length of 0 appends nothing; a length the table or the
+// host bound cannot hold (reported as the decode reports it), or a bad table
+// entry, is skipped and reported.
+struct SlotFromAppend {
+    const int32_t* seq_lens;
+    const int32_t* block_tables;
+    int32_t max_blocks, block_size, num_blocks, max_seq_len;
+    __device__ __forceinline__ int64_t operator()(int64_t j, bool report) const {
+        const int32_t t = __ldg(seq_lens + j);
+        if (t == 0) return -1;
+        const int64_t cap = min((int64_t)max_seq_len, (int64_t)max_blocks * block_size);
+        if (t < 0 || t > cap) {
+            if (report) raise_error(PA_DEVERR_SEQ_LEN);
+            return -1;
+        }
+        const int32_t p = t - 1;
+        const int32_t id = __ldg(block_tables + j * max_blocks + p / block_size);
+        if (id < 0 || id >= num_blocks) {
+            if (report) raise_error(PA_DEVERR_TABLE_ENTRY);
+            return -1;
+        }
+        return (int64_t)id * block_size + p % block_size;
+    }
+};
+
 // One warp per token (a grid-stride loop over tokens): every lane reads the
 // token's slot (one broadcast load), then the warp moves the token's
 // 2 * Hkv * row_bytes bytes, each lane issuing up to kWriteUnroll vector

@@ -49,6 +49,15 @@ class DeviceState:
                          int(step.seq_lens.max()), self.wl.scale, **kw)
 
 
+    def append(self, step, **kw):
+        """The step's write and decode in one pa_decode_append call (steps
+        whose new tokens are each sequence's last position)."""
+        return pa.decode_append(step.q.to(self.dev), step.k_new.to(self.dev),
+                                step.v_new.to(self.dev), self.k_cache, self.v_cache,
+                                step.block_tables.to(self.dev), step.seq_lens.to(self.dev),
+                                int(step.seq_lens.max()), self.wl.scale, **kw)
+
+
 class HostState:
     """Oracle-side copies of the caches, advanced with the oracle's write."""
 

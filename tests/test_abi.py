@@ -119,6 +119,13 @@ def test_invalid_arguments_rejected_before_any_launch(lib):
                          ctypes.byref(d), None) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_decode(None, None, None, None, 4, None, 0, 64, 32, 1.0, 0, None, None, 0,
                          ctypes.byref(d), None) == pa.PA_OK
+    # the fused append: no new rows, or the decode's own argument errors
+    assert lib.pa_decode_append(None, None, None, None, None, None, 4, None, 2, 64, 32, 1.0, 0,
+                                None, None, 0, ctypes.byref(d), None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_append(None, 16, 16, None, None, None, 4, None, 2, 64, 32, 1.0, 0,
+                                None, None, 0, ctypes.byref(d), None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_append(None, 16, 16, None, None, None, 4, None, 2, 64, 30, 1.0, 0,
+                                None, None, 0, ctypes.byref(d), None) == pa.PA_ERR_INVALID_ARG
 
 
 def test_binding_refuses_host_tensors():
@@ -126,6 +133,10 @@ def test_binding_refuses_host_tensors():
     x = torch.zeros(2, 8, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         pa.write_kv(x, x, torch.zeros(2, dtype=torch.int64), torch.zeros(4, 8, 16, 128), x)
+    c = torch.zeros(4, 8, 16, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pa.decode_append(x, x, x, c, c, torch.zeros(2, 1, dtype=torch.int32),
+                         torch.ones(2, dtype=torch.int32), 1)
 
 
 def test_wait_check_refuses_bad_arguments_without_a_gpu(lib):

@@ -67,3 +67,29 @@ def test_reference_arm_describes_the_same_workload():
     wl = workloads.make("mha", **bench.overrides(args))
     assert line["config"] == json.loads(json.dumps(bench.decode_config(args, wl, 1)))
     assert line["impl"] == "reference" and line["config"]["num_seqs"] == 2
+
+
+def test_decode_steps_write_inside_the_decode_call():
+    """The decode workloads' steps add one token per sequence at its last
+    position, so by default their write goes inside the decode call
+    (pa_decode_append); continuous batching, whose steps also write a chunk,
+    keeps the cache-write call."""
+    import pytest
+    from paged_kv_cache_109_gb300 import workloads
+    small = {"mha": dict(num_seqs=3, num_blocks=512),
+             "gqa": dict(num_seqs=8, num_shared=2, num_blocks=4096),
+             "long": dict(num_seqs=1, seq_len=2000),
+             "cb": dict(num_seqs=4, max_len0=100, chunk=30, num_steps=2, num_blocks=256)}
+    for name, kw in small.items():
+        wl = workloads.make(name, **kw)
+        args = bench.make_parser().parse_args(["--workload", name])
+        want = "slot_mapping" if name == "cb" else "append"
+        assert bench.appends_only(wl) == (name != "cb")
+        assert bench.write_mode(args, wl) == want
+        assert bench.write_mode(bench.make_parser().parse_args(
+            ["--workload", name, "--positions"]), wl) == "positions"
+        assert bench.write_mode(bench.make_parser().parse_args(
+            ["--workload", name, "--write", "slot_mapping"]), wl) == "slot_mapping"
+    with pytest.raises(SystemExit):
+        bench.write_mode(bench.make_parser().parse_args(["--workload", "cb", "--write",
+                                                         "append"]), wl)
