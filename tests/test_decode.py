@@ -277,6 +277,26 @@ def test_merge_column_slabs_and_warp_counts(cuda_device, dtype, d, hq, hkv):
     assert pa.last_device_error() == 0
 
 
+@pytest.mark.parametrize("dtype,d,hq,hkv", [(torch.bfloat16, 128, 12, 4),
+                                             (torch.float32, 64, 12, 4)])
+def test_merge_with_thousands_of_pairs(cuda_device, dtype, d, hq, hkv):
+    """A batch of 3972 (sequence, head) pairs, more merge CTAs than fit on the
+    GPU at once, at partition sizes that give 2, 4 and 8 merge warps a pair,
+    with pairs that need no merge next to pairs that do."""
+    rng = np.random.default_rng(31)
+    lens = [1, 64, 65, 1100, 0] + rng.integers(1, 1100, size=326).tolist()
+    q, kc, vc, bt, sl = synthetic(hq, hkv, d, 16, lens, dtype=dtype, seed=31)
+    scale = 1 / math.sqrt(d)
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    atol, rtol = tolerance(dtype)
+    for part in (16, 64, 128, 512):    # 69, 18, 9 and 3 partitions in the longest sequence
+        out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=part)
+        assert_close(out.double().numpy(), ref, atol, rtol, f"partitions of {part}")
+        assert torch.equal(out, gpu_decode(cuda_device, q, kc, vc, bt, sl, scale,
+                                           partition_tokens=part))
+    assert pa.last_device_error() == 0
+
+
 def test_relabelling_physical_blocks_changes_nothing(cuda_device):
     q, kc, vc, bt, sl = synthetic(32, 8, 128, 16, (500, 33, 1200), seed=3, num_blocks=200)
     scale = 1 / math.sqrt(128)

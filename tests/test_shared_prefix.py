@@ -82,6 +82,12 @@ CASES = [
     (256, 8, 128, 16, [(3, [49, 60])], [10], 16),
     (32, 8, 128, 8, [(7, [57, 100, 3])], [9], 0),
     (16, 2, 64, 16, [(2, [0, 100, 40]), (0, [20, 30])], [17], 16),
+    # 101 sequences x 32 heads (3232 merge CTAs), members and plain
+    # sequences side by side, 8- and 2-warp merges
+    (32, 8, 128, 16, [(8, [200 + 37 * j for j in range(40)]), (4, [70 + 11 * j for j in range(30)])],
+     list(range(1, 400, 13)), 64),
+    (32, 8, 128, 16, [(8, [200 + 37 * j for j in range(40)]), (4, [70 + 11 * j for j in range(30)])],
+     list(range(1, 400, 13)), 256),
 ]
 
 
