@@ -68,12 +68,14 @@ WORKLOAD_TEXT = {
 
 # ---- byte model ---------------------------------------------------------------
 
-def step_bytes(wl, k: int, split_traffic: bool = True, shared_prefix: bool = False) -> dict:
+def step_bytes(wl, k: int, split_traffic: bool = True, shared_prefix: bool = False,
+               partition: int = 0, fused: bool = False) -> dict:
     """Algorithmic bytes of step k (see the design notes for the model).
-    With ``split_traffic`` the split-K partial write + read of the library's
-    automatic partition size is included (asks libpa.so for that size); with
-    ``shared_prefix`` the partials of the shared-prefix decode (every group
-    member writes its group's prefix partitions and its own)."""
+    With ``split_traffic`` the split-K partial write + read at ``partition``
+    tokens (0: the library's automatic size, asked of libpa.so) is included;
+    with ``shared_prefix`` the partials of the shared-prefix decode (every
+    group member writes its group's prefix partitions and its own).  With
+    ``fused`` the write is pa_decode_append's, which reads no slot mapping."""
     st = wl.steps[k]
     e = wl.elem_bytes
     row = wl.head_dim * e
@@ -94,8 +96,8 @@ def step_bytes(wl, k: int, split_traffic: bool = True, shared_prefix: bool = Fal
     split, ws, part = 0, 0, None
     if split_traffic:
         import paged_kv_cache_109_gb300 as pa
-        ws = pa.decode_workspace_bytes(n, hq, int(lens.max()), wl.k_cache, 0)
-        part = pa.decode_partition_tokens(n, hq, int(lens.max()), wl.k_cache)
+        ws = pa.decode_workspace_bytes(n, hq, int(lens.max()), wl.k_cache, partition)
+        part = partition or pa.decode_partition_tokens(n, hq, int(lens.max()), wl.k_cache)
         member_pk = {}
         if shared_prefix:
             for members, blocks in wl.prefix_groups:
@@ -112,7 +114,8 @@ def step_bytes(wl, k: int, split_traffic: bool = True, shared_prefix: bool = Fal
             if parts > 1:
                 split += 2 * parts * hq * (wl.head_dim + 2) * 4
     n_tok = st.slot_mapping.numel()
-    write = n_tok * (2 * per_tok + 8)                   # read k,v + write cache rows + slot
+    # read k,v + write cache rows (+ the slot, unless the decode call appends)
+    write = n_tok * (2 * per_tok + (0 if fused else 8))
     return {"logical_kv": logical_kv, "unique_kv": unique_kv, "decode": unique_kv + q_out +
             tables + split, "decode_logical": logical_kv + q_out + tables + split,
             "write": write, "workspace": ws, "partition": part}
@@ -476,15 +479,20 @@ def run_ours(args, rank, world, device):
                                                    kc) == 1
     mode = write_mode(args, wl)
     if mode == "append" and once:
-        raise SystemExit("--write append: this batch's shared blocks are read once, which "
-                         "the fused call does not do; use --write slot_mapping")
+        # the fused call runs the plain decode; where the shared-prefix decode
+        # reads the shared blocks once, the step keeps it and writes first
+        if args.write == "append":
+            raise SystemExit("--write append: this batch's shared blocks are read once, which "
+                             "the fused call does not do; use --write slot_mapping")
+        mode = "slot_mapping"
     # where the shared-prefix decode would run the plain decode anyway, the
     # step's fused call is that same plain decode
     if mode == "append":
         shared = False
-    bytes_ = [step_bytes(wl, k, shared_prefix=once) for k in range(nsteps_wl)]
-    maxlens = [int(st.seq_lens.max()) for st in wl.steps]
     part = args.partition or 0
+    bytes_ = [step_bytes(wl, k, shared_prefix=once, partition=part, fused=mode == "append")
+              for k in range(nsteps_wl)]
+    maxlens = [int(st.seq_lens.max()) for st in wl.steps]
     ws_need = max(pa.decode_shared_prefix_workspace_bytes(wl.num_seqs, wl.num_q_heads, m,
                                                           groups.max_prefix_blocks, kc, part)
                   if shared else
@@ -585,6 +593,8 @@ def run_ours(args, rank, world, device):
         "config": decode_config(args, wl, world),
         "kernel_config": {
             "partition_tokens": b0["partition"],
+            "write": {"append": "inside pa_decode_append", "positions": "pa_write_kv_positions",
+                      "slot_mapping": "pa_write_kv"}[mode],
             "decode": ("pa_decode_shared_prefix, automatic mode (%s): %d group(s), "
                        "%s shared blocks"
                        % ("shared blocks read once" if once
