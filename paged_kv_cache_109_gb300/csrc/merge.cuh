@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(32 * W) merge_kernel(const DecodeArgs a) {
 }
 
 // Warps per merge CTA for a call whose longest sequence has max_parts
-// partitions: 2 up to two chunks, 4 up to four, else 8.
+// partitions: 2 up to two chunks, 4 up to four, else 8.  (The launch halves
+// this while the grid would not fit on the GPU in one wave.)
 inline int merge_warps(int32_t max_parts) {
     return max_parts <= 2 * kMergeChunk ? 2 : max_parts <= 4 * kMergeChunk ? 4 : 8;
 }

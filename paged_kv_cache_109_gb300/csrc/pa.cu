@@ -116,12 +116,47 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+template <typename E, int W, int VEC>
+cudaError_t launch_merge_k(dim3 grid, cudaStream_t st, const DecodeArgs& a) {
+    return launch_pdl(merge_kernel<E, W, VEC>, grid, dim3(32 * W), 0, st, a);
+}
+
+// CTAs of merge_kernel<E, W, VEC> one SM holds (0 if unknown), per device.
+template <typename E, int W, int VEC>
+int merge_ctas_per_sm() {
+    static int cached[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, merge_kernel<E, W, VEC>, 32 * W,
+                                                          0) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
 template <typename E, int VEC>
 cudaError_t launch_merge_w(int warps, dim3 grid, cudaStream_t st, const DecodeArgs& a) {
+    // fewer warps a pair while the grid would take more than one wave on
+    // the GPU (a second wave of merge CTAs costs more than a warp's extra
+    // chunk rounds); an unknown occupancy changes nothing
+    const int64_t sms = std::max(1, device_sm_count());
+    auto fits = [&](int w) {
+        const int per = w == 8   ? merge_ctas_per_sm<E, 8, VEC>()
+                        : w == 4 ? merge_ctas_per_sm<E, 4, VEC>()
+                                 : merge_ctas_per_sm<E, 2, VEC>();
+        return per <= 0 || (int64_t)grid.x <= per * sms;
+    };
+    while (warps > 1 && !fits(warps)) warps /= 2;
     switch (warps) {
-        case 2: return launch_pdl(merge_kernel<E, 2, VEC>, grid, dim3(64), 0, st, a);
-        case 4: return launch_pdl(merge_kernel<E, 4, VEC>, grid, dim3(128), 0, st, a);
-        default: return launch_pdl(merge_kernel<E, 8, VEC>, grid, dim3(256), 0, st, a);
+        case 1: return launch_merge_k<E, 1, VEC>(grid, st, a);
+        case 2: return launch_merge_k<E, 2, VEC>(grid, st, a);
+        case 4: return launch_merge_k<E, 4, VEC>(grid, st, a);
+        default: return launch_merge_k<E, 8, VEC>(grid, st, a);
     }
 }
 
