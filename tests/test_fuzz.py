@@ -81,6 +81,55 @@ def test_fuzz_write_then_decode(cuda_device, seed):
 
 
 @pytest.mark.parametrize("seed", range(16))
+def test_fuzz_decode_append(cuda_device, seed):
+    """The decode step in one call (pa_decode_append) on random shapes: its
+    caches equal the oracle's write of each sequence's last position, its
+    output the oracle's decode, and both equal pa_write_kv_positions +
+    pa_decode bit for bit.  The appended slots hold NaN before the call."""
+    rng = np.random.default_rng(3000 + seed)
+    hkv, g, d, bs, lens = _case(rng)
+    hq = hkv * g
+    dtype = torch.float32 if rng.random() < 0.15 else torch.bfloat16
+    kc, vc, bt, gen = _pool(rng, hkv, d, bs, lens, dtype)
+    n = len(lens)
+    for i, t in enumerate(lens):
+        if t > 0:
+            kc[int(bt[i, (t - 1) // bs]), :, (t - 1) % bs] = float("nan")
+            vc[int(bt[i, (t - 1) // bs]), :, (t - 1) % bs] = float("nan")
+    sl = torch.tensor(lens, dtype=torch.int32)
+    k_new = torch.randn(n, hkv, d, generator=gen).to(dtype)
+    v_new = torch.randn(n, hkv, d, generator=gen).to(dtype)
+    q = torch.randn(n, hq, d, generator=gen).to(dtype)
+    scale = float(rng.uniform(0.5, 1.5)) / math.sqrt(d)
+    part = 0 if rng.random() < 0.5 else bs * int(rng.integers(1, 9))
+    max_len = max(max(lens), 1)
+
+    dev = cuda_device
+    kd, vd = kc.to(dev), vc.to(dev)
+    out = pa.decode_append(q.to(dev), k_new.to(dev), v_new.to(dev), kd, vd, bt.to(dev),
+                           sl.to(dev), max_len, scale, partition_tokens=part)
+    kr, vr = kc.to(dev), vc.to(dev)
+    pa.write_kv_positions(k_new.to(dev), v_new.to(dev),
+                          torch.arange(n, dtype=torch.int32, device=dev), (sl - 1).to(dev),
+                          bt.to(dev), kr, vr)
+    ref_gpu = pa.decode(q.to(dev), kr, vr, bt.to(dev), sl.to(dev), max_len, scale,
+                        partition_tokens=part)
+    torch.cuda.synchronize()
+    slots = torch.from_numpy(oracle.slots_from_positions(
+        torch.arange(n, dtype=torch.int32), sl - 1, bt, bs))
+    assert oracle.write_kv(k_new, v_new, slots, kc, vc) == 0
+    what = f"hq={hq} hkv={hkv} d={d} B={bs} lens={lens} part={part} {dtype}"
+    assert torch.equal(kd.cpu().view(torch.uint8), kc.view(torch.uint8)), what
+    assert torch.equal(vd.cpu().view(torch.uint8), vc.view(torch.uint8)), what
+    assert torch.equal(kr, kd) and torch.equal(vr, vd), what
+    assert torch.equal(out.view(torch.uint8), ref_gpu.view(torch.uint8)), what
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    atol, rtol = (F32_ATOL, 0.0) if dtype == torch.float32 else (BF16_ATOL, BF16_RTOL)
+    assert_close(out.cpu().double().numpy(), ref, atol, rtol, what)
+    assert pa.last_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(16))
 def test_fuzz_prefill(cuda_device, seed):
     rng = np.random.default_rng(2000 + seed)
     hkv, g, d, bs, lens = _case(rng, prefill=True)
