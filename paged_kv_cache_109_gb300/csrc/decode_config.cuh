@@ -45,10 +45,11 @@ int device_sm_count() {
 // ---- kernel selection --------------------------------------------------------
 
 // Groups of more than 16 query heads are split into sub-groups of 16, one CTA
-// each, reading the same K/V tiles (the later reads mostly hit L2).  Head dims
-// 80, 96 and 112 load as two 64-column boxes whose columns past the head dim
-// are zero-filled by the copy (out of the tensor map's bounds).
-bool tma_head_dim(int32_t D) { return D == 64 || D == 80 || D == 96 || D == 112 || D == 128; }
+// each, reading the same K/V tiles (the later reads mostly hit L2).  Every
+// head dim that is a multiple of 16 up to 128 loads as 64-column boxes (one
+// up to 64, two above) whose columns past the head dim are zero-filled by
+// the copy (out of the tensor map's bounds) and never read from memory.
+bool tma_head_dim(int32_t D) { return D % 16 == 0 && D >= 16 && D <= 128; }
 
 bool fast_shape(const pa_cache_desc* c, int32_t group) {
     if (c->dtype != PA_BF16 || group < 1) return false;

@@ -55,7 +55,7 @@ struct TmaMmaCfg {
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kChunk = 16;                     // tokens per pipeline stage
     static constexpr int kBoxCols = 64;                   // 64 bf16 = 128 bytes (swizzle span)
-    // head dims 80-112: a second box whose columns past D arrive as zeros
+    // head dims 16-48 and 80-112: the (last) box's columns past D arrive as zeros
     static constexpr int kBoxes = (D + kBoxCols - 1) / kBoxCols;
     static constexpr int kBoxBytes = kChunk * 128;        // 16 rows x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;  // 16 rows x kBoxes x 64 columns

@@ -304,6 +304,9 @@ cudaError_t dispatch_fast_cas(dim3 grid, const CUtensorMap& mk, const CUtensorMa
     }
     if constexpr (!CAS) {
         switch (a.head_dim) {
+            case 16: return launch_fast_d<16, false>(grid, mk, mv, a, st);
+            case 32: return launch_fast_d<32, false>(grid, mk, mv, a, st);
+            case 48: return launch_fast_d<48, false>(grid, mk, mv, a, st);
             case 80: return launch_fast_d<80, false>(grid, mk, mv, a, st);
             case 96: return launch_fast_d<96, false>(grid, mk, mv, a, st);
             case 112: return launch_fast_d<112, false>(grid, mk, mv, a, st);

@@ -67,7 +67,10 @@ def test_path_selection(lib):
     assert path(32, desc(d=80, bs=8)) == 1
     assert path(128, desc(d=112, bs=32)) == 1
     assert path(40, desc(d=96, bs=24)) == 2            # G=5 at a block size TMA does not take
-    assert path(64, desc(d=48)) == 2                   # D=48: mma.sync
+    assert path(64, desc(d=48)) == 1                   # D=48: one box, 16 columns zero-filled
+    assert path(8, desc(d=16, bs=8)) == 1              # D=16, B=8
+    assert path(32, desc(d=32, bs=64)) == 1
+    assert path(64, desc(d=48, bs=24)) == 2            # D=48 at a block size TMA does not take
     assert path(32, desc(d=96, bs=24)) == 0            # G=4: CUDA cores
     assert path(64, desc(d=40)) == 0                   # not a multiple of 16: CUDA cores
     assert path(64, desc(d=256)) == 0                  # over 128: CUDA cores

@@ -77,7 +77,7 @@ def _oracle(kc, vc, bt, sl, q, k_new, v_new, bs, scale):
 
 
 # (kv heads, group, head dim, block size, dtype, partition): the TMA kernel
-# (fused) for the first seven, then the mma.sync, tiled and generic kernels
+# (fused) for the first eight, then the mma.sync, tiled and generic kernels
 # (cache write first)
 SHAPES = [
     (8, 4, 128, 16, torch.bfloat16, 0),
@@ -87,7 +87,8 @@ SHAPES = [
     (2, 32, 112, 16, torch.bfloat16, 64),      # two sub-groups per kv head
     (4, 8, 80, 64, torch.bfloat16, 128),
     (1, 5, 128, 256, torch.bfloat16, 256),
-    (2, 8, 48, 16, torch.bfloat16, 64),        # mma.sync kernel
+    (2, 4, 32, 16, torch.bfloat16, 64),        # head dim 32: one box, half zero-filled
+    (2, 8, 48, 24, torch.bfloat16, 48),        # mma.sync kernel
     (2, 2, 96, 4, torch.bfloat16, 32),         # tiled kernel, bf16
     (2, 4, 128, 16, torch.float32, 64),        # tiled kernel, fp32
     (2, 3, 20, 5, torch.bfloat16, 20),         # generic kernel
@@ -103,7 +104,7 @@ def test_append_matches_write_then_decode_and_oracle(cuda_device, hkv, group, d,
     kc, vc, bt, sl, q, k_new, v_new = _batch(hkv, group, d, bs, dtype, lens, seed=hkv * d + bs)
     max_len = int(sl.max())
     scale = 1 / math.sqrt(d)
-    fused = SHAPES.index((hkv, group, d, bs, dtype, part)) < 7
+    fused = SHAPES.index((hkv, group, d, bs, dtype, part)) < 8
     assert (pa.decode_path(hkv * group, kc) == 1) == fused
     (out, kd, vd), (ref, kr, vr) = _run_both(cuda_device, kc, vc, bt, sl, q, k_new, v_new,
                                              max_len, part, scale)

@@ -105,6 +105,12 @@ FAST_CASES = [
     (32, 8, 112, 16, (17, 400, 2049)),                             # D=112, G=4
     (128, 8, 96, 16, (5, 700)),                                    # D=96, G=16
     (8, 8, 96, 8, (1, 9, 130)),                                    # D=96 MHA, B=8
+    (64, 8, 48, 32, (1, 31, 32, 33, 900)),                         # D=48: one box, 16 columns zero
+    (32, 2, 48, 16, (1, 17, 700)),                                 # D=48, G=16
+    (16, 4, 16, 16, (1, 15, 16, 17, 400)),                         # D=16: one k-step
+    (32, 8, 32, 8, (1, 7, 8, 9, 300)),                             # D=32, B=8
+    (8, 8, 32, 64, (63, 64, 65, 500)),                             # D=32 MHA, B=64
+    (48, 2, 16, 16, (5, 333)),                                     # D=16, G=24: sub-groups
 ]
 
 
@@ -150,7 +156,7 @@ def test_portable_kernel_matches_oracle(cuda_device, hq, hkv, d, bs, lengths, dt
     (6, 3, 12, 16, (30, 70), torch.bfloat16, 0),           # 24-byte rows: the generic kernel
     (6, 3, 12, 16, (30, 70), torch.bfloat16, 32),
     (40, 8, 96, 24, (1, 100, 257), torch.bfloat16, 0),     # mma.sync, G=5 (lo parts in rows 8-15)
-    (64, 8, 48, 16, (1, 100, 257), torch.bfloat16, 64),    # mma.sync, D=48
+    (64, 8, 48, 24, (1, 100, 257), torch.bfloat16, 48),    # mma.sync, D=48, B=24
     (96, 8, 80, 5, (700, 33), torch.bfloat16, 35),         # mma.sync, G=12, B=5
     (64, 4, 64, 1, (1100, 3), torch.bfloat16, 1100),       # mma.sync, G=16, >512 blocks a partition
     (256, 8, 112, 24, (500, 1, 90), torch.bfloat16, 0),    # mma.sync, G=32: two sub-groups
