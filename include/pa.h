@@ -50,7 +50,8 @@
  * call first synchronises its stream, copies its index arrays to the host and
  * checks them as a whole.  Duplicate slots, two copies into one block (or,
  * inside one pool, onto a source), entries or slots outside the pool, lengths
- * past their bounds and query rows out of order are then refused with
+ * past their bounds, query rows out of order and appends into a block that
+ * another table also reaches are then refused with
  * PA_ERR_INVALID_ARG before launch (the first violation is printed to
  * stderr).  This is slow and is not for use under stream capture.
  *
@@ -239,7 +240,8 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * appends nothing and is reported (PA_DEVERR_SEQ_LEN, PA_DEVERR_TABLE_ENTRY),
  * as pa_decode reports it.  The appended slot must belong to this sequence
  * alone (a block shared with another table is copied first: pa_copy_blocks);
- * two sequences appending to one slot is undefined.
+ * two sequences appending to one slot is undefined.  Both are refused under
+ * PA_DEBUG.
  * Other arguments, the workspace and the errors as pa_decode.
  */
 pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,

@@ -117,6 +117,36 @@ inline pa_status check_tables(const int32_t* tables, int32_t max_blocks, const i
     return PA_OK;
 }
 
+// A decode step's appends (pa_decode_append): each sequence with T > 0 writes
+// position T - 1 of its own table.  Refused: two sequences on one slot, and
+// a slot in a block that another sequence's table also reaches (a shared
+// block must be copied before it is written).  The lengths and entries
+// themselves are check_tables' business.
+inline pa_status check_appends(const int32_t* tables, int32_t max_blocks, const int32_t* seq_lens,
+                               int32_t num_seqs, const pa_cache_desc* c, cudaStream_t st) {
+    std::vector<int32_t> tab, len;
+    if (!fetch(tab, tables, (size_t)num_seqs * max_blocks, st) ||
+        !fetch(len, seq_lens, (size_t)num_seqs, st))
+        return PA_ERR_CUDA;
+    const int32_t B = c->block_size;
+    std::vector<int32_t> owners((size_t)c->num_blocks, 0);   // tables reaching each block
+    for (int32_t i = 0; i < num_seqs; ++i)
+        for (int32_t b = 0; b < (len[i] + B - 1) / B; ++b) {
+            const int32_t id = tab[(size_t)i * max_blocks + b];
+            if (id >= 0 && id < c->num_blocks) ++owners[id];
+        }
+    std::vector<int64_t> slots;
+    for (int32_t i = 0; i < num_seqs; ++i) {
+        if (len[i] <= 0) continue;
+        const int32_t id = tab[(size_t)i * max_blocks + (len[i] - 1) / B];
+        if (id < 0 || id >= c->num_blocks) continue;
+        if (owners[id] > 1)
+            return fail("append into a block another table reaches (sequence, block)", i, id);
+        slots.push_back((int64_t)id * B + (len[i] - 1) % B);
+    }
+    return check_slot_list(std::move(slots), (int64_t)c->num_blocks * B);
+}
+
 // Shared-prefix groups: member lists ordered from 0, within the host bounds,
 // every member a valid sequence in exactly one group whose seq_group entry
 // names it (and -1 for the other sequences), and every member's first

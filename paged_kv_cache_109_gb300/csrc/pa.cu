@@ -563,6 +563,11 @@ pa_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
         const pa_status r = debug::check_tables(block_tables, max_blocks_per_seq, seq_lens,
                                                 num_seqs, max_seq_len, nullptr, 0, cache, st);
         if (r != PA_OK) return r;
+        if (append) {
+            const pa_status r3 = debug::check_appends(block_tables, max_blocks_per_seq, seq_lens,
+                                                      num_seqs, cache, st);
+            if (r3 != PA_OK) return r3;
+        }
         if (sh) {
             const pa_status r2 = debug::check_groups(block_tables, max_blocks_per_seq, num_seqs,
                                                      sh->seq_group, sh->member_start,

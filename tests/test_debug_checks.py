@@ -134,3 +134,46 @@ def test_without_pa_debug_the_pass_is_off(monkeypatch, cuda_device):
     pa.write_kv(k.to(dev), v.to(dev), slots, kd, vd)
     torch.cuda.synchronize()
     assert pa.last_device_error() == 0
+
+
+def test_append_into_a_shared_block_is_refused(debug_on):
+    """pa_decode_append whose appended slot lies in a block another table
+    also reaches (not copied first) is refused before launch; the same batch
+    with the block made private passes and matches the oracle."""
+    import math
+    dev = debug_on
+    kc, vc, kd, vd = _pool(dev)
+    # both sequences' tables start with block 7; sequence 0 (5 tokens, B = 4)
+    # appends into its own block 3, sequence 1 (3 tokens) into block 7
+    bt = torch.tensor([[7, 3], [7, -1]], dtype=torch.int32)
+    sl = torch.tensor([5, 3], dtype=torch.int32)
+    q = torch.randn(2, 4, 64, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    k, v = _tokens(2)
+    before = kd.clone()
+    _refused(lambda: pa.decode_append(q.to(dev), k.to(dev), v.to(dev), kd, vd, bt.to(dev),
+                                      sl.to(dev), 8))
+    assert torch.equal(kd, before)
+    bt[1, 0] = 9                                        # sequence 1 on a private block
+    out = pa.decode_append(q.to(dev), k.to(dev), v.to(dev), kd, vd, bt.to(dev), sl.to(dev), 8)
+    torch.cuda.synchronize()
+    slots = torch.from_numpy(oracle.slots_from_positions(torch.arange(2, dtype=torch.int32),
+                                                         sl - 1, bt, 4))
+    kh, vh = kc.clone(), vc.clone()
+    oracle.write_kv(k, v, slots, kh, vh)
+    ref = oracle.decode(q, kh, vh, bt, sl, 1 / math.sqrt(64))
+    assert torch.equal(kd.cpu(), kh)
+    assert_close(out.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, "debug append")
+
+
+def test_two_appends_on_one_slot_are_refused(debug_on):
+    """Two sequences whose tables end in the same block at the same offset
+    (one slot appended twice) are refused; the shared-block rule names it
+    first."""
+    dev = debug_on
+    _, _, kd, vd = _pool(dev)
+    bt = torch.tensor([[2, 5], [4, 5]], dtype=torch.int32)
+    sl = torch.tensor([6, 6], dtype=torch.int32)
+    q = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    k, v = _tokens(2)
+    _refused(lambda: pa.decode_append(q.to(dev), k.to(dev), v.to(dev), kd, vd, bt.to(dev),
+                                      sl.to(dev), 8))
