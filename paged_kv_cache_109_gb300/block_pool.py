@@ -131,6 +131,38 @@ class BlockPool:
         table[-1] = fresh
         return tail, fresh
 
+    def append_step(self, seqs: Sequence[Hashable]) -> list[tuple[int, int]]:
+        """One decode step: each of ``seqs`` appends one position, the token
+        ``pa_decode_append`` then writes at its new length - 1.  Per sequence,
+        in order (nxmr.cn article §4.2, the append rule): a full tail block is
+        followed by a fresh block; a partly filled tail that other sequences
+        share is first replaced by a private copy (``copy_on_write``);
+        otherwise the token goes into the tail as it is.  Returns the
+        (old, new) block pairs the device must copy (``pa_copy_blocks``)
+        before the step.  All or nothing: when the pool cannot cover every
+        sequence's blocks, ``MemoryError`` is raised and no state changes."""
+        if len(set(seqs)) != len(seqs):
+            raise ValueError("a sequence appears twice in one step")
+        # dry run: blocks needed, with the reference drops of earlier copies
+        drops: dict[int, int] = {}
+        need = 0
+        for seq in seqs:
+            n, table = self.lengths[seq], self.tables[seq]
+            if n % self.block_size == 0:
+                need += 1
+            elif self.ref_cnt[table[-1]] - drops.get(table[-1], 0) > 1:
+                need += 1
+                drops[table[-1]] = drops.get(table[-1], 0) + 1
+        if need > len(self.free_queue):
+            raise MemoryError(f"need {need} blocks, {len(self.free_queue)} free")
+        pairs = []
+        for seq in seqs:
+            pair = self.copy_on_write(seq)
+            if pair is not None:
+                pairs.append(pair)
+            self.grow(seq, 1)
+        return pairs
+
     def swap_out(self, seq: Hashable, host: "BlockPool") -> list[tuple[int, int]]:
         """Move ``seq``'s blocks to the host pool (paper notes, swapping):
         returns the (device block, host block) pairs to copy; the device blocks

@@ -12,6 +12,7 @@ import torch
 import oracle
 import paged_kv_cache_109_gb300 as pa
 from paged_kv_cache_109_gb300 import workloads
+from paged_kv_cache_109_gb300.block_pool import BlockPool
 from tests._gpu import (BF16_ATOL, BF16_RTOL, DeviceState, HostState, assert_close,
                         sample_pairs, tolerance)
 
@@ -305,5 +306,54 @@ def test_append_in_a_cuda_graph(cuda_device):
         oracle.write_kv(kn, vn, slots, kh, vh)
         ref = oracle.decode(q, kh, vh, perm, lens, 1 / math.sqrt(d))
         assert_close(out.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, f"graph step {s}")
+    assert torch.equal(kd.cpu(), kh) and torch.equal(vd.cpu(), vh)
+    assert pa.last_device_error() == 0
+
+
+def test_fork_then_append_steps(cuda_device):
+    """The decode loop with shared blocks: three sequences forked from a
+    parent whose tail block is partly filled (ref_cnt 4), and a fifth on its
+    own, take six steps.  Each step is BlockPool.append_step (copy-on-write
+    of the shared tail for all but its last sharer, fresh blocks when a tail
+    fills), pa_copy_blocks of its pairs, then pa_decode_append; the oracle
+    replays the same copies and writes at the pool's own slots."""
+    hkv, group, d, bs = 8, 4, 128, 16
+    nb = 128
+    pool = BlockPool(nb, bs, np.random.default_rng(1).permutation(nb))
+    pool.add("P", 37)
+    for c in ("c0", "c1", "c2"):
+        pool.fork("P", c)
+    pool.add("Q", 100)
+    seqs = ["P", "c0", "c1", "c2", "Q"]
+    g = torch.Generator().manual_seed(44)
+    kc = torch.randn(nb, hkv, bs, d, generator=g).to(torch.bfloat16)
+    vc = torch.randn(nb, hkv, bs, d, generator=g).to(torch.bfloat16)
+    dev = cuda_device
+    kd, vd = kc.to(dev), vc.to(dev)
+    kh, vh = kc.clone(), vc.clone()
+    scale = 1 / math.sqrt(d)
+    copies = 0
+    for step in range(6):
+        pairs = pool.append_step(seqs)
+        copies += len(pairs)
+        if pairs:
+            pt = torch.tensor(pairs, dtype=torch.int64)
+            pa.copy_blocks(kd, vd, kd, vd, pt.to(dev))
+            assert oracle.copy_blocks(kh, vh, kh, vh, pt) == 0
+        lens = torch.tensor([pool.lengths[s] for s in seqs], dtype=torch.int32)
+        bt = torch.tensor(pool.table_rows(seqs, pool.blocks_for(int(lens.max()))),
+                          dtype=torch.int32)
+        q = torch.randn(len(seqs), hkv * group, d, generator=g).to(torch.bfloat16)
+        kn = torch.randn(len(seqs), hkv, d, generator=g).to(torch.bfloat16)
+        vn = torch.randn(len(seqs), hkv, d, generator=g).to(torch.bfloat16)
+        out = pa.decode_append(q.to(dev), kn.to(dev), vn.to(dev), kd, vd, bt.to(dev),
+                               lens.to(dev), int(lens.max()), scale, partition_tokens=32)
+        torch.cuda.synchronize()
+        slots = torch.tensor([pool.slot(s, pool.lengths[s] - 1) for s in seqs],
+                             dtype=torch.int64)
+        assert oracle.write_kv(kn, vn, slots, kh, vh) == 0
+        ref = oracle.decode(q, kh, vh, bt, lens, scale)
+        assert_close(out.cpu().double().numpy(), ref, BF16_ATOL, BF16_RTOL, f"step {step}")
+    assert copies == 3                                 # c0, c1, c2 copy P's tail once each
     assert torch.equal(kd.cpu(), kh) and torch.equal(vd.cpu(), vh)
     assert pa.last_device_error() == 0

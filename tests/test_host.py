@@ -257,6 +257,39 @@ def test_fork_copy_on_write_and_swap():
     assert (list(pool.free_queue), dict(pool.tables)) == before
 
 
+def test_append_step_follows_the_append_rule():
+    """A decode step's appends: a full tail takes a fresh block, a shared
+    partly filled tail is copied first (one copy for the first of its
+    sharers; the last sharer then owns it alone), a private tail is written
+    in place; all or nothing when the pool runs short."""
+    pool = BlockPool(10, 4, free_order=range(10))
+    pool.add("A", 6)                                   # [0, 1]: tail 1 half full
+    pool.fork("A", "B")                                # shares 0 and 1
+    pool.add("C", 8)                                   # [2, 3]: tail full
+    pool.add("D", 2)                                   # [4]: private, half full
+    pairs = pool.append_step(["A", "B", "C", "D"])
+    assert pairs == [(1, 5)]                           # A copies the shared tail
+    assert pool.tables["A"] == [0, 5] and pool.tables["B"] == [0, 1]
+    assert pool.ref_cnt[1] == 1 and pool.ref_cnt[5] == 1
+    assert pool.tables["C"] == [2, 3, 6] and pool.tables["D"] == [4]
+    assert [pool.lengths[s] for s in "ABCD"] == [7, 7, 9, 3]
+    # the new positions' slots are where pa_decode_append writes
+    assert pool.slot("A", 6) == 5 * 4 + 2 and pool.slot("C", 8) == 6 * 4
+    # all or nothing: one block left, a step that needs two changes nothing
+    assert pool.num_free == 3
+    pool.add("E", 4)                                   # block 7, full
+    pool.add("F", 4)                                   # block 8, full
+    before = (list(pool.free_queue), {k: list(v) for k, v in pool.tables.items()},
+              dict(pool.lengths), list(pool.ref_cnt))
+    with pytest.raises(MemoryError):
+        pool.append_step(["A", "E", "F"])              # A in place, E and F a block each
+    assert (list(pool.free_queue), {k: list(v) for k, v in pool.tables.items()},
+            dict(pool.lengths), list(pool.ref_cnt)) == before
+    assert pool.append_step(["A", "E"]) == [] and pool.tables["E"] == [7, 9]
+    with pytest.raises(ValueError):
+        pool.append_step(["A", "A"])
+
+
 def test_positions_give_the_slot_mapping():
     """Every workload's (seq_id, position) per new token maps, through the
     oracle's addressing, to the slot mapping the host pool produced."""
