@@ -263,7 +263,9 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
     } else if (warp == C::kMmaWarp) {
         // ---- MMA issue -----------------------------------------------------
         constexpr uint32_t kIdS = umma_idesc_bf16(128, C::kKeys, 0);
-        constexpr uint32_t kIdO = umma_idesc_bf16(128, D, 1);
+        // P V produces the head dim's columns only (N = hd, a multiple of 16):
+        // in the 128-column tile of head dims 80-112 the rest of V is zeros
+        const uint32_t kIdO = umma_idesc_bf16(128, hd, 1);
         // Descriptors of step 0; a step adds its byte offset / 16 to the start
         // address field (addresses stay below 2^18, so the field never carries).
         uint64_t qdesc[C::kTiles];
