@@ -348,9 +348,9 @@ pa_status pa_decode_shared_prefix(const void* q, const void* k_cache, const void
  * query_start_loc  device or pinned int32 [num_seqs + 1], non-decreasing, last = total_q.
  * max_q_len        host upper bound of L_i (sizes the grid).
  * Other arguments as pa_decode.  L_i > T_i is reported (PA_DEVERR_SEQ_LEN)
- * and that sequence's rows are left untouched.  bf16 with head_dim 64, 80, 96,
- * 112 or 128 (the last three in a 128-column tile whose extra columns are zero),
- * block_size 8 or a multiple of 16, a group size of at most 128 and scale >= 0
+ * and that sequence's rows are left untouched.  bf16 with head_dim a multiple
+ * of 16 up to 128 (16-48 in a 64-column tile, 80-112 in a 128-column tile,
+ * whose extra columns are zero), block_size 8 or a multiple of 16, a group size of at most 128 and scale >= 0
  * runs on the TMA + tcgen05 kernel (tensor-memory accumulators); other valid
  * shapes (head_dim <= 256) and scales on a warp-level tensor-core kernel
  * (bf16, head_dim a multiple of 16, 16-byte aligned q and caches), else on

@@ -941,8 +941,8 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     constexpr int32_t kTilesPerCta = 2;
     a.scale_log2 = scale * kLog2e;
     // the tensor-core kernel takes its row maximum before scaling: scale >= 0
-    // (head dims 80-112 run in a 128-column tile whose columns past the head
-    // dim are zeros)
+    // (head dims 16-48 run in a 64-column tile, 80-112 in a 128-column one,
+    // whose columns past the head dim are zeros)
     const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) && aligned(out, 16) &&
                       aligned(k_cache, 16) && aligned(v_cache, 16) && scale >= 0.f;
     cudaError_t err;

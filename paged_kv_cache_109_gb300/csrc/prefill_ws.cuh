@@ -154,8 +154,9 @@ prefill_ws_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // rows past tpt * G (G not dividing 128) carry nothing: no Q, no output
     const bool row_ok = softmax && r < tpt * G && tok < ntok;
     const int32_t pos = pos0 + min(tok, ntok - 1);
-    // the head dim; the tile is D columns (head dims 80-112 in a 128-column
-    // tile: the columns past hd are zeros in Q, K and V and never stored)
+    // the head dim; the tile is D columns (head dims 16-48 in a 64-column
+    // tile, 80-112 in a 128-column one: the columns past hd are zeros in Q,
+    // K and V and never stored)
     const int32_t hd = a.head_dim;
     const int64_t row_elem = ((int64_t)(q0 + tok0 + tok) * a.num_q_heads + g * G + head) * hd;
     if (softmax) {

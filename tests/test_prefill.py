@@ -70,6 +70,9 @@ FAST = [
     (32, 32, 80, 16, (70, 129), (70, 33)),                        # D=80, MHA
     (64, 8, 112, 32, (257, 40), (100, 40)),                       # D=112, G=8, B=32
     (40, 8, 96, 8, (150, 3), (150, 3)),                           # D=96, G=5, B=8
+    (32, 8, 48, 16, (300, 17, 1000), (300, 5, 100)),              # D=48 in a 64-column tile
+    (16, 4, 32, 32, (257, 40), (100, 40)),                        # D=32, B=32
+    (8, 8, 16, 8, (45, 200), (45, 31)),                           # D=16, MHA, B=8
 ]
 
 
