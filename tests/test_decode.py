@@ -591,3 +591,61 @@ def test_million_token_sequences(cuda_device):
         out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=p)
         assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, f"million tokens, {p}")
     assert pa.last_device_error() == 0
+
+
+# ---- the launch's limits ------------------------------------------------------------
+
+def test_most_sequences_one_call_takes(cuda_device):
+    """65535 sequences (the grid's z limit) of 1 to 40 tokens, through
+    pa_decode and pa_decode_append, against the oracle on every output; one
+    more is refused before launch."""
+    n = 65535
+    rng = np.random.default_rng(65535)
+    lens = rng.integers(1, 41, size=n).tolist()
+    q, kc, vc, bt, sl = synthetic(2, 1, 64, 16, lens, seed=65)
+    scale = 1 / math.sqrt(64)
+    out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale)
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "65535 sequences")
+    dev = cuda_device
+    g = torch.Generator().manual_seed(66)
+    k_new = torch.randn(n, 1, 64, generator=g).to(torch.bfloat16)
+    v_new = torch.randn(n, 1, 64, generator=g).to(torch.bfloat16)
+    kd, vd = kc.to(dev), vc.to(dev)
+    out2 = pa.decode_append(q.to(dev), k_new.to(dev), v_new.to(dev), kd, vd, bt.to(dev),
+                            sl.to(dev), 40, scale)
+    torch.cuda.synchronize()
+    slots = torch.from_numpy(oracle.slots_from_positions(torch.arange(n, dtype=torch.int32),
+                                                         sl - 1, bt, 16))
+    kh, vh = kc.clone(), vc.clone()
+    oracle.write_kv(k_new, v_new, slots, kh, vh)
+    assert torch.equal(kd.cpu(), kh) and torch.equal(vd.cpu(), vh)
+    ref2 = oracle.decode(q, kh, vh, bt, sl, scale)
+    assert_close(out2.cpu().double().numpy(), ref2, BF16_ATOL, BF16_RTOL, "65535 appends")
+    assert pa.last_device_error() == 0
+    q1 = torch.zeros(n + 1, 2, 64, dtype=torch.bfloat16, device=dev)
+    bt1 = torch.zeros(n + 1, bt.shape[1], dtype=torch.int32, device=dev)
+    sl1 = torch.ones(n + 1, dtype=torch.int32, device=dev)
+    with pytest.raises(pa.PaError) as e:
+        pa.decode(q1, kd, vd, bt1, sl1, 40, scale)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
+
+
+def test_most_partitions_one_sequence_takes(cuda_device):
+    """One sequence of 16 * 65535 tokens in 16-token partitions: 65535
+    partials per head, the most a call takes, merged against the oracle; a
+    bound of one more partition is refused before launch."""
+    T = 16 * 65535
+    q, kc, vc, bt, sl = synthetic(8, 1, 64, 16, (T, 3), seed=67)
+    scale = 1 / math.sqrt(64)
+    out = gpu_decode(cuda_device, q, kc, vc, bt, sl, scale, partition_tokens=16)
+    ref = oracle.decode(q, kc, vc, bt, sl, scale)
+    assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "65535 partitions")
+    assert pa.last_device_error() == 0
+    dev = cuda_device
+    wide = torch.full((2, bt.shape[1] + 1), -1, dtype=torch.int32)
+    wide[:, :bt.shape[1]] = bt
+    with pytest.raises(pa.PaError) as e:
+        pa.decode(q.to(dev), kc.to(dev), vc.to(dev), wide.to(dev), sl.to(dev), T + 16, scale,
+                  partition_tokens=16)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
