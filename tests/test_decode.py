@@ -352,6 +352,24 @@ def test_zero_length_sequences(cuda_device):
     assert_close(out.double().numpy(), ref, BF16_ATOL, BF16_RTOL, "zero-length")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_batch_of_empty_sequences(cuda_device, dtype):
+    """Every length 0 (a host bound of 0): zero rows from pa_decode and
+    pa_decode_append, no cache row written, nothing reported."""
+    q, kc, vc, bt, sl = synthetic(8, 2, 64, 16, (0, 0, 0), dtype=dtype, seed=9)
+    dev = cuda_device
+    q = q + 1                                          # nonzero queries
+    out = gpu_decode(dev, q, kc, vc, bt, sl, 0.125)
+    assert out.shape == q.shape and not out.any()
+    kd, vd = kc.to(dev), vc.to(dev)
+    k_new = torch.ones(3, 2, 64, dtype=dtype, device=dev)
+    out2 = pa.decode_append(q.to(dev), k_new, k_new, kd, vd, bt.to(dev), sl.to(dev), 0, 0.125)
+    torch.cuda.synchronize()
+    assert not out2.any()
+    assert torch.equal(kd.cpu(), kc) and torch.equal(vd.cpu(), vc)
+    assert pa.last_device_error() == 0
+
+
 # ---- device-side bounds checks (host-planted bad inputs; nothing faults) --------
 
 def test_bad_table_entry_is_reported_not_faulting(cuda_device):
