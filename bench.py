@@ -1059,6 +1059,10 @@ def overrides(args) -> dict:
         out["num_seqs"] = args.num_seqs
         if args.workload == "gqa":
             out["num_shared"] = max(1, args.num_seqs // 4)
+    if args.prefix_len:
+        out["prefix_len"] = args.prefix_len
+    if args.num_shared:
+        out["num_shared"] = args.num_shared
     if args.num_blocks:
         out["num_blocks"] = args.num_blocks
     if args.dtype == "f32":
@@ -1134,6 +1138,10 @@ def make_parser() -> argparse.ArgumentParser:
     ap.add_argument("--num-blocks", type=int, default=0, help="smaller block pool (profiling)")
     ap.add_argument("--block-size", type=int, default=0,
                     help="block-size sweep: tokens per block (pool bytes kept constant)")
+    ap.add_argument("--prefix-len", type=int, default=0,
+                    help="gqa: tokens of the shared prefix (whole blocks; 512 by default)")
+    ap.add_argument("--num-shared", type=int, default=0,
+                    help="gqa: sequences that share the prefix (32 by default)")
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="decode a workload with shared-prefix groups (gqa) with the plain "
                          "pa_decode instead of pa_decode_shared_prefix")
@@ -1161,6 +1169,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.workload in ("copy", "swap", "prefill") and (args.dtype != "bf16" or args.head_dim):
         ap.error("--dtype and --head-dim apply to the decode workloads")
+    if args.workload != "gqa" and (args.prefix_len or args.num_shared):
+        ap.error("--prefix-len and --num-shared apply to the gqa workload")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
