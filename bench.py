@@ -1059,9 +1059,9 @@ def overrides(args) -> dict:
         out["num_seqs"] = args.num_seqs
         if args.workload == "gqa":
             out["num_shared"] = max(1, args.num_seqs // 4)
-    if args.prefix_len:
+    if getattr(args, "prefix_len", 0):
         out["prefix_len"] = args.prefix_len
-    if args.num_shared:
+    if getattr(args, "num_shared", 0):
         out["num_shared"] = args.num_shared
     if args.num_blocks:
         out["num_blocks"] = args.num_blocks

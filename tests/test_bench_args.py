@@ -14,7 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _ns(**kw):
-    base = dict(num_seqs=0, num_blocks=0, block_size=0, dtype="bf16", head_dim=0, workload="mha")
+    base = dict(num_seqs=0, num_blocks=0, block_size=0, dtype="bf16", head_dim=0, workload="mha",
+                prefix_len=0, num_shared=0)
     base.update(kw)
     return argparse.Namespace(**base)
 
@@ -27,6 +28,12 @@ def test_overrides_reach_the_workload_and_the_json_line():
     assert json.loads(json.dumps(bench.overrides_json(ns))) == {
         "num_seqs": 4, "num_shared": 1, "dtype": "f32", "head_dim": 96}
     assert bench.overrides(_ns()) == {}
+    # the shared-prefix size of the gqa batch
+    ov = bench.overrides(_ns(workload="gqa", prefix_len=4096, num_shared=64))
+    assert ov == {"prefix_len": 4096, "num_shared": 64}
+    from paged_kv_cache_109_gb300 import workloads
+    wl = workloads.make("gqa", num_seqs=16, num_blocks=8192, **ov | {"num_shared": 8})
+    assert wl.prefix_groups[0][1] == 4096 // wl.block_size
 
 
 def test_block_size_sweep_keeps_pool_bytes():
