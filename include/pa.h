@@ -368,7 +368,8 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
 
 /*
  * Which decode kernel these arguments select: 1 = the TMA + tensor-core
- * kernel (bf16, head_dim a multiple of 16 up to 128, block_size 8 or a multiple
+ * kernel (bf16, head_dim a multiple of 16 up to 128, or 256 with groups of
+ * two or more query heads per kv head, block_size 8 or a multiple
  * of 16 up to 256, any group size: a group of more than 16 query heads is
  * split into CTAs of 16 that read the same K/V tiles), 2 = the warp-level tensor-core
  * kernel (bf16, head_dim a multiple of 16 up to 128 that kernel 1 does not

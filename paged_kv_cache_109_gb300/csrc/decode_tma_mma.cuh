@@ -67,7 +67,7 @@ struct TmaMmaCfg {
     static constexpr int kKSteps = D / 16;
     static constexpr int kDTiles = D / 8;
     static constexpr int kMaxTableSlice = 2048;            // block ids per partition
-    static_assert(D % 16 == 0 && D <= 128, "tile shape");
+    static_assert(D % 16 == 0 && D <= 256, "tile shape");
     static_assert(kWarps * kRows * (D + 2) * 4 <= kRingBytes, "combine area");
     // dynamic shared bytes for a partition of part_tokens tokens
     static size_t smem_bytes(int32_t part_tokens, int32_t block_size) {
@@ -78,8 +78,11 @@ struct TmaMmaCfg {
     static size_t smem_bytes_max() { return smem_bytes(kMaxTableSlice, 1); }
 };
 
+// Head dim 256 holds a 256-column accumulator and 16 k-steps of Q in
+// registers: one CTA per SM (up to 255 registers a thread), two 16 KiB
+// stages per warp.
 template <int D, bool G16, bool CAS>
-__global__ void __launch_bounds__(128, PA_MIN_CTAS_PER_SM)
+__global__ void __launch_bounds__(128, D > 128 ? 1 : PA_MIN_CTAS_PER_SM)
 decode_tma_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
     using C = TmaMmaCfg<D, G16>;

@@ -310,6 +310,7 @@ cudaError_t dispatch_fast_cas(dim3 grid, const CUtensorMap& mk, const CUtensorMa
             case 80: return launch_fast_d<80, false>(grid, mk, mv, a, st);
             case 96: return launch_fast_d<96, false>(grid, mk, mv, a, st);
             case 112: return launch_fast_d<112, false>(grid, mk, mv, a, st);
+            case 256: return launch_fast_d<256, false>(grid, mk, mv, a, st);
             default: break;
         }
     }
@@ -544,7 +545,9 @@ pa_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                    !aligned(v_new, elem_bytes(cache)) || !map_step_arg(k_new) ||
                    !map_step_arg(v_new)))
         return PA_ERR_INVALID_ARG;
-    const bool fused = append && fast && aligned(k_new, 16) && aligned(v_new, 16);
+    // (the kernel's row patch covers 128 columns: head dim 256 writes first)
+    const bool fused = append && fast && cache->head_dim <= 128 && aligned(k_new, 16) &&
+                       aligned(v_new, 16);
     // shared-prefix decode on the TMA kernel: workspace slots for the
     // groups' prefix partitions in front of each member's own
     const bool cas = sh != nullptr && fast &&
@@ -943,8 +946,9 @@ pa_status pa_prefill(const void* q, const int32_t* query_start_loc, int32_t tota
     // the tensor-core kernel takes its row maximum before scaling: scale >= 0
     // (head dims 16-48 run in a 64-column tile, 80-112 in a 128-column one,
     // whose columns past the head dim are zeros)
-    const bool fast = path == 1 && a.tokens_per_tile > 0 && aligned(q, 16) && aligned(out, 16) &&
-                      aligned(k_cache, 16) && aligned(v_cache, 16) && scale >= 0.f;
+    const bool fast = path == 1 && cache->head_dim <= 128 && a.tokens_per_tile > 0 &&
+                      aligned(q, 16) && aligned(out, 16) && aligned(k_cache, 16) &&
+                      aligned(v_cache, 16) && scale >= 0.f;
     cudaError_t err;
     if (fast) {
         CUtensorMap mk, mv;

@@ -90,11 +90,12 @@ def sample_pairs(step, num_q_heads, count, seed=0):
 
 def decode_kernel(dtype, d, bs, group):
     """The decode kernel pa_decode_path names for a shape: 1 TMA + tensor
-    cores (bf16 head dims that are multiples of 16 up to 128 at block sizes 8
-    and multiples of 16), 2 mma.sync (groups of 5 or more heads on those head
-    dims at other block sizes), 0 CUDA cores (fp32 and the rest)."""
-    if dtype == torch.bfloat16 and d % 16 == 0 and 16 <= d <= 128 and \
-            (bs == 8 or (bs % 16 == 0 and bs <= 256)):
+    cores (bf16 head dims that are multiples of 16 up to 128, and 256 with
+    groups of two or more, at block sizes 8 and multiples of 16), 2 mma.sync
+    (groups of 5 or more heads on the head dims up to 128 at other block
+    sizes), 0 CUDA cores (fp32 and the rest)."""
+    tma_d = (d % 16 == 0 and 16 <= d <= 128) or (d == 256 and group >= 2)
+    if dtype == torch.bfloat16 and tma_d and (bs == 8 or (bs % 16 == 0 and bs <= 256)):
         return 1
     if dtype == torch.bfloat16 and d % 16 == 0 and d <= 128 and group >= 5:
         return 2

@@ -73,7 +73,9 @@ def test_path_selection(lib):
     assert path(64, desc(d=48, bs=24)) == 2            # D=48 at a block size TMA does not take
     assert path(32, desc(d=96, bs=24)) == 0            # G=4: CUDA cores
     assert path(64, desc(d=40)) == 0                   # not a multiple of 16: CUDA cores
-    assert path(64, desc(d=256)) == 0                  # over 128: CUDA cores
+    assert path(64, desc(d=256)) == 1                  # D=256, G=8: four boxes, one CTA a SM
+    assert path(8, desc(d=256)) == 0                   # D=256, G=1: CUDA cores
+    assert path(64, desc(d=192)) == 0                  # other head dims over 128: CUDA cores
     assert path(16, desc(d=64, bs=64, hkv=4)) == 1
     assert path(8, desc(d=8, bs=4, hkv=2, dtype=pa.PA_F32)) == 0
     assert path(30, desc()) == -1                      # Hq not a multiple of Hkv

@@ -111,6 +111,10 @@ FAST_CASES = [
     (32, 8, 32, 8, (1, 7, 8, 9, 300)),                             # D=32, B=8
     (8, 8, 32, 64, (63, 64, 65, 500)),                             # D=32 MHA, B=64
     (48, 2, 16, 16, (5, 333)),                                     # D=16, G=24: sub-groups
+    (32, 8, 256, 16, (1, 15, 16, 17, 300, 2049)),                  # D=256: four boxes, G=4
+    (64, 8, 256, 32, (33, 700, 4000)),                             # D=256, G=8, B=32
+    (16, 8, 256, 8, (9, 300)),                                     # D=256, G=2, B=8
+    (32, 1, 256, 16, (100, 1, 900)),                               # D=256, G=32: sub-groups
 ]
 
 

@@ -20,7 +20,7 @@ BLOCK_SIZES = (8, 16, 32, 48, 64, 128)
 def _case(rng, prefill=False):
     hkv = int(rng.choice([1, 2, 4, 8]))
     g = int(rng.choice([1, 2, 3, 4, 5, 8, 16, 24, 32]))
-    d = int(rng.choice([16, 32, 48, 64, 80, 96, 112, 128]))
+    d = int(rng.choice([16, 32, 48, 64, 80, 96, 112, 128, 256]))
     bs = int(rng.choice(BLOCK_SIZES))
     n = int(rng.integers(1, 7))
     lens = rng.integers(0 if not prefill else 1, 700, size=n)
