@@ -226,8 +226,8 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * the output are bit for bit those of pa_write_kv_positions(k_new, v_new,
  * seq_ids = 0 .. num_seqs - 1, positions = T_i - 1) followed by pa_decode.
  *
- * On the TMA decode kernel (pa_decode_path 1, k_new and v_new 16-byte
- * aligned) the write is fused into the decode: the CTA whose partition holds
+ * On the TMA decode kernel (pa_decode_path 1, head_dim up to 128, k_new and
+ * v_new 16-byte aligned) the write is fused into the decode: the CTA whose partition holds
  * position T_i - 1 attends to the new rows in place of the slot's old
  * contents and stores them, so the step is one launch shorter.  Otherwise
  * the cache write (slots from the lengths and tables) runs first, then the
